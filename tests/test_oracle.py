@@ -1,0 +1,294 @@
+"""Pins for the CPU oracle (no GPU).
+
+Each test ties the oracle to something other than itself: hand-derived
+golden values, closed forms, brute force in plain Python, invariants of the
+fixed grid, or an fp64 library matmul.  A plausible slip anywhere in the
+oracle (a wrong nibble or byte position, a dropped scale, a transposed
+operand, a wrong offset, round-half-up instead of half-even, a wrong clamp)
+fails at least one of them; tests/test_oracle_mutants.py checks that claim
+by compiling planted mistakes into the oracle.
+"""
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(name):
+    with open(os.path.join(GOLD, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                yield line.split()
+
+
+# ------------------------------------------------------------ P-h storage ---
+def test_storage_accounting_matches_printed_sizes():
+    """Packed bytes per weight (bits/8) plus one bf16 scale per 128-group
+    reproduce the W8A16 card's 1.00 GB -> 521 MB within the fixture's bound."""
+    kv = {k: float(v) for k, v in _rows("storage_accounting.txt")}
+    K, N = 2560, 9728
+    for bits in (4, 8):
+        words = oracle.packed_words(bits, K, N)
+        assert words * 4 == K * N * bits // 8
+    per_weight_w8 = 1 + 2 / 128
+    predicted = kv["params"] * per_weight_w8 / (kv["params"] * 2)
+    printed = kv["w8a16_bytes_printed"] / kv["bf16_bytes_printed"]
+    assert abs(predicted - printed) / printed < kv["ratio_tolerance"]
+    # bf16 size of the parameters is the printed "1.00 GB" (GiB-ish units)
+    assert abs(kv["params"] * 2 / 2**30 - 1.0) < 0.01
+
+
+# -------------------------------------------------------- RTN scale pins ---
+def test_rtn_scales_golden():
+    for bits, amax, want in _rows("rtn_scales.txt"):
+        bits, amax, want = int(bits), float(amax), int(want, 16)
+        W = np.zeros((128, 64), dtype=np.float32)
+        W[5, 3] = amax
+        W[77, 3] = -amax / 2
+        s = oracle.rtn_scales(W, bits)
+        assert s[0, 3] == want, (bits, amax, hex(s[0, 3]))
+        # columns with absmax 0 get scale 1.0
+        assert s[0, 0] == 0x3F80
+
+
+def test_rtn_negative_absmax_and_code_extremes():
+    """absmax is taken over |w|: a group whose largest magnitude is negative
+    gets the same scale, and RTN codes reach exactly -qpos .. qpos."""
+    for bits, qpos in ((4, 7), (8, 127)):
+        W = np.zeros((256, 64), dtype=np.float32)
+        W[3, 0], W[9, 0] = -1.0, 0.25
+        W[130, 1], W[200, 1] = 1.0, -0.5
+        s = oracle.rtn_scales(W, bits)
+        assert s[0, 0] == s[1, 1]
+        q = oracle.quantize(W, s, bits)
+        assert q[3, 0] == -qpos and q[130, 1] == qpos
+
+
+# ---------------------------------------------------------- P-c rounding ---
+def test_rounding_ties_and_clamp_golden():
+    for bits, sb, w, want in _rows("rounding.txt"):
+        bits, sb, w, want = int(bits), int(sb, 16), float(w), int(want)
+        W = np.zeros((128, 64), dtype=np.float32)
+        W[17, 9] = w
+        s = np.full((1, 64), sb, dtype=np.uint16)
+        q = oracle.quantize(W, s, bits)
+        assert q[17, 9] == want, (bits, hex(sb), w, q[17, 9])
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_codes_stay_in_range(bits):
+    rng = np.random.default_rng(7)
+    lo, hi = (-8, 7) if bits == 4 else (-128, 127)
+    for scale in (1e-30, 1e-3, 1.0, 1e3, 1e30):
+        W = (rng.standard_normal((256, 128)) * scale).astype(np.float32)
+        W[0, :] = np.float32(scale * 50)  # outliers
+        packed, s, q = oracle.pack_symmetric(W, bits)
+        assert q.min() >= lo and q.max() <= hi
+        # RTN codes never use the extra negative code
+        assert q.min() >= -hi
+        # supplied (too small) scales clamp
+        s_small = np.full_like(s, 0x0080)  # smallest normal bf16
+        q2 = oracle.quantize(W, s_small, bits)
+        assert q2.min() >= lo and q2.max() <= hi
+
+
+# ------------------------------------------------------- P-a round trip ---
+@pytest.mark.parametrize("bits", [4, 8])
+def test_pack_unpack_round_trip(bits):
+    lo, hi = (-8, 7) if bits == 4 else (-128, 127)
+    rng = np.random.default_rng(bits)
+    for K, N in ((128, 64), (256, 192), (384, 128)):
+        q = rng.integers(lo, hi + 1, size=(K, N)).astype(np.int8)
+        p = oracle.pack(q, bits)
+        assert p.size * 32 == K * N * bits
+        assert np.array_equal(oracle.unpack(p, K, N, bits), q)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_every_value_at_every_position(bits):
+    """Brute force: every code value at every slot position survives."""
+    lo, hi = (-8, 7) if bits == 4 else (-128, 127)
+    K, N = 128, 64
+    idx = np.arange(K * N).reshape(K, N)
+    for v in range(hi - lo + 1):
+        q = (((idx + v) % (hi - lo + 1)) + lo).astype(np.int8)
+        assert np.array_equal(oracle.unpack(oracle.pack(q, bits), K, N, bits), q)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_layout_is_a_bijection(bits):
+    """Read every field of every packed word directly (no layout formula):
+    the element indices stored there, written in base-16 (or base-256)
+    digit planes, must be a permutation of all elements."""
+    K, N = 256, 128
+    width = bits
+    mask = (1 << width) - 1
+    off = 8 if bits == 4 else 128
+    idx = np.arange(K * N, dtype=np.int64).reshape(K, N)
+    nplanes = int(np.ceil(np.log2(K * N) / width))
+    recovered = None
+    fields = 32 // width
+    for p in range(nplanes):
+        digit = (idx >> (width * p)) & mask
+        packed = oracle.pack((digit - off).astype(np.int8), bits)
+        vals = np.stack([(packed >> (width * f)) & mask for f in range(fields)],
+                        axis=1).astype(np.int64).ravel()
+        recovered = vals << (width * p) if recovered is None else \
+            recovered | (vals << (width * p))
+    assert np.array_equal(np.sort(recovered), np.arange(K * N))
+
+
+def test_layout_positions_golden():
+    for bits, K, N, k, n, w, sh in _rows("layout_positions.txt"):
+        bits, K, N, k, n, w, sh = map(int, (bits, K, N, k, n, w, sh))
+        lo = -8 if bits == 4 else -128
+        q = np.full((K, N), lo, dtype=np.int8)  # stored field value 0
+        q[k, n] = lo + 1                          # stored field value 1
+        p = oracle.pack(q, bits)
+        nz = np.flatnonzero(p)
+        assert list(nz) == [w], (bits, k, n, nz[:4])
+        assert int(p[w]) == 1 << sh, (bits, k, n, hex(int(p[w])))
+
+
+# --------------------------------------------------- P-b grid idempotence ---
+@pytest.mark.parametrize("bits", [4, 8])
+def test_fixed_grid_idempotence(bits):
+    """s*q is exact in fp32, so re-rounding it with the same s returns q."""
+    rng = np.random.default_rng(11)
+    lo, hi = (-8, 7) if bits == 4 else (-128, 127)
+    K, N = 512, 128
+    q = rng.integers(lo, hi + 1, size=(K, N)).astype(np.int8)
+    # random bf16 scales over many binades, including subnormal-free tiny ones
+    sf = np.exp(rng.uniform(np.log(1e-6), np.log(1e3), size=(K // 128, N)))
+    s = oracle.f32_to_bf16_bits(sf.astype(np.float32))
+    sv = oracle.bf16_bits_to_f32(s).astype(np.float64)
+    W64 = np.repeat(sv, 128, axis=0) * q.astype(np.float64)
+    W = W64.astype(np.float32)
+    assert np.array_equal(W.astype(np.float64), W64)  # exactness of s*q
+    packed, s_out, q_out = oracle.pack_symmetric(W, bits, scales_in=s)
+    assert np.array_equal(q_out, q)
+    assert np.array_equal(s_out, s)
+    assert np.array_equal(oracle.unpack(packed, K, N, bits), q)
+    # and re-packing the dequantized weights is a fixed point
+    W2 = oracle.dequant(q_out, s_out)
+    assert np.array_equal(W2, W)
+
+
+# ----------------------------------------------------------- P-g s = 1 ---
+def test_unit_scale_dequant_is_the_codes():
+    K, N = 256, 64
+    q = np.empty((K, N), dtype=np.int8)
+    for k in range(K):          # hand enumeration of all codes
+        for n in range(N):
+            q[k, n] = ((k * 7 + n * 3) % 16) - 8
+    s = np.full((K // 128, N), 0x3F80, dtype=np.uint16)
+    W = oracle.dequant(q, s)
+    assert np.array_equal(W, q.astype(np.float32))
+
+
+# ------------------------------------------------------ P-d identity probe ---
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("K", [128, 256])
+def test_identity_probe_recovers_weights(bits, K):
+    """Running the identity through the quantized product gives back the
+    effective dense weight (the identity-probe of the W8A16 card's fused-KV
+    patch, site 2)."""
+    X, q, s = synth.small_case(K, K, 64, bits, seed=K + bits)
+    eye = np.zeros((K, K), dtype=np.float32)
+    np.fill_diagonal(eye, 1.0)
+    X = oracle.f32_to_bf16_bits(eye)
+    packed = oracle.pack(q, bits)
+    Y = oracle.gemm(X, packed, s, K, 64, bits)
+    sv = oracle.bf16_bits_to_f32(s).astype(np.float64)
+    expect = np.repeat(sv, 128, axis=0) * q.astype(np.float64)
+    assert np.array_equal(Y, expect)
+
+
+# --------------------------------------------- P-e exact integer brute force ---
+@pytest.mark.parametrize("bits", [4, 8])
+def test_exact_bruteforce_power_of_two_scales(bits):
+    """Tiny shape, powers-of-two scales, small integer activations: compare
+    the oracle with a pure-Python exact-rational triple loop."""
+    rng = np.random.default_rng(3 + bits)
+    M, K, N = 3, 256, 64
+    lo, hi = (-8, 7) if bits == 4 else (-128, 127)
+    q = rng.integers(lo, hi + 1, size=(K, N)).astype(np.int8)
+    e = rng.integers(-6, 3, size=(K // 128, N))
+    s = oracle.f32_to_bf16_bits((2.0 ** e).astype(np.float32))
+    Xi = rng.integers(-4, 5, size=(M, K))
+    X = oracle.f32_to_bf16_bits(Xi.astype(np.float32))
+    Y = oracle.gemm(X, oracle.pack(q, bits), s, K, N, bits)
+    for m in range(M):
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                acc += Fraction(int(Xi[m, k])) * Fraction(2) ** int(e[k // 128, n]) \
+                    * int(q[k, n])
+            assert Fraction(Y[m, n]) == acc, (m, n)
+
+
+def test_scale_row_selection_bruteforce():
+    """Distinct scale per group and per column: a wrong group index or a
+    transposed scale tensor is caught."""
+    M, K, N = 2, 384, 64
+    q = np.ones((K, N), dtype=np.int8)
+    e = np.arange(K // 128)[:, None] * 2 + (np.arange(N)[None, :] % 5)
+    s = oracle.f32_to_bf16_bits((2.0 ** e).astype(np.float32))
+    X = oracle.f32_to_bf16_bits(np.ones((M, K), dtype=np.float32))
+    Y = oracle.gemm(X, oracle.pack(q, 4), s, K, N, 4)
+    for n in range(N):
+        want = sum(128 * 2.0 ** int(e[g, n]) for g in range(K // 128))
+        assert Y[0, n] == want and Y[1, n] == want
+
+
+# -------------------------------------------------- P-f on-grid agreement ---
+@pytest.mark.parametrize("bits", [4, 8])
+def test_on_grid_weights_match_fp64_matmul(bits):
+    """Weights already on the grid: quantization is lossless, so the oracle
+    equals an fp64 library matmul of X and W (up to fp64 summation order)."""
+    X, q, s = synth.small_case(5, 384, 192, bits, seed=21)
+    sv = oracle.bf16_bits_to_f32(s).astype(np.float64)
+    W = (np.repeat(sv, 128, axis=0) * q).astype(np.float32)
+    packed, s2, q2 = oracle.pack_symmetric(W, bits, scales_in=s)
+    Y = oracle.gemm(X, packed, s2, 384, 192, bits)
+    Xf = oracle.bf16_bits_to_f32(X).astype(np.float64)
+    ref = Xf @ W.astype(np.float64)
+    assert np.max(np.abs(Y - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
+def test_gemm_row_subset_and_threads_agree():
+    X, q, s = synth.small_case(9, 256, 128, 4, seed=5)
+    p = oracle.pack(q, 4)
+    full = oracle.gemm(X, p, s, 256, 128, 4, nthreads=1)
+    sub = oracle.gemm(X, p, s, 256, 128, 4, rows=[8, 0, 3], nthreads=3)
+    assert np.array_equal(sub, full[[8, 0, 3]])
+    assert oracle.gemm(X, p, s, 256, 128, 4, rows=[]).shape == (0, 128)
+
+
+def test_bf16_rounding_helpers():
+    vals = np.array([1.0, 1.00390625, 1.01171875, -2.5, 3e38, 1e-40],
+                    dtype=np.float32)
+    # 1.00390625 = 1 + 2^-8 is a tie between 1 and 1 + 2^-7 -> even (1.0);
+    # 1.01171875 = 1 + 3*2^-8 is a tie between 1+2^-7 and 1+2^-6 -> 1+2^-6
+    want = np.array([0x3F80, 0x3F80, 0x3F82, 0xC020, 0x7F62, 0x0001],
+                    dtype=np.uint16)
+    got = oracle.f32_to_bf16_bits(vals)
+    assert np.array_equal(got, want), [hex(int(x)) for x in got]
+    assert np.array_equal(oracle.bf16_bits_to_f32(want[:4]),
+                          np.array([1.0, 1.0, 1.015625, -2.5], np.float32))
+
+
+def test_shape_checks():
+    with pytest.raises(ValueError):
+        oracle.pack(np.zeros((100, 64), np.int8), 4)
+    with pytest.raises(ValueError):
+        oracle.pack(np.zeros((128, 48), np.int8), 4)
+    with pytest.raises(ValueError):
+        oracle.rtn_scales(np.zeros((128, 64), np.float32), 4, group=64)
