@@ -130,11 +130,12 @@ void wqo_widen_bf16(const uint16_t* Wh, int64_t count, float* W_out) {
  *   lane = 4*c + t4
  * INT4 (4 words per lane per (slab, group)):
  *   word  = kb,  nibble = r/2 + 4*(r%2),  stored value u = q + 8
- * INT8 (8 words per lane per (slab, group)):
+ * INT8 (8 words per lane per (slab, group), stored as two halves of 4):
  *   word  = 2*kb + r/4,  byte = (r%4)/2 + 2*((r%4)%2),  u = q + 128
  * Linear word index:
- *   (((nt * (K/128) + g) * 8 + j8) * 32 + lane) * WPL + word,
- *   WPL = 4 (INT4) or 8 (INT8).
+ *   INT4: (((nt * (K/128) + g) * 8 + j8) * 32 + lane) * 4 + word
+ *   INT8: ((((nt * (K/128) + g) * 8 + j8) * 2 + word/4) * 32 + lane) * 4
+ *         + word%4
  */
 static int64_t word_index(int64_t k, int64_t n, int64_t K, int bits,
                           int* shift_out) {
@@ -142,17 +143,16 @@ static int64_t word_index(int64_t k, int64_t n, int64_t K, int bits,
   int64_t g = k / 128, kk = k % 128;
   int64_t kb = kk / 32, t4 = (kk % 32) / 8, r = kk % 8;
   int64_t lane = 4 * c + t4;
-  int64_t wpl = (bits == 4) ? 4 : 8;
-  int64_t word;
+  int64_t slab = (nt * (K / 128) + g) * 8 + j8;
   if (bits == 4) {
-    word = kb;
+    int64_t word = kb;
     *shift_out = (int)(4 * (r / 2 + 4 * (r % 2)));
-  } else {
-    int64_t rr = r % 4;
-    word = 2 * kb + r / 4;
-    *shift_out = (int)(8 * (rr / 2 + 2 * (rr % 2)));
+    return (slab * 32 + lane) * 4 + word;
   }
-  return (((nt * (K / 128) + g) * 8 + j8) * 32 + lane) * wpl + word;
+  int64_t rr = r % 4;
+  int64_t word = 2 * kb + r / 4;
+  *shift_out = (int)(8 * (rr / 2 + 2 * (rr % 2)));
+  return ((slab * 2 + word / 4) * 32 + lane) * 4 + word % 4;
 }
 
 int64_t wqo_packed_words(int bits, int64_t K, int64_t N) {

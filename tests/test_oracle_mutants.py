@@ -28,7 +28,9 @@ MUTANTS = {
                             "bf16_to_f32(s[(k % group) % (K / group) * N + n]) * (float)q[k * N + n]"),
     "fp32 accumulation": ("y[n] += x * (double)wrow[n];", "y[n] = (float)(y[n] + x * (double)wrow[n]);"),
     "X row stride": ("j->X[m * j->K + k]", "j->X[m * j->N + k]"),
-    "group stride": ("(nt * (K / 128) + g)", "(nt + g)"),
+    "group stride": ("(nt * (K / 128) + g) * 8 + j8", "(nt + g) * 8 + j8"),
+    "int8 half split": ("((slab * 2 + word / 4) * 32 + lane) * 4 + word % 4",
+                        "((slab * 2 + word % 2) * 32 + lane) * 4 + word / 2"),
     "bf16 round half up": ("u += 0x7FFFu + lsb;", "u += 0x8000u;"),
 }
 
