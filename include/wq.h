@@ -1,0 +1,172 @@
+/*
+ * wq.h -- C ABI of the GB300 (sm_103a) weight-only quantized GEMM library.
+ *
+ * The operation is the quantized Linear of a weight-only INT4 / INT8 model:
+ *
+ *     Y[M,N] = X[M,K] . dequant(Wq)[K,N],   dequant(Wq)[k,n] = s[k/128,n] * q[k,n]
+ *
+ * with symmetric integer codes q, one bf16 scale per 128-element group along
+ * K, bf16 activations X and output Y, fp32 accumulation.  Sources:
+ *   - "Quantize the Target, Quantize the Drafter: Efficient Inference with
+ *     Qwen3.5-4B" (arXiv 2607.04244 HTML): QAD paragraph (student weights are
+ *     the dequantized s (.) Wq with frozen symmetric per-group scales),
+ *     packing paragraph (round the updated weights back onto the same grid,
+ *     served as W4A16), drafter-PTQ paragraph (group-wise symmetric INT4,
+ *     group size 128).
+ *   - "Qwen3.5-4B-DFlash-W8A16" model card, "What changed vs upstream" table
+ *     (int8 weight-only, RTN, symmetric, group 128) and "Required vLLM
+ *     patches" item 3 (the drafter's qkv projection runs the int8 GEMM).
+ *
+ * Conventions for every entry point
+ *   - All data pointers are DEVICE pointers owned by the caller; the library
+ *     keeps no reference to them after the call returns.
+ *   - Work is enqueued on `stream` and never synchronised; results are
+ *     ready when the stream reaches that point.  Calls on different streams
+ *     may run concurrently.
+ *   - Arguments are checked before anything is launched: a non-OK status
+ *     means nothing was enqueued.  A launch failure returns WQ_ERR_CUDA.
+ *   - Every wait inside a kernel is bounded; a wait that runs out records
+ *     WQ_ERR_DEVICE_TIMEOUT in a per-device error word that
+ *     wq_last_device_error() reads after the caller synchronises.
+ *   - Layouts are row-major and contiguous: X [M,K], Y [M,N], W [K,N],
+ *     scales [K/128, N] (bf16 bit patterns).  A torch Linear weight
+ *     [N,K] is passed transposed.  Pointers must be 16-byte aligned.
+ *   - Shapes: group == 128, K % 128 == 0, N % 64 == 0, M >= 0 (M == 0 is a
+ *     no-op), K*N < 2^40.
+ *
+ * Packed weight layout (tile-interleaved, uint32 words; the pages fix no
+ * layout, this one is the library's own).  Element (k, n):
+ *   nt = n/64, j8 = (n%64)/8, c = n%8, g = k/128, kk = k%128,
+ *   kb = kk/32, t4 = (kk%32)/8, r = kk%8, lane = 4c + t4,
+ *   slab = (nt*(K/128) + g)*8 + j8
+ *   INT4: word index (slab*32 + lane)*4 + kb, nibble r/2 + 4*(r%2),
+ *         field value q + 8
+ *   INT8: w = 2kb + r/4, word index ((slab*2 + w/4)*32 + lane)*4 + w%4,
+ *         byte (r%4)/2 + 2*((r%4)%2), field value q + 128
+ * A 64-column x 128-deep (tile, group) cell is one contiguous 4 KiB (INT4)
+ * or 8 KiB (INT8) block.
+ */
+#ifndef WQ_H_
+#define WQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define WQ_API __attribute__((visibility("default")))
+#else
+#define WQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  WQ_OK = 0,
+  WQ_ERR_NULL = 1,           /* a required pointer is NULL */
+  WQ_ERR_SHAPE = 2,          /* K, N, M or group outside the supported set */
+  WQ_ERR_UNSUPPORTED = 3,    /* bits not 4/8, dtype unknown, no sm_103 GPU */
+  WQ_ERR_ALIGN = 4,          /* a pointer is not 16-byte aligned */
+  WQ_ERR_CUDA = 5,           /* a CUDA runtime call failed */
+  WQ_ERR_DEVICE_TIMEOUT = 6  /* a bounded in-kernel wait ran out */
+} wq_status;
+
+typedef enum { WQ_F32 = 0, WQ_BF16 = 1 } wq_dtype;
+
+/* Number of uint32 words in a packed [K,N] weight with `bits` (4 or 8)
+   bits per code: K*N/8 or K*N/4.  Returns 0 for unsupported arguments. */
+WQ_API size_t wq_packed_words(int bits, int64_t K, int64_t N);
+
+/*
+ * Pack step (one-off per weight, "at packing time" in the packing paragraph
+ * of the paper above; RTN per the W8A16 card's recipe).
+ *   W          [K,N] fp32 or bf16 (wdt), finite values.
+ *   scales_in  bf16 [K/128,N] or NULL.  Given: the grid is fixed and the
+ *              codes are q = clamp(rint(w/s), qmin, qmax) (round half to
+ *              even, IEEE fp32 divide) -- re-rounding onto a frozen grid.
+ *              Values must be positive and finite.  NULL: RTN scales
+ *              s = bf16_rne(absmax_group / qpos), qpos = 7 (INT4) or 127
+ *              (INT8), s = 1 for an all-zero group.
+ *   scales_out bf16 [K/128,N]: the scales used (a copy of scales_in when
+ *              given; may equal scales_in).
+ *   packed     wq_packed_words(bits,K,N) words, layout above.
+ *   [qmin,qmax] = [-8,7] for bits 4, [-128,127] for bits 8.
+ */
+WQ_API wq_status wq_pack_symmetric(const void* W, wq_dtype wdt, int64_t K, int64_t N,
+                            int bits, int group, const uint16_t* scales_in,
+                            uint16_t* scales_out, uint32_t* packed,
+                            cudaStream_t stream);
+
+/* Interleave ready-made int8 codes [K,N] (e.g. from an external GPTQ/AWQ
+   export; each code must lie in [qmin,qmax], other values are wrapped to the
+   field width) into the packed layout. */
+WQ_API wq_status wq_pack_codes(const int8_t* codes, int64_t K, int64_t N, int bits,
+                        uint32_t* packed, cudaStream_t stream);
+
+/* Inverse of the interleave: int8 codes [K,N] from a packed weight. */
+WQ_API wq_status wq_unpack(const uint32_t* packed, int bits, int64_t K, int64_t N,
+                    int8_t* codes, cudaStream_t stream);
+
+/*
+ * W4A16 GEMM (the verifier's quantized Linear): Y = X . dequant(Wp, scales).
+ *   X bf16 [M,K], Wp packed INT4 (bits 4), scales bf16 [K/128,N],
+ *   Y bf16 [M,N] (fp32 accumulation, round to nearest even on store).
+ *   group must be 128.  Y must not overlap X, Wp or scales.
+ * Small M (one speculative block of 16 tokens, a few blocks) runs the
+ * memory-bound kernel; large M (prefill) runs the tensor-core kernel.
+ */
+WQ_API wq_status wq_gemm_w4a16(const void* X, const uint32_t* Wp, const void* scales,
+                        void* Y, int64_t M, int64_t N, int64_t K, int group,
+                        cudaStream_t stream);
+
+/* W8A16 GEMM (the int8 drafter's quantized Linear): as wq_gemm_w4a16 with a
+   packed INT8 weight (bits 8). */
+WQ_API wq_status wq_gemm_w8a16(const void* X, const uint32_t* Wp, const void* scales,
+                        void* Y, int64_t M, int64_t N, int64_t K, int group,
+                        cudaStream_t stream);
+
+/* The per-device error word of the current device: WQ_OK or
+   WQ_ERR_DEVICE_TIMEOUT.  Synchronous (reads device memory); call after
+   synchronising the streams of interest.  wq_clear_device_error() resets it. */
+WQ_API wq_status wq_last_device_error(void);
+WQ_API wq_status wq_clear_device_error(void);
+
+/* Human-readable name of a status. */
+WQ_API const char* wq_status_string(wq_status status);
+
+/* The CUDA error behind the calling thread's last WQ_ERR_CUDA, as text. */
+WQ_API const char* wq_last_cuda_error(void);
+
+/* Diagnostics for tests.  wq_debug_set_wait_limit_ns: the time limit of
+   every in-kernel wait in nanoseconds (0 restores the default of 2 s).
+   wq_debug_force_timeout(mode): 0 off; 1 every CTA of the next GEMMs first
+   waits on a barrier nothing completes -- the wait runs out, is reported,
+   and the GEMM then runs normally; 2 the data waits look for a phase that
+   never completes, so the GEMM gives up, lets its copies land and reports
+   (its output is then undefined).  Both report WQ_ERR_DEVICE_TIMEOUT
+   through wq_last_device_error() without any fault. */
+WQ_API void wq_debug_set_wait_limit_ns(uint64_t ns);
+WQ_API void wq_debug_force_timeout(int mode);
+
+/* Tuning and test hooks for the small-M kernel: force the number of CTAs
+   of a cluster that split one tile's K range (1..8; 0 restores the
+   automatic choice), and enable programmatic dependent launch, which lets a
+   GEMM start streaming its weights while the preceding kernel on the stream
+   finishes.  With it on, the weights and scales of a GEMM must not be
+   written by the kernel immediately before it on the same stream (X and Y
+   may be).  Both settings are process-wide. */
+WQ_API void wq_debug_set_split(int cs);
+WQ_API void wq_set_programmatic_launch(int on);
+
+/* Which kernel family a GEMM of this shape runs: 0 = small-M split-K
+   kernel, 1 = tensor-core (tcgen05) kernel.  -1 for unsupported shapes. */
+WQ_API int wq_gemm_regime(int bits, int64_t M, int64_t N, int64_t K);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WQ_H_ */

@@ -1,0 +1,80 @@
+"""The C ABI without a GPU: the library loads, exports every symbol that
+include/wq.h declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def wq():
+    import __graft_entry__
+    __graft_entry__.build()
+    import w4a16_weight_only_wq_gb300 as m
+    return m
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "wq.h")).read()
+    return sorted(set(re.findall(r"WQ_API\s+[\w\s\*]*?\b(wq_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for must in ("wq_pack_symmetric", "wq_gemm_w4a16", "wq_gemm_w8a16",
+                 "wq_unpack", "wq_pack_codes", "wq_last_device_error"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(wq):
+    lib = ctypes.CDLL(wq.LIB_PATH)
+    for name in _declared():
+        assert hasattr(lib, name), f"{name} declared in wq.h but not exported"
+    assert set(wq.EXPORTED) == set(_declared())
+
+
+def test_packed_words(wq):
+    assert wq.wq_packed_words(4, 2560, 9728) == 2560 * 9728 // 8
+    assert wq.wq_packed_words(8, 2560, 9728) == 2560 * 9728 // 4
+    assert wq.wq_packed_words(4, 100, 64) == 0
+    assert wq.wq_packed_words(4, 128, 96) == 0
+    assert wq.wq_packed_words(3, 128, 64) == 0
+
+
+def test_argument_errors_without_gpu(wq):
+    A = 1 << 20  # a 16-byte aligned fake address; never dereferenced
+    s = 0
+    assert wq.wq_gemm_w4a16(None, A, A, A, 16, 64, 128, 128, s) == wq.WQ_ERR_NULL
+    assert wq.wq_gemm_w4a16(A, A, A, A, 16, 64, 128, 64, s) == wq.WQ_ERR_SHAPE
+    assert wq.wq_gemm_w4a16(A, A, A, A, 16, 64, 100, 128, s) == wq.WQ_ERR_SHAPE
+    assert wq.wq_gemm_w4a16(A, A, A, A, 16, 96, 128, 128, s) == wq.WQ_ERR_SHAPE
+    assert wq.wq_gemm_w4a16(A, A, A, A, -1, 64, 128, 128, s) == wq.WQ_ERR_SHAPE
+    assert wq.wq_gemm_w8a16(A + 8, A, A, A, 16, 64, 128, 128, s) == wq.WQ_ERR_ALIGN
+    assert wq.wq_gemm_w4a16(A, A, A, A, 0, 64, 128, 128, s) == wq.WQ_OK
+    assert wq.wq_pack_symmetric(A, 0, 128, 64, 5, 128, None, A, A, s) == \
+        wq.WQ_ERR_UNSUPPORTED
+    assert wq.wq_pack_symmetric(A, 7, 128, 64, 4, 128, None, A, A, s) == \
+        wq.WQ_ERR_UNSUPPORTED
+    assert wq.wq_pack_symmetric(A, 0, 128, 64, 4, 128, None, None, A, s) == \
+        wq.WQ_ERR_NULL
+    assert wq.wq_pack_codes(A, 128, 64, 4, A + 4, s) == wq.WQ_ERR_ALIGN
+    assert wq.wq_unpack(A, 4, 128, 60, A, s) == wq.WQ_ERR_SHAPE
+
+
+def test_status_strings(wq):
+    for st in range(7):
+        assert wq.status_string(st).startswith("WQ_")
+    assert "unknown" in wq.status_string(99)
+
+
+def test_regime_selection_is_host_logic(wq):
+    # every benchmark shape has a kernel
+    for bits, M, K, N in ((4, 16, 2560, 2560), (4, 16, 2560, 9728),
+                          (4, 16, 9728, 2560), (8, 16, 2560, 9728),
+                          (4, 1, 2560, 2560), (4, 128, 2560, 9728),
+                          (4, 8192, 2560, 9728)):
+        assert wq.wq_gemm_regime(bits, M, N, K) in (0, 1)
+    assert wq.wq_gemm_regime(4, 16, 96, 128) == -1

@@ -1,0 +1,75 @@
+"""Bounded waits: a wait that runs out reports WQ_ERR_DEVICE_TIMEOUT and the
+context stays usable.  The wait is made to run out by pointing it at a
+barrier nothing completes (no fault, no trap, no hang)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import synth
+from tests.gpu_util import assert_close_to_oracle, bf16_to_dev, i8_to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def wq():
+    import __graft_entry__
+    __graft_entry__.build()
+    import w4a16_weight_only_wq_gb300 as m
+    return m
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_forced_timeout_reports_and_recovers(wq, bits):
+    M, K, N = 16, 1024, 256
+    X, q, s = synth.small_case(M, K, N, bits, seed=8)
+    Wp = wq.pack_codes(i8_to_dev(q), bits)
+    Xt, st = bf16_to_dev(X), bf16_to_dev(s)
+    fn = wq.gemm_w4a16 if bits == 4 else wq.gemm_w8a16
+    torch.cuda.synchronize()
+    assert wq.wq_clear_device_error() == wq.WQ_OK
+    try:
+        wq.wq_debug_set_wait_limit_ns(200_000)  # 0.2 ms
+        wq.wq_debug_force_timeout(1)
+        fn(Xt, Wp, st)
+        torch.cuda.synchronize()
+    finally:
+        wq.wq_debug_force_timeout(0)
+        wq.wq_debug_set_wait_limit_ns(0)
+    assert wq.wq_last_device_error() == wq.WQ_ERR_DEVICE_TIMEOUT
+    assert wq.wq_clear_device_error() == wq.WQ_OK
+    Y = fn(Xt, Wp, st)
+    torch.cuda.synchronize()
+    assert wq.wq_last_device_error() == wq.WQ_OK
+    Yref = oracle.gemm(X, oracle.pack(q, bits), s, K, N, bits)
+    assert_close_to_oracle(Y, Yref, "after timeout")
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_abandoned_data_wait_drains_and_recovers(wq, bits):
+    """The data waits look for a phase that never completes: the kernel gives
+    up, lets its copies land, reports the timeout, and a normal call
+    afterwards is correct."""
+    M, K, N = 16, 9728, 2560  # split across a cluster, ring refills for INT8
+    X, q, s = synth.small_case(M, K, N, bits, seed=12)
+    Wp = wq.pack_codes(i8_to_dev(q), bits)
+    Xt, st = bf16_to_dev(X), bf16_to_dev(s)
+    fn = wq.gemm_w4a16 if bits == 4 else wq.gemm_w8a16
+    torch.cuda.synchronize()
+    assert wq.wq_clear_device_error() == wq.WQ_OK
+    try:
+        wq.wq_debug_set_wait_limit_ns(1_000_000)  # 1 ms
+        wq.wq_debug_force_timeout(2)
+        fn(Xt, Wp, st)
+        torch.cuda.synchronize()
+    finally:
+        wq.wq_debug_force_timeout(0)
+        wq.wq_debug_set_wait_limit_ns(0)
+    assert wq.wq_last_device_error() == wq.WQ_ERR_DEVICE_TIMEOUT
+    assert wq.wq_clear_device_error() == wq.WQ_OK
+    Y = fn(Xt, Wp, st)
+    torch.cuda.synchronize()
+    assert wq.wq_last_device_error() == wq.WQ_OK
+    Yref = oracle.gemm(X, oracle.pack(q, bits), s, K, N, bits)
+    assert_close_to_oracle(Y, Yref, "after an abandoned wait")

@@ -1,0 +1,166 @@
+"""GPU GEMM against the oracle, element by element, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import synth
+from tests.gpu_util import (assert_close_to_oracle, bf16_to_dev,
+                            bf16_to_host_bits, f32_to_dev, i8_to_dev,
+                            words_to_host)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def wq():
+    import __graft_entry__
+    __graft_entry__.build()
+    import w4a16_weight_only_wq_gb300 as m
+    assert torch.cuda.is_available(), "GPU tests need a GPU"
+    return m
+
+
+def _gemm(wq, bits, Xt, Wp, st, N=None, Y=None):
+    fn = wq.gemm_w4a16 if bits == 4 else wq.gemm_w8a16
+    return fn(Xt, Wp, st, N=N, Y=Y)
+
+
+def _run_codes_case(wq, X, q, s, bits, rows=None):
+    K, N = q.shape
+    Wp = wq.pack_codes(i8_to_dev(q), bits)
+    Y = _gemm(wq, bits, bf16_to_dev(X), Wp, bf16_to_dev(s))
+    torch.cuda.synchronize()
+    p_ref = oracle.pack(q, bits)
+    assert np.array_equal(words_to_host(Wp), p_ref)
+    Yref = oracle.gemm(X, p_ref, s, K, N, bits, rows=rows)
+    Ysel = Y if rows is None else Y[torch.as_tensor(rows, device=Y.device)]
+    return assert_close_to_oracle(Ysel, Yref, f"W{bits} M={X.shape[0]} K={K} N={N}")
+
+
+# ------------------------------------------------ small shapes, many tiles ---
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M", [1, 5, 16, 17, 40])
+@pytest.mark.parametrize("K,N", [(128, 64), (640, 192), (1280, 576), (3840, 128)])
+def test_small_shapes(wq, bits, M, K, N):
+    X, q, s = synth.small_case(M, K, N, bits, seed=M * 7 + K + N + bits)
+    _run_codes_case(wq, X, q, s, bits)
+
+
+# --------------------------------------------------------- exact cases ---
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("K", [128, 256])
+def test_identity_probe_bit_exact(wq, bits, K):
+    """X = I recovers bf16(s * q) exactly (identity probe of the W8A16
+    card's fused-KV patch)."""
+    N = 128
+    _, q, s = synth.small_case(1, K, N, bits, seed=K + bits)
+    eye = oracle.f32_to_bf16_bits(np.eye(K, dtype=np.float32))
+    Wp = wq.pack_codes(i8_to_dev(q), bits)
+    Y = _gemm(wq, bits, bf16_to_dev(eye), Wp, bf16_to_dev(s))
+    torch.cuda.synchronize()
+    Yref = oracle.gemm(eye, oracle.pack(q, bits), s, K, N, bits)
+    want = oracle.f32_to_bf16_bits(Yref.astype(np.float32))
+    assert np.array_equal(bf16_to_host_bits(Y), want)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_integer_exact_bruteforce_bit_exact(wq, bits):
+    """Powers-of-two scales and small integer X: every partial sum is exact,
+    so the GPU result must be the oracle's value rounded once to bf16."""
+    M, K, N = 16, 1024, 256
+    rng = np.random.default_rng(17 + bits)
+    lo, hi = (-8, 7) if bits == 4 else (-128, 127)
+    q = rng.integers(lo, hi + 1, size=(K, N)).astype(np.int8)
+    s = oracle.f32_to_bf16_bits(
+        (2.0 ** rng.integers(-8, -2, size=(K // 128, N))).astype(np.float32))
+    X = oracle.f32_to_bf16_bits(rng.integers(-4, 5, size=(M, K)).astype(np.float32))
+    Wp = wq.pack_codes(i8_to_dev(q), bits)
+    Y = _gemm(wq, bits, bf16_to_dev(X), Wp, bf16_to_dev(s))
+    torch.cuda.synchronize()
+    Yref = oracle.gemm(X, oracle.pack(q, bits), s, K, N, bits)
+    want = oracle.f32_to_bf16_bits(Yref.astype(np.float32))
+    assert np.array_equal(Yref.astype(np.float32).astype(np.float64), Yref)
+    assert np.array_equal(bf16_to_host_bits(Y), want)
+
+
+# ------------------------------------------------------ edge behaviours ---
+def test_m_zero_is_a_noop(wq):
+    K, N = 256, 128
+    _, q, s = synth.small_case(1, K, N, 4, seed=3)
+    Wp = wq.pack_codes(i8_to_dev(q), 4)
+    X = torch.empty((0, K), dtype=torch.bfloat16, device="cuda")
+    Y = torch.empty((0, N), dtype=torch.bfloat16, device="cuda")
+    assert wq.wq_gemm_w4a16(X.data_ptr() or None, Wp.data_ptr(), None, None, 0, N,
+                            K, 128, 0) == wq.WQ_OK
+    wq.gemm_w4a16(X, Wp, bf16_to_dev(s), Y=Y)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_output_rows_beyond_m_untouched_and_deterministic(wq, bits):
+    M, K, N = 5, 1280, 640
+    X, q, s = synth.small_case(M, K, N, bits, seed=31)
+    Wp = wq.pack_codes(i8_to_dev(q), bits)
+    Xt, st = bf16_to_dev(X), bf16_to_dev(s)
+    canary = torch.full((M + 3, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    Yv = canary[:M]
+    _gemm(wq, bits, Xt, Wp, st, Y=Yv)
+    Y2 = _gemm(wq, bits, Xt, Wp, st)
+    torch.cuda.synchronize()
+    assert torch.all(canary[M:] == 7.0)
+    assert torch.equal(Yv, Y2), "two calls differ"
+    Yref = oracle.gemm(X, oracle.pack(q, bits), s, K, N, bits)
+    assert_close_to_oracle(Yv, Yref, "canary case")
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_every_cluster_split(wq, bits):
+    """Force each K split 1..8 of the cluster reduction on a ragged shape."""
+    M, K, N = 9, 1152, 320   # 9 groups, 5 tiles
+    X, q, s = synth.small_case(M, K, N, bits, seed=44)
+    try:
+        for cs in range(1, 9):
+            wq.wq_debug_set_split(cs)
+            _run_codes_case(wq, X, q, s, bits)
+    finally:
+        wq.wq_debug_set_split(0)
+
+
+# ------------------------------------------------ the benchmark workloads ---
+def _case_ids(cases):
+    return [c.name for c in cases]
+
+
+FULL = synth.C1 + synth.C2 + synth.C3 + [c for c in synth.C4 if c.kind == "codes"]
+
+
+@pytest.mark.parametrize("case", FULL, ids=_case_ids(FULL))
+def test_workload_codes(wq, case):
+    d = case.draw()
+    _run_codes_case(wq, d["X"], d["q"], d["s"], case.bits)
+
+
+@pytest.mark.parametrize("case", [c for c in synth.C4 if c.kind == "rtn"],
+                         ids=_case_ids([c for c in synth.C4 if c.kind == "rtn"]))
+def test_workload_drafter_rtn(wq, case):
+    d = case.draw()
+    K, N = case.K, case.N
+    packed, st = wq.pack_symmetric(f32_to_dev(d["W"]), 8)
+    Y = wq.gemm_w8a16(bf16_to_dev(d["X"]), packed, st)
+    torch.cuda.synchronize()
+    p_ref, s_ref, _ = oracle.pack_symmetric(d["W"], 8)
+    assert np.array_equal(words_to_host(packed), p_ref)
+    Yref = oracle.gemm(d["X"], p_ref, s_ref, K, N, 8)
+    assert_close_to_oracle(Y, Yref, case.name)
+
+
+@pytest.mark.parametrize("case", synth.C5, ids=_case_ids(synth.C5))
+def test_workload_prefill_sampled_rows(wq, case):
+    """M = 8192: rows sampled from the first and last 128-row tiles and at
+    random are checked one by one against the oracle."""
+    d = case.draw()
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([np.arange(0, 8), np.arange(120, 136),
+                                     np.arange(case.M - 8, case.M),
+                                     rng.integers(0, case.M, 24)]))
+    _run_codes_case(wq, d["X"], d["q"], d["s"], case.bits, rows=rows)

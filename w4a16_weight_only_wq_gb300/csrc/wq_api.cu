@@ -1,0 +1,246 @@
+// wq_api.cu -- the C ABI declared in include/wq.h: argument checks, regime
+// selection, launches on the caller's stream, and the per-device error word.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "wq.h"
+#include "wq_internal.h"
+
+namespace {
+
+// Per-device error word written by bounded waits that ran out.
+__device__ uint32_t g_wq_device_error;
+
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+std::atomic<int> g_force_timeout{0};
+std::atomic<int> g_pdl{0};
+std::atomic<int> g_split_hint{0};
+thread_local cudaError_t t_last_cuda = cudaSuccess;
+
+wq_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return WQ_OK;
+  t_last_cuda = e;
+  return WQ_ERR_CUDA;
+}
+
+struct DeviceInfo {
+  int num_sms = 0;
+  int cc = 0;
+  uint32_t* err = nullptr;
+};
+DeviceInfo g_dev[64];
+std::atomic<uint64_t> g_dev_ready{0};
+std::mutex g_dev_mu;
+
+wq_status device_info(int* dev_out, DeviceInfo* info) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return WQ_ERR_CUDA;
+  *dev_out = dev;
+  const uint64_t bit = 1ull << dev;
+  if (!(g_dev_ready.load(std::memory_order_acquire) & bit)) {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!(g_dev_ready.load() & bit)) {
+      DeviceInfo d;
+      int major = 0, minor = 0;
+      if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return WQ_ERR_CUDA;
+      d.cc = major * 10 + minor;
+      if (d.cc != 103) return WQ_ERR_UNSUPPORTED;  // built for sm_103a only
+      if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_wq_device_error) != cudaSuccess)
+        return WQ_ERR_CUDA;
+      g_dev[dev] = d;
+      g_dev_ready.fetch_or(bit, std::memory_order_release);
+    }
+  }
+  *info = g_dev[dev];
+  return WQ_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+wq_status check_kn(int64_t K, int64_t N) {
+  if (K <= 0 || N <= 0 || K % 128 != 0 || N % 64 != 0) return WQ_ERR_SHAPE;
+  if (K > (int64_t(1) << 30) || N > (int64_t(1) << 30) || K * N >= (int64_t(1) << 40))
+    return WQ_ERR_SHAPE;
+  if (K / 128 > 65535) return WQ_ERR_SHAPE;
+  return WQ_OK;
+}
+
+wq::DiagHost diag_for(const DeviceInfo& d) {
+  wq::DiagHost h;
+  h.err = d.err;
+  h.wait_limit_ns = g_wait_limit_ns.load();
+  h.force_timeout = g_force_timeout.load();
+  return h;
+}
+
+wq_status gemm_common(int bits, const void* X, const uint32_t* Wp,
+                      const void* scales, void* Y, int64_t M, int64_t N,
+                      int64_t K, int group, cudaStream_t stream) {
+  if (!X || !Wp || !scales || !Y) return M == 0 ? WQ_OK : WQ_ERR_NULL;
+  if (group != 128) return WQ_ERR_SHAPE;
+  if (M < 0 || M > (int64_t(1) << 30)) return WQ_ERR_SHAPE;
+  wq_status st = check_kn(K, N);
+  if (st != WQ_OK) return st;
+  if (M * K >= (int64_t(1) << 40) || M * N >= (int64_t(1) << 40)) return WQ_ERR_SHAPE;
+  if (!aligned16(X) || !aligned16(Wp) || !aligned16(scales) || !aligned16(Y))
+    return WQ_ERR_ALIGN;
+  if (M == 0) return WQ_OK;
+  int dev;
+  DeviceInfo d;
+  st = device_info(&dev, &d);
+  if (st != WQ_OK) return st;
+  wq::GemmArgs a;
+  a.X = X;
+  a.Wp = Wp;
+  a.S = scales;
+  a.Y = Y;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.bits = bits;
+  a.num_sms = d.num_sms;
+  a.device = dev;
+  a.pdl = g_pdl.load();
+  a.split_hint = g_split_hint.load();
+  a.diag = diag_for(d);
+  // The small-M kernel takes up to 16 rows per launch; taller inputs are
+  // processed in 16-row slices.
+  const size_t xrow = static_cast<size_t>(K) * 2, yrow = static_cast<size_t>(N) * 2;
+  for (int64_t m0 = 0; m0 < M; m0 += 16) {
+    a.X = static_cast<const char*>(X) + m0 * xrow;
+    a.Y = static_cast<char*>(Y) + m0 * yrow;
+    a.M = (M - m0) < 16 ? (M - m0) : 16;
+    cudaError_t e = wq::launch_gemm_small(a, stream);
+    if (e == cudaErrorNotSupported) return WQ_ERR_SHAPE;
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return WQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t wq_packed_words(int bits, int64_t K, int64_t N) {
+  if ((bits != 4 && bits != 8) || check_kn(K, N) != WQ_OK) return 0;
+  return static_cast<size_t>(bits == 4 ? K * N / 8 : K * N / 4);
+}
+
+wq_status wq_pack_symmetric(const void* W, wq_dtype wdt, int64_t K, int64_t N,
+                            int bits, int group, const uint16_t* scales_in,
+                            uint16_t* scales_out, uint32_t* packed,
+                            cudaStream_t stream) {
+  if (!W || !scales_out || !packed) return WQ_ERR_NULL;
+  if (bits != 4 && bits != 8) return WQ_ERR_UNSUPPORTED;
+  if (wdt != WQ_F32 && wdt != WQ_BF16) return WQ_ERR_UNSUPPORTED;
+  if (group != 128) return WQ_ERR_SHAPE;
+  wq_status st = check_kn(K, N);
+  if (st != WQ_OK) return st;
+  if (!aligned16(W) || !aligned16(packed) || !aligned16(scales_out) ||
+      (scales_in && !aligned16(scales_in)))
+    return WQ_ERR_ALIGN;
+  int dev;
+  DeviceInfo d;
+  st = device_info(&dev, &d);
+  if (st != WQ_OK) return st;
+  cudaError_t e = wq::launch_pack_symmetric(W, wdt == WQ_F32 ? 0 : 1, K, N, bits,
+                                            scales_in, scales_out, packed, stream);
+  return cuda_status(e);
+}
+
+wq_status wq_pack_codes(const int8_t* codes, int64_t K, int64_t N, int bits,
+                        uint32_t* packed, cudaStream_t stream) {
+  if (!codes || !packed) return WQ_ERR_NULL;
+  if (bits != 4 && bits != 8) return WQ_ERR_UNSUPPORTED;
+  wq_status st = check_kn(K, N);
+  if (st != WQ_OK) return st;
+  if (!aligned16(codes) || !aligned16(packed)) return WQ_ERR_ALIGN;
+  int dev;
+  DeviceInfo d;
+  st = device_info(&dev, &d);
+  if (st != WQ_OK) return st;
+  cudaError_t e = wq::launch_pack_codes(codes, K, N, bits, packed, stream);
+  return cuda_status(e);
+}
+
+wq_status wq_unpack(const uint32_t* packed, int bits, int64_t K, int64_t N,
+                    int8_t* codes, cudaStream_t stream) {
+  if (!codes || !packed) return WQ_ERR_NULL;
+  if (bits != 4 && bits != 8) return WQ_ERR_UNSUPPORTED;
+  wq_status st = check_kn(K, N);
+  if (st != WQ_OK) return st;
+  if (!aligned16(codes) || !aligned16(packed)) return WQ_ERR_ALIGN;
+  int dev;
+  DeviceInfo d;
+  st = device_info(&dev, &d);
+  if (st != WQ_OK) return st;
+  cudaError_t e = wq::launch_unpack(packed, bits, K, N, codes, stream);
+  return cuda_status(e);
+}
+
+wq_status wq_gemm_w4a16(const void* X, const uint32_t* Wp, const void* scales,
+                        void* Y, int64_t M, int64_t N, int64_t K, int group,
+                        cudaStream_t stream) {
+  return gemm_common(4, X, Wp, scales, Y, M, N, K, group, stream);
+}
+
+wq_status wq_gemm_w8a16(const void* X, const uint32_t* Wp, const void* scales,
+                        void* Y, int64_t M, int64_t N, int64_t K, int group,
+                        cudaStream_t stream) {
+  return gemm_common(8, X, Wp, scales, Y, M, N, K, group, stream);
+}
+
+wq_status wq_last_device_error(void) {
+  uint32_t v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_wq_device_error, sizeof(v)) != cudaSuccess)
+    return WQ_ERR_CUDA;
+  return static_cast<wq_status>(v);
+}
+
+wq_status wq_clear_device_error(void) {
+  const uint32_t z = 0;
+  if (cudaMemcpyToSymbol(g_wq_device_error, &z, sizeof(z)) != cudaSuccess)
+    return WQ_ERR_CUDA;
+  return WQ_OK;
+}
+
+const char* wq_status_string(wq_status s) {
+  switch (s) {
+    case WQ_OK: return "WQ_OK";
+    case WQ_ERR_NULL: return "WQ_ERR_NULL: a required pointer is NULL";
+    case WQ_ERR_SHAPE: return "WQ_ERR_SHAPE: unsupported M/N/K/group";
+    case WQ_ERR_UNSUPPORTED: return "WQ_ERR_UNSUPPORTED: bits, dtype or device not supported";
+    case WQ_ERR_ALIGN: return "WQ_ERR_ALIGN: pointer not 16-byte aligned";
+    case WQ_ERR_CUDA: return "WQ_ERR_CUDA: a CUDA runtime call failed";
+    case WQ_ERR_DEVICE_TIMEOUT: return "WQ_ERR_DEVICE_TIMEOUT: an in-kernel wait ran out";
+  }
+  return "unknown wq_status";
+}
+
+void wq_debug_set_wait_limit_ns(uint64_t ns) {
+  g_wait_limit_ns.store(ns == 0 ? kDefaultWaitLimitNs : ns);
+}
+
+void wq_debug_force_timeout(int mode) {
+  g_force_timeout.store(mode == 1 || mode == 2 ? mode : 0);
+}
+
+const char* wq_last_cuda_error(void) { return cudaGetErrorString(t_last_cuda); }
+
+void wq_debug_set_split(int cs) { g_split_hint.store(cs < 0 || cs > 8 ? 0 : cs); }
+
+void wq_set_programmatic_launch(int on) { g_pdl.store(on ? 1 : 0); }
+
+int wq_gemm_regime(int bits, int64_t M, int64_t N, int64_t K) {
+  if ((bits != 4 && bits != 8) || M < 0 || check_kn(K, N) != WQ_OK) return -1;
+  return wq::gemm_small_fits(bits, K, N, g_split_hint.load()) ? 0 : -1;
+}
+
+}  // extern "C"

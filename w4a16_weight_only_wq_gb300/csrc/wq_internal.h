@@ -1,0 +1,45 @@
+// wq_internal.h -- launch functions shared between the library's
+// translation units (not part of the public C ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace wq {
+
+struct DiagHost {
+  uint32_t* err;
+  uint64_t wait_limit_ns;
+  int force_timeout;
+};
+
+// Pack / unpack (wq_pack.cu).  Shapes and pointers are validated by the
+// caller.  wdt: 0 = fp32, 1 = bf16.
+cudaError_t launch_pack_symmetric(const void* W, int wdt, int64_t K, int64_t N,
+                                  int bits, const uint16_t* scales_in,
+                                  uint16_t* scales_out, uint32_t* packed,
+                                  cudaStream_t stream);
+cudaError_t launch_pack_codes(const int8_t* codes, int64_t K, int64_t N,
+                              int bits, uint32_t* packed, cudaStream_t stream);
+cudaError_t launch_unpack(const uint32_t* packed, int bits, int64_t K,
+                          int64_t N, int8_t* codes, cudaStream_t stream);
+
+// Small-M split-K GEMM (wq_gemm_small.cu).
+struct GemmArgs {
+  const void* X;
+  const uint32_t* Wp;
+  const void* S;
+  void* Y;
+  int64_t M, N, K;
+  int bits;
+  int num_sms;
+  int device;
+  int pdl;          // launch with programmatic stream serialization
+  int split_hint;   // 0 = automatic cluster split
+  DiagHost diag;
+};
+// Returns cudaErrorNotSupported when the shape does not fit this kernel.
+cudaError_t launch_gemm_small(const GemmArgs& a, cudaStream_t stream);
+bool gemm_small_fits(int bits, int64_t K, int64_t N, int split_hint);
+
+}  // namespace wq
