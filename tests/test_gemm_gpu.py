@@ -164,3 +164,64 @@ def test_workload_prefill_sampled_rows(wq, case):
                                      np.arange(case.M - 8, case.M),
                                      rng.integers(0, case.M, 24)]))
     _run_codes_case(wq, d["X"], d["q"], d["s"], case.bits, rows=rows)
+
+
+# --------------------------------------------- the tensor-core (tcgen05) path ---
+@pytest.fixture
+def tc_regime(wq):
+    wq.wq_debug_force_regime(1)
+    yield
+    wq.wq_debug_force_regime(-1)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M,K,N", [(1, 128, 64), (100, 640, 320), (129, 1280, 576),
+                                   (300, 384, 256), (256, 2560, 512)])
+def test_tc_ragged_shapes(wq, tc_regime, bits, M, K, N):
+    assert wq.wq_gemm_regime(bits, M, N, K) == 1
+    X, q, s = synth.small_case(M, K, N, bits, seed=M + K + N + bits)
+    _run_codes_case(wq, X, q, s, bits)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_tc_identity_probe_bit_exact(wq, tc_regime, bits):
+    """X = I through the tensor-core path gives bf16(s*q) exactly."""
+    K, N = 256, 320
+    _, q, s = synth.small_case(1, K, N, bits, seed=5 + bits)
+    eye = oracle.f32_to_bf16_bits(np.eye(K, dtype=np.float32))
+    Wp = wq.pack_codes(i8_to_dev(q), bits)
+    Y = _gemm(wq, bits, bf16_to_dev(eye), Wp, bf16_to_dev(s))
+    torch.cuda.synchronize()
+    Yref = oracle.gemm(eye, oracle.pack(q, bits), s, K, N, bits)
+    want = oracle.f32_to_bf16_bits(Yref.astype(np.float32))
+    assert np.array_equal(bf16_to_host_bits(Y), want)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_tc_integer_exact_bit_exact(wq, tc_regime, bits):
+    M, K, N = 200, 1024, 512
+    rng = np.random.default_rng(23 + bits)
+    lo, hi = (-8, 7) if bits == 4 else (-128, 127)
+    q = rng.integers(lo, hi + 1, size=(K, N)).astype(np.int8)
+    s = oracle.f32_to_bf16_bits(
+        (2.0 ** rng.integers(-8, -2, size=(K // 128, N))).astype(np.float32))
+    X = oracle.f32_to_bf16_bits(rng.integers(-4, 5, size=(M, K)).astype(np.float32))
+    Wp = wq.pack_codes(i8_to_dev(q), bits)
+    Y = _gemm(wq, bits, bf16_to_dev(X), Wp, bf16_to_dev(s))
+    torch.cuda.synchronize()
+    Yref = oracle.gemm(X, oracle.pack(q, bits), s, K, N, bits)
+    want = oracle.f32_to_bf16_bits(Yref.astype(np.float32))
+    assert np.array_equal(bf16_to_host_bits(Y), want)
+
+
+def test_tc_deterministic_and_rows_beyond_m_untouched(wq, tc_regime):
+    M, K, N = 130, 768, 384
+    X, q, s = synth.small_case(M, K, N, 4, seed=77)
+    Wp = wq.pack_codes(i8_to_dev(q), 4)
+    Xt, st = bf16_to_dev(X), bf16_to_dev(s)
+    canary = torch.full((M + 5, N), 3.0, dtype=torch.bfloat16, device="cuda")
+    wq.gemm_w4a16(Xt, Wp, st, Y=canary[:M])
+    Y2 = wq.gemm_w4a16(Xt, Wp, st)
+    torch.cuda.synchronize()
+    assert torch.all(canary[M:] == 3.0)
+    assert torch.equal(canary[:M], Y2)

@@ -38,7 +38,7 @@ EXPORTED = (
     "wq_gemm_w4a16", "wq_gemm_w8a16", "wq_last_device_error",
     "wq_clear_device_error", "wq_status_string", "wq_debug_set_wait_limit_ns",
     "wq_debug_force_timeout", "wq_gemm_regime", "wq_debug_set_split",
-    "wq_set_programmatic_launch", "wq_last_cuda_error",
+    "wq_set_programmatic_launch", "wq_last_cuda_error", "wq_debug_force_regime",
 )
 
 
@@ -74,6 +74,7 @@ def _load() -> ctypes.CDLL:
         "wq_debug_set_split": ([I], None),
         "wq_set_programmatic_launch": ([I], None),
         "wq_last_cuda_error": ([], ctypes.c_char_p),
+        "wq_debug_force_regime": ([I], None),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -144,6 +145,11 @@ def wq_gemm_regime(bits: int, M: int, N: int, K: int) -> int:
 
 def wq_debug_set_split(cs: int) -> None:
     _lib.wq_debug_set_split(int(cs))
+
+
+def wq_debug_force_regime(regime: int) -> None:
+    """0 small-M kernel, 1 tensor-core kernel, -1 automatic."""
+    _lib.wq_debug_force_regime(int(regime))
 
 
 def wq_set_programmatic_launch(on: bool) -> None:

@@ -19,6 +19,17 @@ std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
 std::atomic<int> g_force_timeout{0};
 std::atomic<int> g_pdl{0};
 std::atomic<int> g_split_hint{0};
+std::atomic<int> g_force_regime{-1};
+
+// Rows up to which the small-M kernel (16 rows per launch) is used; larger
+// M runs on the tensor-core kernel.
+constexpr int64_t kSmallMaxM = 32;
+
+int pick_regime(int64_t M) {
+  const int f = g_force_regime.load();
+  if (f == 0 || f == 1) return f;
+  return M <= kSmallMaxM ? 0 : 1;
+}
 thread_local cudaError_t t_last_cuda = cudaSuccess;
 
 wq_status cuda_status(cudaError_t e) {
@@ -110,6 +121,11 @@ wq_status gemm_common(int bits, const void* X, const uint32_t* Wp,
   a.pdl = g_pdl.load();
   a.split_hint = g_split_hint.load();
   a.diag = diag_for(d);
+  if (pick_regime(M) == 1) {
+    cudaError_t e = wq::launch_gemm_tc(a, stream);
+    if (e == cudaErrorNotSupported) return WQ_ERR_UNSUPPORTED;
+    return cuda_status(e);
+  }
   // The small-M kernel takes up to 16 rows per launch; taller inputs are
   // processed in 16-row slices.
   const size_t xrow = static_cast<size_t>(K) * 2, yrow = static_cast<size_t>(N) * 2;
@@ -238,8 +254,13 @@ void wq_debug_set_split(int cs) { g_split_hint.store(cs < 0 || cs > 8 ? 0 : cs);
 
 void wq_set_programmatic_launch(int on) { g_pdl.store(on ? 1 : 0); }
 
+void wq_debug_force_regime(int regime) {
+  g_force_regime.store(regime == 0 || regime == 1 ? regime : -1);
+}
+
 int wq_gemm_regime(int bits, int64_t M, int64_t N, int64_t K) {
   if ((bits != 4 && bits != 8) || M < 0 || check_kn(K, N) != WQ_OK) return -1;
+  if (pick_regime(M) == 1) return 1;
   return wq::gemm_small_fits(bits, K, N, g_split_hint.load()) ? 0 : -1;
 }
 
