@@ -69,6 +69,10 @@ def parse_args():
     ap.add_argument("--sweep", action="store_true",
                     help="time every benchmark GEMM shape and print a table "
                          "(one JSON object per shape) instead of the bench line")
+    ap.add_argument("--only", default="",
+                    help="sweep: only cases whose name contains this text")
+    ap.add_argument("--shape", default="",
+                    help="sweep: one extra shape M,K,N,bits (e.g. 1024,2560,9728,4)")
     return ap.parse_args()
 
 
@@ -491,6 +495,10 @@ def run_sweep(args):
     sh = int(stream.cuda_stream)
     cases = synth.C1 + synth.C2 + synth.C3 + \
         [c for c in synth.C4 if c.kind == "codes"] + synth.C5
+    if args.shape:
+        m_, k_, n_, b_ = (int(v) for v in args.shape.split(","))
+        cases = [synth.GemmCase(f"shape_w{b_}_m{m_}_{k_}x{n_}", m_, k_, n_, b_, 9)]
+    cases = [c for c in cases if args.only in c.name]
     for case in cases:
         d = case.draw()
         bits, m, k, n = case.bits, case.M, case.K, case.N

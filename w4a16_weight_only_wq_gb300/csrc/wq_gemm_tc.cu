@@ -34,8 +34,8 @@ namespace wq {
 namespace {
 
 constexpr int kBM = 128, kBN = 256, kBK = 64;
-constexpr int kStages = 3;       // k64 stages of X and dequantized W
-constexpr int kQStages = 2;      // 128-deep groups of packed W
+constexpr int kAStages = 4;      // k64 stages of X (TMA)
+constexpr int kBStages = 4;      // k64 stages of dequantized W (even: a group per pass)
 constexpr int kDequantWarps = 8;
 constexpr int kEpiWarps = 4;
 constexpr int kFirstDequantWarp = 2;
@@ -47,14 +47,15 @@ constexpr uint32_t kTmemCols = 2 * kBN;  // two accumulators
 
 template <int BITS>
 struct TcCfg {
+  static constexpr int kQStages = BITS == 4 ? 2 : 1;          // packed groups in flight
   static constexpr int kCellWords = BITS == 4 ? 1024 : 2048;  // 64 cols x 128 k
   static constexpr int kCellBytes = kCellWords * 4;
   static constexpr int kQBytes = 4 * kCellBytes + kBN * 2;    // 4 cells + scales
   static constexpr int kOffA = 0;
-  static constexpr int kOffBd = kOffA + kStages * kABytes;
-  static constexpr int kOffQ = kOffBd + kStages * kBdBytes;
+  static constexpr int kOffBd = kOffA + kAStages * kABytes;
+  static constexpr int kOffQ = kOffBd + kBStages * kBdBytes;
   static constexpr int kOffBar = kOffQ + kQStages * kQBytes;
-  static constexpr int kNumBars = 4 * kStages + 2 * kQStages + 4 + 1;
+  static constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 * kQStages + 4 + 1;
   static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;  // + align slack
 };
 
@@ -67,69 +68,86 @@ struct TcParams {
   KernelDiag diag;
 };
 
-// Dequantize one k64 half `h` of the packed group in `q_base` (4 cells of
-// 64 columns + 256 scales) into the bf16 stage at `bd_addr` (256 rows of
-// 128 bytes, 16-byte chunk c of row r stored at chunk c ^ (r % 8)).
-// Thread (dw, lane): lane = 4c + t4 reads the words of column c of each of
-// its slabs, which sit in consecutive 16-byte lanes of a cell.
+// Dequantize one packed 128-deep group (4 cells of 64 columns + 256 scales
+// at `q_base`) into the two bf16 k64 stages at `bd0` (k 0..63) and `bd1`
+// (k 64..127): 256 rows of 128 bytes, 16-byte chunk j of row r stored at
+// chunk j ^ (r % 8) (the 128-byte-swizzled K-major layout).  One thread per
+// column n = row.  The row's packed words are 64 (INT4) or 2 x 64 (INT8)
+// contiguous bytes of the cell, four 16-byte lanes t4 = 0..3; lane
+// t4 = (i + c/2) % 4 is handled in step i so that both the loads and the
+// chunk stores of a quarter-warp fall on distinct banks.
 template <int BITS>
-__device__ __forceinline__ void dequant_stage(uint32_t q_base, uint32_t bd_addr, int h,
-                                              int dw, int lane, int valid_cells) {
+__device__ __forceinline__ void dequant_group(uint32_t q_base, uint32_t bd0, uint32_t bd1,
+                                              int n, bool valid) {
   using C = TcCfg<BITS>;
   constexpr uint32_t kMask = 0x000F000Fu;
   constexpr uint32_t kLo = 0x43004300u;  // bf16 128
   constexpr uint32_t kHi = 0x45004500u;  // bf16 2048
-  const int c = lane >> 2, t4 = lane & 3;
+  if (!valid) return;
+  const int ci = n >> 6, j8 = (n >> 3) & 7, c = n & 7;
+  const uint32_t s1 = ld_shared_u16(q_base + 4 * C::kCellBytes + n * 2);
+  const uint32_t s2 = s1 | (s1 << 16);
+  const uint32_t row0 = bd0 + (n >> 3) * 1024 + c * 128;
+  const uint32_t row1 = bd1 + (n >> 3) * 1024 + c * 128;
+  const int rot = c >> 1;
+  if constexpr (BITS == 4) {
+    constexpr uint32_t kB4 = 0x43084308u;  // 136
+    // lane 4c + t4 holds words kb = 0..3: k = 32 kb + 8 t4 + 0..7
+    const uint32_t base = q_base + ci * C::kCellBytes + (j8 * 32 + 4 * c) * 16;
+    uint4 w[4];
 #pragma unroll
-  for (int si = 0; si < 4; ++si) {
-    const int J = dw * 4 + si;  // slab 0..31 of the 256 columns
-    const int ci = J >> 3, j8 = J & 7;
-    if (ci >= valid_cells) continue;
-    const int n_loc = ci * 64 + j8 * 8 + c;
-    const uint32_t s1 = ld_shared_u16(q_base + 4 * C::kCellBytes + n_loc * 2);
-    const uint32_t s2 = s1 | (s1 << 16);
-    const uint32_t row = bd_addr + (n_loc >> 3) * 1024 + c * 128;
-    if constexpr (BITS == 4) {
-      constexpr uint32_t kB4 = 0x43084308u;  // 136
-      const uint2 w = ld_shared_v2(q_base + ci * C::kCellBytes +
-                                   ((j8 * 32 + lane) * 4 + 2 * h) * 4);
+    for (int i = 0; i < 4; ++i) w[i] = ld_shared_v4(base + ((i + rot) & 3) * 16);
 #pragma unroll
-      for (int b = 0; b < 2; ++b) {
-        const uint32_t word = b ? w.y : w.x;
+    for (int i = 0; i < 4; ++i) {
+      const int t4 = (i + rot) & 3;
+#pragma unroll
+      for (int kb = 0; kb < 4; ++kb) {
+        const uint32_t word = kb == 0 ? w[i].x : kb == 1 ? w[i].y : kb == 2 ? w[i].z : w[i].w;
         const uint32_t q0 = bf16x2_sub(lop3_and_or(word, kMask, kLo), kB4);
         const uint32_t q1 = bf16x2_sub(lop3_and_or(word >> 4, kMask, kLo), kB4);
         const uint32_t q2 = bf16x2_sub(lop3_and_or(word >> 8, kMask, kLo), kB4);
         const uint32_t q3 = bf16x2_sub(lop3_and_or(word >> 12, kMask, kLo), kB4);
-        const int chunk = 4 * b + t4;
-        st_shared_v4(row + ((chunk ^ c) << 4), bf16x2_mul(q0, s2), bf16x2_mul(q1, s2),
-                     bf16x2_mul(q2, s2), bf16x2_mul(q3, s2));
+        const int chunk = 4 * (kb & 1) + t4;
+        st_shared_v4((kb < 2 ? row0 : row1) + ((chunk ^ c) << 4), bf16x2_mul(q0, s2),
+                     bf16x2_mul(q1, s2), bf16x2_mul(q2, s2), bf16x2_mul(q3, s2));
       }
-    } else {
-      constexpr uint32_t kB8Lo = 0x43004300u;  // 128
-      constexpr uint32_t kB8Hi = 0x45084508u;  // 2176
-      const uint4 w = ld_shared_v4(q_base + ci * C::kCellBytes +
-                                   (((j8 * 2 + h) * 32 + lane) * 4) * 4);
-      uint32_t v[8];
+    }
+  } else {
+    constexpr uint32_t kB8Lo = 0x43004300u;  // 128
+    constexpr uint32_t kB8Hi = 0x45084508u;  // 2176
 #pragma unroll
-      for (int wi = 0; wi < 4; ++wi) {
-        const uint32_t word = wi == 0 ? w.x : wi == 1 ? w.y : wi == 2 ? w.z : w.w;
-        const uint32_t lo01 = bf16x2_sub(lop3_and_or(word, kMask, kLo), kB8Lo);
-        const uint32_t hi01 = bf16x2_sub(lop3_and_or(word >> 4, kMask, kHi), kB8Hi);
-        const uint32_t lo23 = bf16x2_sub(lop3_and_or(word >> 8, kMask, kLo), kB8Lo);
-        const uint32_t hi23 = bf16x2_sub(lop3_and_or(word >> 12, kMask, kHi), kB8Hi);
-        v[2 * wi] = bf16x2_mul(bf16x2_add(hi01, lo01), s2);
-        v[2 * wi + 1] = bf16x2_mul(bf16x2_add(hi23, lo23), s2);
-      }
+    for (int h = 0; h < 2; ++h) {
+      // half h: lane 4c + t4 holds words wi = 0..3,
+      // k = 32 (2h + wi/2) + 8 t4 + 4 (wi & 1) + 0..3
+      const uint32_t base = q_base + ci * C::kCellBytes + ((j8 * 2 + h) * 32 + 4 * c) * 16;
+      uint4 w[4];
 #pragma unroll
-      for (int b = 0; b < 2; ++b) {
-        const int chunk = 4 * b + t4;
-        st_shared_v4(row + ((chunk ^ c) << 4), v[4 * b], v[4 * b + 1], v[4 * b + 2],
-                     v[4 * b + 3]);
+      for (int i = 0; i < 4; ++i) w[i] = ld_shared_v4(base + ((i + rot) & 3) * 16);
+      const uint32_t row = h == 0 ? row0 : row1;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int t4 = (i + rot) & 3;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          uint32_t v[4];
+#pragma unroll
+          for (int hw = 0; hw < 2; ++hw) {
+            const int wi = 2 * b + hw;
+            const uint32_t word = wi == 0 ? w[i].x : wi == 1 ? w[i].y : wi == 2 ? w[i].z : w[i].w;
+            const uint32_t lo01 = bf16x2_sub(lop3_and_or(word, kMask, kLo), kB8Lo);
+            const uint32_t hi01 = bf16x2_sub(lop3_and_or(word >> 4, kMask, kHi), kB8Hi);
+            const uint32_t lo23 = bf16x2_sub(lop3_and_or(word >> 8, kMask, kLo), kB8Lo);
+            const uint32_t hi23 = bf16x2_sub(lop3_and_or(word >> 12, kMask, kHi), kB8Hi);
+            v[2 * hw] = bf16x2_mul(bf16x2_add(hi01, lo01), s2);
+            v[2 * hw + 1] = bf16x2_mul(bf16x2_add(hi23, lo23), s2);
+          }
+          const int chunk = 4 * b + t4;
+          st_shared_v4(row + ((chunk ^ c) << 4), v[0], v[1], v[2], v[3]);
+        }
       }
     }
   }
 }
-
 
 // Bounded wait that also gives up as soon as another role has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
@@ -154,32 +172,35 @@ template <int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const TcParams p) {
   using C = TcCfg<BITS>;
+  constexpr int kQStages = C::kQStages;
   extern __shared__ uint8_t smem_raw[];
-  // 1024-byte alignment for the swizzled operand stages.
+  // 1024-byte alignment (of the shared-window offset) for the swizzled stages.
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* a_full = bars;                       // [kStages] X tile landed
-  uint64_t* bd_full = a_full + kStages;          // [kStages] W tile dequantized
-  uint64_t* st_empty = bd_full + kStages;        // [kStages] MMA done with stage
-  uint64_t* q_full = st_empty + kStages;         // [kQStages] packed group landed
+  uint64_t* a_full = bars;                       // [kAStages] X tile landed
+  uint64_t* a_empty = a_full + kAStages;         // [kAStages] MMA done with X tile
+  uint64_t* bd_full = a_empty + kAStages;        // [kBStages] W tile dequantized
+  uint64_t* bd_empty = bd_full + kBStages;       // [kBStages] MMA done with W tile
+  uint64_t* q_full = bd_empty + kBStages;        // [kQStages] packed group landed
   uint64_t* q_empty = q_full + kQStages;         // [kQStages] packed group consumed
   uint64_t* acc_full = q_empty + kQStages;       // [2] accumulator ready
   uint64_t* acc_empty = acc_full + 2;            // [2] accumulator drained
   uint64_t* never_bar = acc_empty + 2;           // test hook
-  uint64_t* spare = never_bar + 1;               // (unused, keeps kNumBars exact)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  (void)spare;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = p.K / kBK;
   const int tiles = p.mt * p.nt;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kAStages; ++i) {
       mbar_init(&a_full[i], 1);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < kBStages; ++i) {
       mbar_init(&bd_full[i], kDequantWarps);
-      mbar_init(&st_empty[i], 1);
+      mbar_init(&bd_empty[i], 1);
     }
     for (int i = 0; i < kQStages; ++i) {
       mbar_init(&q_full[i], 1);
@@ -216,15 +237,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const TcParams p) {
       int it = 0, iq = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
-        const int m0 = (t % p.mt) * kBM, ntile = t / p.mt, n0 = ntile * kBN;
+        const int m0 = (t % p.mt) * kBM, n0 = (t / p.mt) * kBN;
         const int cells = min(4, (p.N - n0) / 64);
         for (int kk = 0; kk < nk; ++kk, ++it) {
-          const int s = it % kStages;
-          if (it >= kStages &&
-              !wait_or_abort(&st_empty[s], ((it / kStages) - 1) & 1, p.diag, abort_flag)) {
-            ok = false;
-            break;
-          }
           if ((kk & 1) == 0) {  // first half of a group: fetch the packed group
             const int q = iq % kQStages, g = kk >> 1;
             if (iq >= kQStages &&
@@ -243,8 +258,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const TcParams p) {
             ++iq;
             q_issued = iq;
           }
-          mbar_arrive_expect_tx(&a_full[s], kABytes);
-          tma_load_2d(smem + C::kOffA + s * kABytes, &tmx, kk * kBK, m0, &a_full[s]);
+          const int sa = it % kAStages;
+          if (it >= kAStages &&
+              !wait_or_abort(&a_empty[sa], ((it / kAStages) - 1) & 1, p.diag, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&a_full[sa], kABytes);
+          tma_load_2d(smem + C::kOffA + sa * kABytes, &tmx, kk * kBK, m0, &a_full[sa]);
           a_issued = it + 1;
         }
       }
@@ -264,20 +285,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const TcParams p) {
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + b * kBN;
         for (int kk = 0; kk < nk; ++kk, ++it) {
-          const int s = it % kStages;
-          const uint32_t par = (it / kStages) & 1;
-          if (!wait_or_abort(&a_full[s], par, p.diag, abort_flag) ||
-              !wait_or_abort(&bd_full[s], par, p.diag, abort_flag)) {
+          const int sa = it % kAStages, sb = it % kBStages;
+          if (!wait_or_abort(&a_full[sa], (it / kAStages) & 1, p.diag, abort_flag) ||
+              !wait_or_abort(&bd_full[sb], (it / kBStages) & 1, p.diag, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t a_desc = smem_desc_sw128(smem_addr(smem + C::kOffA + s * kABytes));
-          const uint64_t b_desc = smem_desc_sw128(smem_addr(smem + C::kOffBd + s * kBdBytes));
+          const uint64_t a_desc = smem_desc_sw128(smem_addr(smem + C::kOffA + sa * kABytes));
+          const uint64_t b_desc = smem_desc_sw128(smem_addr(smem + C::kOffBd + sb * kBdBytes));
 #pragma unroll
           for (int j = 0; j < kBK / 16; ++j)  // +32 bytes per K=16 step
             umma_bf16(d_tmem, a_desc + 2 * j, b_desc + 2 * j, idesc, (kk | j) != 0);
-          umma_commit(&st_empty[s]);
+          umma_commit(&a_empty[sa]);
+          umma_commit(&bd_empty[sb]);
           mma_issued = it + 1;
         }
         if (ok) umma_commit(&acc_full[b]);
@@ -285,29 +306,34 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const TcParams p) {
     }
   } else if (warp < kFirstEpiWarp) {
     // ------------------------------------------------- dequant warps ---
-    const int dw = warp - kFirstDequantWarp;
+    // One thread per column of the 256-column tile; a whole group (two k64
+    // stages) per pass.
+    const int n = (warp - kFirstDequantWarp) * 32 + lane;
     int it = 0, iq = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
       const int n0 = (t / p.mt) * kBN;
-      const int cells = min(4, (p.N - n0) / 64);
-      for (int kk = 0; kk < nk; ++kk, ++it) {
-        const int s = it % kStages, q = iq % kQStages, h = kk & 1;
+      const bool valid = n0 + n < p.N;
+      for (int kk = 0; kk < nk; kk += 2, it += 2, ++iq) {
+        const int s0 = it % kBStages, s1 = (it + 1) % kBStages, q = iq % kQStages;
         if (!wait_or_abort(&q_full[q], (iq / kQStages) & 1, p.diag, abort_flag) ||
-            (it >= kStages &&
-             !wait_or_abort(&st_empty[s], ((it / kStages) - 1) & 1, p.diag, abort_flag))) {
+            (it >= kBStages &&
+             (!wait_or_abort(&bd_empty[s0], ((it / kBStages) - 1) & 1, p.diag, abort_flag) ||
+              !wait_or_abort(&bd_empty[s1], (((it + 1) / kBStages) - 1) & 1, p.diag,
+                             abort_flag)))) {
           ok = false;
           break;
         }
-        dequant_stage<BITS>(smem_addr(smem + C::kOffQ + q * C::kQBytes),
-                            smem_addr(smem + C::kOffBd + s * kBdBytes), h, dw, lane, cells);
+        dequant_group<BITS>(smem_addr(smem + C::kOffQ + q * C::kQBytes),
+                            smem_addr(smem + C::kOffBd + s0 * kBdBytes),
+                            smem_addr(smem + C::kOffBd + s1 * kBdBytes), n, valid);
         fence_proxy_async_smem();  // generic stores -> tensor-core reads
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&bd_full[s]);
-          if (h == 1) mbar_arrive(&q_empty[q]);
+          mbar_arrive(&bd_full[s0]);
+          mbar_arrive(&bd_full[s1]);
+          mbar_arrive(&q_empty[q]);
         }
-        if (h == 1) ++iq;
       }
     }
   } else {
@@ -351,9 +377,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const TcParams p) {
     KernelDiag drain = p.diag;
     if (drain.wait_limit_ns < 1000000000ull) drain.wait_limit_ns = 1000000000ull;
     if (warp == 0 && lane == 0) {
-      for (int s = 0; s < kStages && s < a_issued; ++s) {
-        const int last = s + ((a_issued - 1 - s) / kStages) * kStages;
-        mbar_wait_bounded(&a_full[s], (last / kStages) & 1, drain);
+      for (int s = 0; s < kAStages && s < a_issued; ++s) {
+        const int last = s + ((a_issued - 1 - s) / kAStages) * kAStages;
+        mbar_wait_bounded(&a_full[s], (last / kAStages) & 1, drain);
       }
       for (int q = 0; q < kQStages && q < q_issued; ++q) {
         const int last = q + ((q_issued - 1 - q) / kQStages) * kQStages;
@@ -362,7 +388,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const TcParams p) {
     }
     if (warp == 1 && lane == 0 && mma_issued > 0) {
       const int last = mma_issued - 1;
-      mbar_wait_bounded(&st_empty[last % kStages], (last / kStages) & 1, drain);
+      mbar_wait_bounded(&a_empty[last % kAStages], (last / kAStages) & 1, drain);
     }
     __syncthreads();
   }
