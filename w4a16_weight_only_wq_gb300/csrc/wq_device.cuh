@@ -66,6 +66,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr,
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep up to `hint_ns` inside the
+// instruction while the phase is incomplete (instead of spinning).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar_addr, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for phase `parity` of `bar` to complete, giving up after
 // `limit_ns`.  Returns false (and records the timeout) when it gives up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar,

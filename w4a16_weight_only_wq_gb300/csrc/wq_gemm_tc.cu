@@ -36,17 +36,19 @@ namespace {
 constexpr int kBM = 128, kBN = 256, kBK = 64;
 constexpr int kAStages = 4;      // k64 stages of X (TMA)
 constexpr int kBStages = 4;      // k64 stages of dequantized W (even: a group per pass)
-constexpr int kDequantWarps = 8;
 constexpr int kEpiWarps = 4;
 constexpr int kFirstDequantWarp = 2;
-constexpr int kFirstEpiWarp = kFirstDequantWarp + kDequantWarps;  // 10
-constexpr int kThreads = (kFirstEpiWarp + kEpiWarps) * 32;         // 448
 constexpr int kABytes = kBM * kBK * 2;   // 16 KiB
 constexpr int kBdBytes = kBN * kBK * 2;  // 32 KiB
 constexpr uint32_t kTmemCols = 2 * kBN;  // two accumulators
 
 template <int BITS>
 struct TcCfg {
+  // INT4: two dequant threads per column (each takes two of its four
+  // 16-byte lanes); INT8 (more registers per thread): one.
+  static constexpr int kDequantWarps = BITS == 4 ? 16 : 8;
+  static constexpr int kFirstEpiWarp = kFirstDequantWarp + kDequantWarps;
+  static constexpr int kThreads = (kFirstEpiWarp + kEpiWarps) * 32;
   static constexpr int kQStages = BITS == 4 ? 2 : 1;          // packed groups in flight
   static constexpr int kCellWords = BITS == 4 ? 1024 : 2048;  // 64 cols x 128 k
   static constexpr int kCellBytes = kCellWords * 4;
@@ -74,11 +76,11 @@ struct TcParams {
 // chunk j ^ (r % 8) (the 128-byte-swizzled K-major layout).  One thread per
 // column n = row.  The row's packed words are 64 (INT4) or 2 x 64 (INT8)
 // contiguous bytes of the cell, four 16-byte lanes t4 = 0..3; lane
-// t4 = (i + c/2) % 4 is handled in step i so that both the loads and the
-// chunk stores of a quarter-warp fall on distinct banks.
+// t4 = i ^ (c/2) is handled in step i so that both the loads and the
+// chunk stores (at chunk ^ c) of a quarter-warp fall on distinct banks.
 template <int BITS>
 __device__ __forceinline__ void dequant_group(uint32_t q_base, uint32_t bd0, uint32_t bd1,
-                                              int n, bool valid) {
+                                              int n, int part, bool valid) {
   using C = TcCfg<BITS>;
   constexpr uint32_t kMask = 0x000F000Fu;
   constexpr uint32_t kLo = 0x43004300u;  // bf16 128
@@ -93,13 +95,15 @@ __device__ __forceinline__ void dequant_group(uint32_t q_base, uint32_t bd0, uin
   if constexpr (BITS == 4) {
     constexpr uint32_t kB4 = 0x43084308u;  // 136
     // lane 4c + t4 holds words kb = 0..3: k = 32 kb + 8 t4 + 0..7
+    // this thread takes steps i = 2 part, 2 part + 1
     const uint32_t base = q_base + ci * C::kCellBytes + (j8 * 32 + 4 * c) * 16;
-    uint4 w[4];
+    uint4 w[2];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) w[i] = ld_shared_v4(base + ((i + rot) & 3) * 16);
+    for (int ii = 0; ii < 2; ++ii) w[ii] = ld_shared_v4(base + ((2 * part + ii) ^ rot) * 16);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int t4 = (i + rot) & 3;
+    for (int ii = 0; ii < 2; ++ii) {
+      const int i = ii;
+      const int t4 = (2 * part + ii) ^ rot;
 #pragma unroll
       for (int kb = 0; kb < 4; ++kb) {
         const uint32_t word = kb == 0 ? w[i].x : kb == 1 ? w[i].y : kb == 2 ? w[i].z : w[i].w;
@@ -122,11 +126,11 @@ __device__ __forceinline__ void dequant_group(uint32_t q_base, uint32_t bd0, uin
       const uint32_t base = q_base + ci * C::kCellBytes + ((j8 * 2 + h) * 32 + 4 * c) * 16;
       uint4 w[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) w[i] = ld_shared_v4(base + ((i + rot) & 3) * 16);
+      for (int i = 0; i < 4; ++i) w[i] = ld_shared_v4(base + (i ^ rot) * 16);
       const uint32_t row = h == 0 ? row0 : row1;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int t4 = (i + rot) & 3;
+        const int t4 = i ^ rot;
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
           uint32_t v[4];
@@ -150,15 +154,18 @@ __device__ __forceinline__ void dequant_group(uint32_t q_base, uint32_t bd0, uin
 }
 
 // Bounded wait that also gives up as soon as another role has aborted.
+// `hint_ns` lets a long waiter sleep inside try_wait rather than spin.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
-                                              const KernelDiag& d, volatile int* abort_flag) {
+                                              const KernelDiag& d, volatile int* abort_flag,
+                                              uint32_t hint_ns = 0) {
   const uint32_t a = smem_addr(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 16; ++i)
-      if (mbar_try_wait(a, parity)) return true;
+      if (hint_ns ? mbar_try_wait_sleep(a, parity, hint_ns) : mbar_try_wait(a, parity))
+        return true;
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > d.wait_limit_ns) {
       atomicMax(d.err, kErrTimeout);
@@ -169,10 +176,12 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
 }
 
 template <int BITS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(TcCfg<BITS>::kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const TcParams p) {
   using C = TcCfg<BITS>;
   constexpr int kQStages = C::kQStages;
+  constexpr int kDequantWarps = C::kDequantWarps;
+  constexpr int kFirstEpiWarp = C::kFirstEpiWarp;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment (of the shared-window offset) for the swizzled stages.
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -306,9 +315,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const TcParams p) {
     }
   } else if (warp < kFirstEpiWarp) {
     // ------------------------------------------------- dequant warps ---
-    // One thread per column of the 256-column tile; a whole group (two k64
-    // stages) per pass.
-    const int n = (warp - kFirstDequantWarp) * 32 + lane;
+    // One (INT8) or two (INT4) threads per column of the 256-column tile; a
+    // whole group (two k64 stages) per pass.
+    const int dwi = warp - kFirstDequantWarp;
+    const int n = (dwi & 7) * 32 + lane;
+    const int part = dwi >> 3;
     int it = 0, iq = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
@@ -326,7 +337,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const TcParams p) {
         }
         dequant_group<BITS>(smem_addr(smem + C::kOffQ + q * C::kQBytes),
                             smem_addr(smem + C::kOffBd + s0 * kBdBytes),
-                            smem_addr(smem + C::kOffBd + s1 * kBdBytes), n, valid);
+                            smem_addr(smem + C::kOffBd + s1 * kBdBytes), n, part, valid);
         fence_proxy_async_smem();  // generic stores -> tensor-core reads
         __syncwarp();
         if (lane == 0) {
@@ -342,7 +353,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const TcParams p) {
     int tl = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++tl) {
       const int b = tl & 1;
-      if (!wait_or_abort(&acc_full[b], (tl >> 1) & 1, p.diag, abort_flag)) break;
+      if (!wait_or_abort(&acc_full[b], (tl >> 1) & 1, p.diag, abort_flag, 20000)) break;
       tc_fence_after();
       const int m0 = (t % p.mt) * kBM, n0 = (t / p.mt) * kBN;
       const int m = m0 + lane_base + lane;
@@ -477,7 +488,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t stream) {
   const int tiles = p.mt * p.nt;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(tiles < a.num_sms ? tiles : a.num_sms));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(a.bits == 4 ? TcCfg<4>::kThreads : TcCfg<8>::kThreads);
   cfg.dynamicSmemBytes = a.bits == 4 ? TcCfg<4>::kSmem : TcCfg<8>::kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attrs[1];
