@@ -69,6 +69,10 @@ def parse_args():
     ap.add_argument("--sweep", action="store_true",
                     help="time every benchmark GEMM shape and print a table "
                          "(one JSON object per shape) instead of the bench line")
+    ap.add_argument("--regime", type=int, default=-1,
+                    help="with --sweep: run every GEMM on one kernel family "
+                         "(0 warp-MMA small-M, 1 tiled tensor-core, "
+                         "2 tensor-memory small-M); -1 automatic")
     ap.add_argument("--only", default="",
                     help="sweep: only cases whose name contains this text")
     ap.add_argument("--shape", default="",
@@ -491,6 +495,7 @@ def run_sweep(args):
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or 132 * 2**20)
     wq.wq_set_programmatic_launch(bool(args.pdl))
+    wq.wq_debug_force_regime(args.regime)
     stream = torch.cuda.Stream(device=dev)
     sh = int(stream.cuda_stream)
     cases = synth.C1 + synth.C2 + synth.C3 + \

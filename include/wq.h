@@ -161,13 +161,14 @@ WQ_API void wq_debug_force_timeout(int mode);
 WQ_API void wq_debug_set_split(int cs);
 WQ_API void wq_set_programmatic_launch(int on);
 
-/* Test hook: run every GEMM on one kernel family regardless of M (0 small-M
-   kernel, 1 tensor-core kernel; any other value restores the automatic
-   choice: M <= 32 small-M kernel, larger M tensor-core kernel). */
+/* Test hook: run every GEMM on one kernel family regardless of M (0 the
+   warp-MMA small-M kernel, 1 the tiled tensor-core kernel, 2 the
+   tensor-memory small-M kernel; any other value restores the automatic
+   choice: M <= 32 kernel 0 in 16-row slices, larger M kernel 1). */
 WQ_API void wq_debug_force_regime(int regime);
 
-/* Which kernel family a GEMM of this shape runs: 0 = small-M split-K
-   kernel, 1 = tensor-core (tcgen05) kernel.  -1 for unsupported shapes. */
+/* Which kernel family a GEMM of this shape runs (numbering as in
+   wq_debug_force_regime).  -1 for unsupported shapes. */
 WQ_API int wq_gemm_regime(int bits, int64_t M, int64_t N, int64_t K);
 
 #ifdef __cplusplus

@@ -20,8 +20,15 @@ def wq():
     return m
 
 
+@pytest.fixture(params=[0, 1, 2], ids=["warpmma", "tc", "tmem"])
+def regime(wq, request):
+    wq.wq_debug_force_regime(request.param)
+    yield request.param
+    wq.wq_debug_force_regime(-1)
+
+
 @pytest.mark.parametrize("bits", [4, 8])
-def test_forced_timeout_reports_and_recovers(wq, bits):
+def test_forced_timeout_reports_and_recovers(wq, regime, bits):
     M, K, N = 16, 1024, 256
     X, q, s = synth.small_case(M, K, N, bits, seed=8)
     Wp = wq.pack_codes(i8_to_dev(q), bits)
@@ -47,7 +54,8 @@ def test_forced_timeout_reports_and_recovers(wq, bits):
 
 
 @pytest.mark.parametrize("bits", [4, 8])
-def test_abandoned_data_wait_drains_and_recovers(wq, bits):
+@pytest.mark.parametrize("small", [0, 2], ids=["warpmma", "tmem"])
+def test_abandoned_data_wait_drains_and_recovers(wq, small, bits):
     """The data waits look for a phase that never completes: the kernel gives
     up, lets its copies land, reports the timeout, and a normal call
     afterwards is correct."""
@@ -59,6 +67,7 @@ def test_abandoned_data_wait_drains_and_recovers(wq, bits):
     torch.cuda.synchronize()
     assert wq.wq_clear_device_error() == wq.WQ_OK
     try:
+        wq.wq_debug_force_regime(small)
         wq.wq_debug_set_wait_limit_ns(1_000_000)  # 1 ms
         wq.wq_debug_force_timeout(2)
         fn(Xt, Wp, st)
@@ -66,6 +75,7 @@ def test_abandoned_data_wait_drains_and_recovers(wq, bits):
     finally:
         wq.wq_debug_force_timeout(0)
         wq.wq_debug_set_wait_limit_ns(0)
+        wq.wq_debug_force_regime(-1)
     assert wq.wq_last_device_error() == wq.WQ_ERR_DEVICE_TIMEOUT
     assert wq.wq_clear_device_error() == wq.WQ_OK
     Y = fn(Xt, Wp, st)

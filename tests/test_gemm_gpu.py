@@ -38,19 +38,34 @@ def _run_codes_case(wq, X, q, s, bits, rows=None):
     return assert_close_to_oracle(Ysel, Yref, f"W{bits} M={X.shape[0]} K={K} N={N}")
 
 
+@pytest.fixture(params=[0, 2], ids=["warpmma", "tmem"])
+def small_kernel(wq, request):
+    """Run the test on each small-M kernel: 0 the warp-MMA kernel (the
+    default for M <= 32), 2 the tensor-memory kernel."""
+    wq.wq_debug_force_regime(request.param)
+    yield request.param
+    wq.wq_debug_force_regime(-1)
+
+
 # ------------------------------------------------ small shapes, many tiles ---
 @pytest.mark.parametrize("bits", [4, 8])
 @pytest.mark.parametrize("M", [1, 5, 16, 17, 40])
 @pytest.mark.parametrize("K,N", [(128, 64), (640, 192), (1280, 576), (3840, 128)])
-def test_small_shapes(wq, bits, M, K, N):
+def test_small_shapes(wq, small_kernel, bits, M, K, N):
+    assert wq.wq_gemm_regime(bits, M, N, K) == small_kernel
     X, q, s = synth.small_case(M, K, N, bits, seed=M * 7 + K + N + bits)
     _run_codes_case(wq, X, q, s, bits)
+
+
+def test_default_kernel_choice(wq):
+    for M, want in [(1, 0), (16, 0), (32, 0), (33, 1), (8192, 1)]:
+        assert wq.wq_gemm_regime(4, M, 2560, 2560) == want
 
 
 # --------------------------------------------------------- exact cases ---
 @pytest.mark.parametrize("bits", [4, 8])
 @pytest.mark.parametrize("K", [128, 256])
-def test_identity_probe_bit_exact(wq, bits, K):
+def test_identity_probe_bit_exact(wq, small_kernel, bits, K):
     """X = I recovers bf16(s * q) exactly (identity probe of the W8A16
     card's fused-KV patch)."""
     N = 128
@@ -65,7 +80,7 @@ def test_identity_probe_bit_exact(wq, bits, K):
 
 
 @pytest.mark.parametrize("bits", [4, 8])
-def test_integer_exact_bruteforce_bit_exact(wq, bits):
+def test_integer_exact_bruteforce_bit_exact(wq, small_kernel, bits):
     """Powers-of-two scales and small integer X: every partial sum is exact,
     so the GPU result must be the oracle's value rounded once to bf16."""
     M, K, N = 16, 1024, 256
@@ -97,7 +112,7 @@ def test_m_zero_is_a_noop(wq):
 
 
 @pytest.mark.parametrize("bits", [4, 8])
-def test_output_rows_beyond_m_untouched_and_deterministic(wq, bits):
+def test_output_rows_beyond_m_untouched_and_deterministic(wq, small_kernel, bits):
     M, K, N = 5, 1280, 640
     X, q, s = synth.small_case(M, K, N, bits, seed=31)
     Wp = wq.pack_codes(i8_to_dev(q), bits)
@@ -114,7 +129,7 @@ def test_output_rows_beyond_m_untouched_and_deterministic(wq, bits):
 
 
 @pytest.mark.parametrize("bits", [4, 8])
-def test_every_cluster_split(wq, bits):
+def test_every_cluster_split(wq, small_kernel, bits):
     """Force each K split 1..8 of the cluster reduction on a ragged shape."""
     M, K, N = 9, 1152, 320   # 9 groups, 5 tiles
     X, q, s = synth.small_case(M, K, N, bits, seed=44)

@@ -25,9 +25,11 @@ std::atomic<int> g_force_regime{-1};
 // M runs on the tensor-core kernel.
 constexpr int64_t kSmallMaxM = 32;
 
+// 0: warp-MMA small-M kernel (16 rows per launch), 1: tensor-core tiled
+// kernel, 2: tensor-memory small-M kernel (16 rows per launch).
 int pick_regime(int64_t M) {
   const int f = g_force_regime.load();
-  if (f == 0 || f == 1) return f;
+  if (f >= 0 && f <= 2) return f;
   return M <= kSmallMaxM ? 0 : 1;
 }
 thread_local cudaError_t t_last_cuda = cudaSuccess;
@@ -126,14 +128,18 @@ wq_status gemm_common(int bits, const void* X, const uint32_t* Wp,
     if (e == cudaErrorNotSupported) return WQ_ERR_UNSUPPORTED;
     return cuda_status(e);
   }
-  // The small-M kernel takes up to 16 rows per launch; taller inputs are
+  // The small-M kernels take up to 16 rows per launch; taller inputs are
   // processed in 16-row slices.
+  const int regime = pick_regime(M);
   const size_t xrow = static_cast<size_t>(K) * 2, yrow = static_cast<size_t>(N) * 2;
   for (int64_t m0 = 0; m0 < M; m0 += 16) {
     a.X = static_cast<const char*>(X) + m0 * xrow;
     a.Y = static_cast<char*>(Y) + m0 * yrow;
     a.M = (M - m0) < 16 ? (M - m0) : 16;
-    cudaError_t e = wq::launch_gemm_small(a, stream);
+    cudaError_t e = cudaErrorNotSupported;
+    if (regime == 2) e = wq::launch_gemm_skinny(a, stream);
+    // shapes the tensor-memory kernel cannot index go to the warp-MMA kernel
+    if (regime == 0 || e == cudaErrorNotSupported) e = wq::launch_gemm_small(a, stream);
     if (e == cudaErrorNotSupported) return WQ_ERR_SHAPE;
     if (e != cudaSuccess) return cuda_status(e);
   }
@@ -255,13 +261,15 @@ void wq_debug_set_split(int cs) { g_split_hint.store(cs < 0 || cs > 8 ? 0 : cs);
 void wq_set_programmatic_launch(int on) { g_pdl.store(on ? 1 : 0); }
 
 void wq_debug_force_regime(int regime) {
-  g_force_regime.store(regime == 0 || regime == 1 ? regime : -1);
+  g_force_regime.store(regime >= 0 && regime <= 2 ? regime : -1);
 }
 
 int wq_gemm_regime(int bits, int64_t M, int64_t N, int64_t K) {
   if ((bits != 4 && bits != 8) || M < 0 || check_kn(K, N) != WQ_OK) return -1;
-  if (pick_regime(M) == 1) return 1;
-  return wq::gemm_small_fits(bits, K, N, g_split_hint.load()) ? 0 : -1;
+  int r = pick_regime(M);
+  if (r == 2 && (bits == 4 ? K * N / 256 : K * N / 128) > INT32_MAX) r = 0;
+  if (r == 0 && !wq::gemm_small_fits(bits, K, N, g_split_hint.load())) return -1;
+  return r;
 }
 
 }  // extern "C"

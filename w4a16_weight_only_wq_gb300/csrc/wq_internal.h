@@ -42,6 +42,9 @@ struct GemmArgs {
 cudaError_t launch_gemm_small(const GemmArgs& a, cudaStream_t stream);
 bool gemm_small_fits(int bits, int64_t K, int64_t N, int split_hint);
 
+// Tensor-memory GEMM for M <= 16 (wq_gemm_skinny.cu).
+cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t stream);
+
 // Tensor-core GEMM for large M (wq_gemm_tc.cu).
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t stream);
 
