@@ -78,3 +78,5 @@ def test_regime_selection_is_host_logic(wq):
                           (4, 8192, 2560, 9728)):
         assert wq.wq_gemm_regime(bits, M, N, K) in (0, 1)
     assert wq.wq_gemm_regime(4, 16, 96, 128) == -1
+    # a small-M shape whose X slice cannot fit shared memory runs tiled
+    assert wq.wq_gemm_regime(4, 16, 64, 128 * 1000) == 1

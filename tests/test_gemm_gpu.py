@@ -57,6 +57,16 @@ def test_small_shapes(wq, small_kernel, bits, M, K, N):
     _run_codes_case(wq, X, q, s, bits)
 
 
+@pytest.mark.parametrize("bits", [4, 8])
+def test_small_m_long_k_falls_back_to_tiled(wq, bits):
+    """K = 128000 with one column tile: X of a CTA's K range does not fit
+    the small-M kernel's shared memory, so the tiled kernel runs it."""
+    M, K, N = 16, 128 * 1000, 64
+    assert wq.wq_gemm_regime(bits, M, N, K) == 1
+    X, q, s = synth.small_case(M, K, N, bits, seed=91 + bits)
+    _run_codes_case(wq, X, q, s, bits)
+
+
 def test_default_kernel_choice(wq):
     for M, want in [(1, 0), (16, 0), (32, 0), (33, 1), (8192, 1)]:
         assert wq.wq_gemm_regime(4, M, 2560, 2560) == want

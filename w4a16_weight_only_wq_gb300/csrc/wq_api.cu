@@ -123,14 +123,15 @@ wq_status gemm_common(int bits, const void* X, const uint32_t* Wp,
   a.pdl = g_pdl.load();
   a.split_hint = g_split_hint.load();
   a.diag = diag_for(d);
-  if (pick_regime(M) == 1) {
+  int regime = pick_regime(M);
+  if (regime == 0 && !wq::gemm_small_fits(bits, K, N, a.split_hint)) regime = 1;
+  if (regime == 1) {
     cudaError_t e = wq::launch_gemm_tc(a, stream);
     if (e == cudaErrorNotSupported) return WQ_ERR_UNSUPPORTED;
     return cuda_status(e);
   }
   // The small-M kernels take up to 16 rows per launch; taller inputs are
   // processed in 16-row slices.
-  const int regime = pick_regime(M);
   const size_t xrow = static_cast<size_t>(K) * 2, yrow = static_cast<size_t>(N) * 2;
   for (int64_t m0 = 0; m0 < M; m0 += 16) {
     a.X = static_cast<const char*>(X) + m0 * xrow;
@@ -268,7 +269,8 @@ int wq_gemm_regime(int bits, int64_t M, int64_t N, int64_t K) {
   if ((bits != 4 && bits != 8) || M < 0 || check_kn(K, N) != WQ_OK) return -1;
   int r = pick_regime(M);
   if (r == 2 && (bits == 4 ? K * N / 256 : K * N / 128) > INT32_MAX) r = 0;
-  if (r == 0 && !wq::gemm_small_fits(bits, K, N, g_split_hint.load())) return -1;
+  // shapes whose X slice does not fit the small-M kernel run on the tiled one
+  if (r == 0 && !wq::gemm_small_fits(bits, K, N, g_split_hint.load())) r = 1;
   return r;
 }
 

@@ -150,6 +150,15 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
+// Split cluster barrier: arrive early (relaxed: orders nothing), wait later
+// (acquire).  Every thread of every CTA of the cluster takes part.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Address of the same shared variable in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t dsmem_map(const void* p, uint32_t rank) {
   uint32_t out;
@@ -166,6 +175,10 @@ __device__ __forceinline__ float dsmem_ld_f32(uint32_t cluster_addr) {
                : "r"(cluster_addr)
                : "memory");
   return v;
+}
+
+__device__ __forceinline__ void dsmem_st_f32(uint32_t cluster_addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
 }
 
 // ----------------------------------------------------------- warp MMA ---

@@ -8,23 +8,25 @@
 //
 //  * Work unit: a 64-column tile x a contiguous range of 128-deep groups.
 //    A thread-block cluster of `cs` CTAs shares one tile and splits its K
-//    range; the partial sums meet in distributed shared memory and are
-//    added in rank order (deterministic, no global workspace).  The split is
-//    chosen so that every CTA of the grid is resident at once (one per SM).
-//  * A producer warp fills a ring of shared-memory slots, one group per
-//    slot: the tile's packed cell (4 KiB INT4 / 8 KiB INT8, contiguous) by
-//    one bulk copy (TMA, no tensor map), and the group's 16 rows of X and 64
-//    scales by 16-byte LDGSTS (cp.async).  The slot's "full" mbarrier
-//    completes when the bulk bytes have landed and every producer lane's
-//    cp.async have landed; an "empty" mbarrier hands the slot back.
+//    range; each CTA pushes its partial sums into the owning CTA's shared
+//    memory (distributed shared memory), where they are added in rank order
+//    (deterministic, no global workspace).  The split is chosen so that
+//    every CTA of the grid is resident at once (one per SM).
+//  * Copies are few and large, because the copy engine of an SM issues one
+//    copy every ~30 ns whatever its size: the tile's packed cells over the
+//    CTA's K range are contiguous, so a chunk of four groups (16 KiB INT4 /
+//    32 KiB INT8) is one bulk copy, and X is one bulk copy per row for the
+//    whole K range.  The producer warp issues weight chunk 0, waits for the
+//    preceding kernel (programmatic launch), issues X, then the rest of the
+//    weight ring; scales travel with their chunk (16-byte cp.async).
 //  * Sixteen consumer warps each take half a group (32 columns) at a time.
 //    Dequant happens in registers: one LOP3 turns two 4-bit fields into the
 //    bf16 values 128 + u (INT8: 128 + lo and 2048 + 16 hi), one exact
 //    bf16x2 subtract removes the bias, and the codes feed mma.sync m16n8k16
-//    (bf16 in, fp32 accumulate) as the B operand; A is X read from the slot.
-//    The group's partial is scaled by s[group, n] in fp32 and accumulated.
-//  * X rows sit 320 bytes apart in a slot so that the 16-byte fragment loads
-//    of a warp hit distinct banks.
+//    (bf16 in, fp32 accumulate) as the B operand; A is X read from shared
+//    memory.  The group's partial is scaled by s[group, n] in fp32.
+//  * X rows sit (256 x groups + 64) bytes apart, 64 modulo 128, so that the
+//    16-byte fragment loads of a quarter-warp hit distinct banks.
 #include <cuda_bf16.h>
 
 #include <atomic>
@@ -39,19 +41,18 @@ namespace {
 constexpr int kConsumerWarps = 16;
 constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kXRowStride = 320;  // bytes
-constexpr int kXBytes = 16 * kXRowStride;
-constexpr int kPartBytes = 16 * 64 * 4;
-constexpr int kRedStride = 33;  // floats per row of a half-tile partial
+constexpr int kChunk = 4;                  // groups per weight chunk
+constexpr int kRedStride = 33;             // floats per row of a half-tile partial
 constexpr int kRedBytes = kConsumerWarps * 16 * kRedStride * 4;
+constexpr int kPartFloats = 1024 + 8;      // cs slices of ceil(1024 / cs) floats
 
 template <int BITS>
 struct Cell {
   static constexpr int kWords = BITS == 4 ? 1024 : 2048;
   static constexpr int kBytes = kWords * 4;
-  static constexpr int kScaleOff = kBytes;
-  static constexpr int kXOff = kBytes + 128;
-  static constexpr int kSlot = kXOff + kXBytes;
+  // weight chunk slot: kChunk cells, then kChunk x 64 scales
+  static constexpr int kSlot = kChunk * kBytes + kChunk * 128;
+  static constexpr int kScaleOff = kChunk * kBytes;
 };
 
 struct SmallParams {
@@ -59,21 +60,26 @@ struct SmallParams {
   const uint32_t* Wp;
   const uint16_t* S;
   __nv_bfloat16* Y;
-  int M, N, K, G, cs, slots;
+  int M, N, K, G, cs, wslots, xstride;
   KernelDiag diag;
 };
 
-__host__ __device__ constexpr int slot_region(int slots, int slot_bytes) {
-  return slots * slot_bytes > kRedBytes ? slots * slot_bytes : kRedBytes;
+// Shared memory: [weight ring | CTA reduction][X rows][part][barriers]
+__host__ __device__ constexpr int wregion_bytes(int wslots, int slot) {
+  return wslots * slot > kRedBytes ? wslots * slot : kRedBytes;
 }
-__host__ __device__ constexpr int smem_bytes_for(int slots, int slot_bytes) {
-  return slot_region(slots, slot_bytes) + kPartBytes + (2 * slots + 1) * 8 + 16;
+__host__ __device__ constexpr int smem_bytes_for(int wslots, int slot, int xstride) {
+  return wregion_bytes(wslots, slot) + 16 * xstride + kPartFloats * 4 + (2 * wslots + 2) * 8 + 16;
 }
+// X row stride for ng groups: 256 bytes per group, plus 64 so that rows g
+// and g + 1 sit 64 bytes apart modulo 128 (conflict-free fragment loads).
+__host__ __device__ constexpr int x_stride(int ng) { return ng * 256 + 64; }
 
 // Half a group (slabs 4h .. 4h+3, 32 columns) of one 64-column tile:
 // tmp = X_group . codes, then acc += s[group, n] * tmp per output column.
 template <int BITS>
 __device__ __forceinline__ void process_half(float (&acc)[4][4], uint32_t slot_addr,
+                                             uint32_t s_addr, uint32_t x_addr, int xstride,
                                              int half, int lane) {
   using C = Cell<BITS>;
   constexpr uint32_t kMask = 0x000F000Fu;
@@ -83,8 +89,8 @@ __device__ __forceinline__ void process_half(float (&acc)[4][4], uint32_t slot_a
   constexpr uint32_t kB8Lo = 0x43004300u;  // 128
   constexpr uint32_t kB8Hi = 0x45084508u;  // 2176 = 2048 + 128
   const int g = lane >> 2, t4 = lane & 3;
-  const uint32_t xa_addr = slot_addr + C::kXOff + g * kXRowStride + 16 * t4;
-  const uint32_t xb_addr = xa_addr + 8 * kXRowStride;
+  const uint32_t xa_addr = x_addr + g * xstride + 16 * t4;
+  const uint32_t xb_addr = xa_addr + 8 * xstride;
   const float zero[4] = {0.f, 0.f, 0.f, 0.f};
   float tmp[4][4];
 
@@ -151,7 +157,7 @@ __device__ __forceinline__ void process_half(float (&acc)[4][4], uint32_t slot_a
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
     const int tt = half * 4 + t;
-    const uint32_t s2 = ld_shared_u32(slot_addr + C::kScaleOff + (tt * 8 + 2 * t4) * 2);
+    const uint32_t s2 = ld_shared_u32(s_addr + (tt * 8 + 2 * t4) * 2);
     const float s0 = bf16_lo_to_f32(s2), s1 = bf16_hi_to_f32(s2);
     acc[t][0] = fmaf(s0, tmp[t][0], acc[t][0]);
     acc[t][1] = fmaf(s1, tmp[t][1], acc[t][1]);
@@ -166,37 +172,40 @@ gemm_small_kernel(const SmallParams p) {
   using C = Cell<BITS>;
   extern __shared__ __align__(16) uint8_t smem[];
 
-  const int cs = p.cs, D = p.slots;
+  const int cs = p.cs, DW = p.wslots, xs = p.xstride;
   const int tile = blockIdx.x / cs;
   const int rank = blockIdx.x % cs;  // == %cluster_ctarank for cluster (cs,1,1)
   const int g0 = (p.G * rank) / cs;
   const int ng = (p.G * (rank + 1)) / cs - g0;
+  const int nch = (ng + kChunk - 1) / kChunk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Each consumer warp owns one half (32 columns) of the tile.
   const int half = warp & 1;
+  const int rows = min(16, p.M);
 
-  // Same offsets in every CTA of the cluster (`part` is read remotely).
-  uint8_t* slots = smem;
-  float* red = reinterpret_cast<float*>(smem);  // aliases the drained slots
-  const int region = slot_region(D, C::kSlot);
-  float* part = reinterpret_cast<float*>(smem + region);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + region + kPartBytes);
-  uint64_t* empty = full + D;
-  uint64_t* never_bar = empty + D;  // test hook: nothing ever arrives here
+  uint8_t* wring = smem;
+  float* red = reinterpret_cast<float*>(smem);  // aliases the drained weight ring
+  const int wregion = wregion_bytes(DW, C::kSlot);
+  uint8_t* xbuf = smem + wregion;
+  float* part = reinterpret_cast<float*>(xbuf + 16 * xs);
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(part + kPartFloats);
+  uint64_t* wempty = wfull + DW;
+  uint64_t* xfull = wempty + DW;
+  uint64_t* never_bar = xfull + 1;
   int& s_err = *reinterpret_cast<int*>(never_bar + 1);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < D; ++i) {
-      mbar_init(&full[i], 1 + 32);  // bulk-copy arrival + one per producer lane
-      mbar_init(&empty[i], 2);      // both halves consumed
+    for (int i = 0; i < DW; ++i) {
+      mbar_init(&wfull[i], 1 + 32);       // bulk-copy arrival + one per producer lane
+      mbar_init(&wempty[i], 2 * kChunk);  // both halves of every group of the chunk
     }
+    mbar_init(xfull, 1);
     mbar_init(never_bar, 1);
     fence_mbar_init();
     s_err = 0;
   }
   __syncthreads();
-  // Test hook 1: a wait that nothing completes runs out, reports, and the
-  // kernel then carries on normally.
+  // Every CTA of the cluster has started before any remote store (below).
+  if (cs > 1) cluster_arrive_relaxed();
   if (p.diag.force_timeout == 1) mbar_wait_bounded(never_bar, 0, p.diag);
 
   float acc[4][4];
@@ -205,55 +214,54 @@ gemm_small_kernel(const SmallParams p) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) acc[t][c] = 0.f;
 
-  int issued = 0;  // producer: groups whose copies were issued
+  int issued = 0;  // producer: chunks whose copies were issued
   if (warp == kProducerWarp) {
     // ------------------------------------------------------- producer ---
-    // Weights are not written by the preceding kernel, so the first round
-    // of cells is fetched before the programmatic-launch dependency
-    // resolves; X (which may be) is fetched after it.
-    const int first = min(ng, D);
-    const int mrows = min(p.M, 16);
-    auto issue_w = [&](int i, int slot) {
-      mbar_arrive_expect_tx(&full[slot], C::kBytes);
-      bulk_g2s(slots + slot * C::kSlot,
-               p.Wp + (static_cast<size_t>(tile) * p.G + g0 + i) * C::kWords, C::kBytes,
-               &full[slot]);
-    };
-    auto issue_xs = [&](int i, int slot) {
-      const int g = g0 + i;
-      const uint32_t base = smem_addr(slots + slot * C::kSlot);
-#pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        const int c = lane + 32 * it, row = c >> 4, col = c & 15;
-        const bool live = row < mrows;
-        const __nv_bfloat16* src =
-            live ? p.X + static_cast<size_t>(row) * p.K + static_cast<size_t>(g) * 128 + col * 8
-                 : p.X;
-        cp_async_16(base + C::kXOff + row * kXRowStride + col * 16, src, live ? 16u : 0u);
+    // Weights and scales do not depend on the preceding kernel: the first
+    // ring of chunks is requested before the programmatic-launch wait.
+    auto issue_chunk = [&](int c) {
+      const int slot = c % DW;
+      const int gc = min(kChunk, ng - c * kChunk);  // groups in this chunk
+      uint8_t* dst = wring + slot * C::kSlot;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&wfull[slot], gc * C::kBytes);
+        bulk_g2s(dst, p.Wp + (static_cast<size_t>(tile) * p.G + g0 + c * kChunk) * C::kWords,
+                 gc * C::kBytes, &wfull[slot]);
       }
-      if (lane < 8)
-        cp_async_16(base + C::kScaleOff + lane * 16,
-                    p.S + static_cast<size_t>(g) * p.N + tile * 64 + lane * 8, 16u);
-      cp_async_mbar_arrive_noinc(&full[slot]);
+      // scales: gc x 128 bytes, 16 bytes per lane (up to kChunk x 8 pieces)
+      for (int piece = lane; piece < gc * 8; piece += 32) {
+        const int gi = piece >> 3, part16 = piece & 7;
+        cp_async_16(smem_addr(dst + C::kScaleOff + gi * 128 + part16 * 16),
+                    p.S + static_cast<size_t>(g0 + c * kChunk + gi) * p.N + tile * 64 + part16 * 8,
+                    16u);
+      }
+      cp_async_mbar_arrive_noinc(&wfull[slot]);
     };
-    if (lane == 0)
-      for (int i = 0; i < first; ++i) issue_w(i, i);
+    // Chunk 0 first, then (once the preceding kernel is done) X, so that the
+    // first group can start as early as possible; then the rest of the ring.
+    const int first = min(nch, DW);
+    issue_chunk(0);
     pdl_launch_dependents();
     pdl_wait_primary();
-    for (int i = 0; i < first; ++i) issue_xs(i, i);
+    // X: the rows' whole K range of this CTA, one bulk copy per row.
+    if (lane == 0) mbar_arrive_expect_tx(xfull, rows * ng * 256);
+    __syncwarp();
+    if (lane < rows)
+      bulk_g2s(xbuf + lane * xs, p.X + static_cast<size_t>(lane) * p.K + static_cast<size_t>(g0) * 128,
+               ng * 256, xfull);
+    for (int c = 1; c < first; ++c) issue_chunk(c);
     issued = first;
-    for (int i = D; i < ng; ++i) {
-      const int slot = i % D;
-      int e_ok = 1;
-      if (lane == 0) e_ok = mbar_wait_bounded(&empty[slot], ((i / D) - 1) & 1, p.diag);
-      e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
-      if (!e_ok) {
+    for (int c = first; c < nch; ++c) {
+      const int slot = c % DW;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait_bounded(&wempty[slot], ((c / DW) - 1) & 1, p.diag);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
         s_err = 1;
         break;
       }
-      if (lane == 0) issue_w(i, slot);
-      issue_xs(i, slot);
-      issued = i + 1;
+      issue_chunk(c);
+      issued = c + 1;
     }
     cp_async_wait_all();
   } else {
@@ -261,35 +269,40 @@ gemm_small_kernel(const SmallParams p) {
     pdl_wait_primary();  // consumers store Y, which the preceding kernel may use
     // ------------------------------------------------------ consumers ---
     // Warp w handles half (w & 1) of groups (w >> 1), (w >> 1) + 8, ...
+    bool have_x = false;
     for (int i = warp >> 1; i < ng; i += kConsumerWarps / 2) {
-      const int slot = i % D;
-      // Test hook 2: look for the phase after the real one, which never
-      // completes, so the give-up-and-drain path runs.
-      const uint32_t parity = ((i / D) + (p.diag.force_timeout == 2 ? 1 : 0)) & 1;
-      if (!mbar_wait_bounded(&full[slot], parity, p.diag)) {
+      const int c = i / kChunk, slot = c % DW, gi = i % kChunk;
+      // Test hook 2: halfway through, wait on a barrier nothing completes,
+      // so that the give-up-and-drain path runs with copies in flight.
+      const bool hook = p.diag.force_timeout == 2 && i == ng / 2;
+      if (!mbar_wait_bounded(hook ? never_bar : &wfull[slot], hook ? 0u : (c / DW) & 1, p.diag) ||
+          (!have_x && !mbar_wait_bounded(xfull, 0, p.diag))) {
         s_err = 1;  // stop here; the slot is not handed back
         break;
       }
-      process_half<BITS>(acc, smem_addr(slots + slot * C::kSlot), half, lane);
+      have_x = true;
+      const uint32_t wbase = smem_addr(wring + slot * C::kSlot);
+      process_half<BITS>(acc, wbase + gi * C::kBytes, wbase + C::kScaleOff + gi * 128,
+                         smem_addr(xbuf) + i * 256, xs, half, lane);
       __syncwarp();
       if (lane == 0) {
         fence_proxy_async_smem();  // our reads of the slot precede its refill
-        mbar_arrive(&empty[slot]);
+        mbar_arrive(&wempty[slot]);
       }
     }
   }
   __syncthreads();
   if (s_err) {
-    // Some wait gave up: let the latest fill of every slot land (bounded,
-    // at least 1 s) before the shared memory is reused or released.  Phases
-    // of a slot complete in order, so the latest one covers the earlier.
+    // Some wait gave up: let every issued copy land (bounded, at least 1 s)
+    // before the shared memory is reused or released.
     if (warp == kProducerWarp && lane == 0) {
       KernelDiag drain = p.diag;
       if (drain.wait_limit_ns < 1000000000ull) drain.wait_limit_ns = 1000000000ull;
-      for (int slot = 0; slot < D && slot < issued; ++slot) {
-        const int last = slot + ((issued - 1 - slot) / D) * D;
-        mbar_wait_bounded(&full[slot], (last / D) & 1, drain);
+      for (int slot = 0; slot < DW && slot < issued; ++slot) {
+        const int last = slot + ((issued - 1 - slot) / DW) * DW;
+        mbar_wait_bounded(&wfull[slot], (last / DW) & 1, drain);
       }
+      mbar_wait_bounded(xfull, 0, drain);
     }
     __syncthreads();
   }
@@ -310,32 +323,36 @@ gemm_small_kernel(const SmallParams p) {
     }
   }
   __syncthreads();
-  const int rows = min(16, p.M);
-  for (int e = threadIdx.x; e < 1024; e += kThreads) {
+  // Element e = row * 64 + col of the tile.  With a cluster, rank r owns
+  // elements [r E / cs, (r + 1) E / cs) and receives every rank's partial
+  // of them in its `part` (slice q at q * slice), by remote stores.
+  const int E = rows * 64;
+  const int slice = (E + cs - 1) / cs;
+  if (cs > 1) cluster_wait();
+  for (int e = threadIdx.x; e < E; e += kThreads) {
     const int r = e >> 6, c = e & 63, h = c >> 5, cc = c & 31;
     float v = 0.f;
 #pragma unroll
     for (int k = 0; k < kConsumerWarps / 2; ++k)
       v += red[(2 * k + h) * 16 * kRedStride + r * kRedStride + cc];
     if (cs == 1) {
-      if (r < rows)
-        p.Y[static_cast<size_t>(r) * p.N + tile * 64 + c] = __float2bfloat16_rn(v);
+      p.Y[static_cast<size_t>(r) * p.N + tile * 64 + c] = __float2bfloat16_rn(v);
     } else {
-      part[e] = v;
+      int owner = (e * cs) / E;  // first rank whose range holds e
+      while (owner + 1 < cs && e >= ((owner + 1) * E) / cs) ++owner;
+      while (e < (owner * E) / cs) --owner;
+      const int off = e - (owner * E) / cs;
+      dsmem_st_f32(dsmem_map(part + rank * slice + off, owner), v);
     }
   }
   if (cs == 1) return;
-
-  // Cluster reduction: CTA `rank` finalises elements [rank*E/cs, ...) of
-  // the tile's E = rows x 64 outputs, adding the cs partials in rank order.
-  cluster_sync();
-  const int e_end = (rows * 64 * (rank + 1)) / cs;
-  for (int e = (rows * 64 * rank) / cs + threadIdx.x; e < e_end; e += kThreads) {
+  cluster_sync();  // every partial has arrived in its owner's `part`
+  const int e0 = (rank * E) / cs, e1 = ((rank + 1) * E) / cs;
+  for (int e = e0 + threadIdx.x; e < e1; e += kThreads) {
     float v = 0.f;
-    for (int q = 0; q < cs; ++q) v += dsmem_ld_f32(dsmem_map(part + e, q));
+    for (int q = 0; q < cs; ++q) v += part[q * slice + (e - e0)];
     p.Y[static_cast<size_t>(e >> 6) * p.N + tile * 64 + (e & 63)] = __float2bfloat16_rn(v);
   }
-  cluster_sync();  // keep this CTA's `part` alive until every peer has read it
 }
 
 // ------------------------------------------------------------ host side ---
@@ -373,16 +390,6 @@ KernelInit<8> g_init8;
 
 int slot_bytes(int bits) { return bits == 4 ? Cell<4>::kSlot : Cell<8>::kSlot; }
 
-// Ring depth: every group of the CTA when it fits, else as many slots as
-// the shared memory holds.
-int ring_slots(int bits, int ng_max, int max_dyn) {
-  const int sb = slot_bytes(bits);
-  int d = (max_dyn - kPartBytes - 64) / (sb + 16);
-  if (ng_max < d) d = ng_max;
-  while (d > 0 && smem_bytes_for(d, sb) > max_dyn) --d;
-  return d;
-}
-
 // Cluster split along K: the largest cs in 1..8 (and <= groups) for which
 // tiles * cs CTAs still fit one per SM, so the whole grid is resident and
 // the per-SM share of cells is as even as the shape allows.
@@ -398,8 +405,13 @@ int choose_split(int64_t K, int64_t N, int num_sms, int hint) {
 }  // namespace
 
 bool gemm_small_fits(int bits, int64_t K, int64_t N, int split_hint) {
-  (void)bits;
-  return choose_split(K, N, 152, split_hint) > 0;
+  const int cs = choose_split(K, N, 152, split_hint);
+  if (cs <= 0) return false;
+  // X for the CTA's K range and at least one weight chunk must fit the
+  // 227 KiB a CTA may use on sm_103.
+  const int64_t ng_max = (K / 128 + cs - 1) / cs;
+  if (ng_max > 4096) return false;
+  return smem_bytes_for(1, slot_bytes(bits), x_stride(static_cast<int>(ng_max))) <= 232448;
 }
 
 cudaError_t launch_gemm_small(const GemmArgs& a, cudaStream_t stream) {
@@ -421,8 +433,14 @@ cudaError_t launch_gemm_small(const GemmArgs& a, cudaStream_t stream) {
   p.K = static_cast<int>(a.K);
   p.G = static_cast<int>(a.K / 128);
   p.cs = cs;
-  p.slots = ring_slots(a.bits, (p.G + cs - 1) / cs, max_dyn);
-  if (p.slots < 1) return cudaErrorNotSupported;
+  const int ng_max = (p.G + cs - 1) / cs;
+  const int nch_max = (ng_max + kChunk - 1) / kChunk;
+  const int sb = slot_bytes(a.bits);
+  p.xstride = x_stride(ng_max);
+  int dw = nch_max;
+  while (dw > 0 && smem_bytes_for(dw, sb, p.xstride) > max_dyn) --dw;
+  if (dw < 1) return cudaErrorNotSupported;
+  p.wslots = dw;
   p.diag.err = a.diag.err;
   p.diag.wait_limit_ns = a.diag.wait_limit_ns;
   p.diag.force_timeout = a.diag.force_timeout;
@@ -430,7 +448,7 @@ cudaError_t launch_gemm_small(const GemmArgs& a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((a.N / 64) * cs));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_bytes_for(p.slots, slot_bytes(a.bits));
+  cfg.dynamicSmemBytes = smem_bytes_for(p.wslots, sb, p.xstride);
   cfg.stream = stream;
   cudaLaunchAttribute attrs[2];
   int na = 0;
