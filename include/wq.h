@@ -162,9 +162,12 @@ WQ_API void wq_debug_set_split(int cs);
 WQ_API void wq_set_programmatic_launch(int on);
 
 /* Test hook: run every GEMM on one kernel family regardless of M (0 the
-   warp-MMA small-M kernel, 1 the tiled tensor-core kernel, 2 the
-   tensor-memory small-M kernel; any other value restores the automatic
-   choice: M <= 32 kernel 0 in 16-row slices, larger M kernel 1). */
+   warp-MMA small-M kernel, 1 the tiled tensor-core kernel with dequantised
+   weights in shared memory, 2 the tensor-memory small-M kernel, 3 the
+   tiled tensor-core kernel with dequantised weights in tensor memory, which
+   needs K/128 to be a multiple of 4 (INT4) or 2 (INT8) and otherwise falls
+   back to 1; any other value restores the automatic choice: M <= 32
+   kernel 0 in 16-row slices, 32 < M <= 384 kernel 3, larger M kernel 1). */
 WQ_API void wq_debug_force_regime(int regime);
 
 /* Which kernel family a GEMM of this shape runs (numbering as in

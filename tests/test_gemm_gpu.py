@@ -68,7 +68,7 @@ def test_small_m_long_k_falls_back_to_tiled(wq, bits):
 
 
 def test_default_kernel_choice(wq):
-    for M, want in [(1, 0), (16, 0), (32, 0), (33, 1), (8192, 1)]:
+    for M, want in [(1, 0), (16, 0), (32, 0), (33, 3), (384, 3), (385, 1), (8192, 1)]:
         assert wq.wq_gemm_regime(4, M, 2560, 2560) == want
 
 
@@ -250,3 +250,84 @@ def test_tc_deterministic_and_rows_beyond_m_untouched(wq, tc_regime):
     torch.cuda.synchronize()
     assert torch.all(canary[M:] == 3.0)
     assert torch.equal(canary[:M], Y2)
+
+
+# ------------------------------- tensor-core kernel, weights in tensor memory ---
+@pytest.fixture
+def wt_regime(wq):
+    wq.wq_debug_force_regime(3)
+    yield
+    wq.wq_debug_force_regime(-1)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M,K,N", [(1, 512, 64), (100, 1024, 320), (129, 512, 576),
+                                   (300, 1536, 256), (256, 2560, 512), (16, 1024, 192)])
+def test_wt_ragged_shapes(wq, wt_regime, bits, M, K, N):
+    assert wq.wq_gemm_regime(bits, M, N, K) == 3
+    X, q, s = synth.small_case(M, K, N, bits, seed=M + K + N + 3 * bits)
+    _run_codes_case(wq, X, q, s, bits)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_wt_unsupported_depth_falls_back(wq, wt_regime, bits):
+    """K / 128 = 5 is not a multiple of the packed chunk: the tiled kernel
+    with weights in shared memory runs instead."""
+    M, K, N = 40, 640, 128
+    assert wq.wq_gemm_regime(bits, M, N, K) == 1
+    X, q, s = synth.small_case(M, K, N, bits, seed=5)
+    _run_codes_case(wq, X, q, s, bits)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_wt_identity_probe_bit_exact(wq, wt_regime, bits):
+    """X = I through the tensor-memory kernel gives bf16(s*q) exactly."""
+    K, N = 512, 320
+    _, q, s = synth.small_case(1, K, N, bits, seed=15 + bits)
+    eye = oracle.f32_to_bf16_bits(np.eye(K, dtype=np.float32))
+    Wp = wq.pack_codes(i8_to_dev(q), bits)
+    Y = _gemm(wq, bits, bf16_to_dev(eye), Wp, bf16_to_dev(s))
+    torch.cuda.synchronize()
+    Yref = oracle.gemm(eye, oracle.pack(q, bits), s, K, N, bits)
+    want = oracle.f32_to_bf16_bits(Yref.astype(np.float32))
+    assert np.array_equal(bf16_to_host_bits(Y), want)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_wt_integer_exact_bit_exact(wq, wt_regime, bits):
+    M, K, N = 200, 1024, 512
+    rng = np.random.default_rng(33 + bits)
+    lo, hi = (-8, 7) if bits == 4 else (-128, 127)
+    q = rng.integers(lo, hi + 1, size=(K, N)).astype(np.int8)
+    s = oracle.f32_to_bf16_bits(
+        (2.0 ** rng.integers(-8, -2, size=(K // 128, N))).astype(np.float32))
+    X = oracle.f32_to_bf16_bits(rng.integers(-4, 5, size=(M, K)).astype(np.float32))
+    Wp = wq.pack_codes(i8_to_dev(q), bits)
+    Y = _gemm(wq, bits, bf16_to_dev(X), Wp, bf16_to_dev(s))
+    torch.cuda.synchronize()
+    Yref = oracle.gemm(X, oracle.pack(q, bits), s, K, N, bits)
+    want = oracle.f32_to_bf16_bits(Yref.astype(np.float32))
+    assert np.array_equal(bf16_to_host_bits(Y), want)
+
+
+def test_wt_deterministic_and_rows_beyond_m_untouched(wq, wt_regime):
+    M, K, N = 130, 1024, 384
+    X, q, s = synth.small_case(M, K, N, 4, seed=78)
+    Wp = wq.pack_codes(i8_to_dev(q), 4)
+    Xt, st = bf16_to_dev(X), bf16_to_dev(s)
+    canary = torch.full((M + 5, N), 3.0, dtype=torch.bfloat16, device="cuda")
+    wq.gemm_w4a16(Xt, Wp, st, Y=canary[:M])
+    Y2 = wq.gemm_w4a16(Xt, Wp, st)
+    torch.cuda.synchronize()
+    assert torch.all(canary[M:] == 3.0)
+    assert torch.equal(canary[:M], Y2)
+
+
+@pytest.mark.parametrize("case", synth.C5, ids=_case_ids(synth.C5))
+def test_wt_workload_prefill_sampled_rows(wq, wt_regime, case):
+    d = case.draw()
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([np.arange(0, 8), np.arange(120, 136),
+                                     np.arange(case.M - 8, case.M),
+                                     rng.integers(0, case.M, 24)]))
+    _run_codes_case(wq, d["X"], d["q"], d["s"], case.bits, rows=rows)

@@ -24,13 +24,19 @@ std::atomic<int> g_force_regime{-1};
 // Rows up to which the small-M kernel (16 rows per launch) is used; larger
 // M runs on the tensor-core kernel.
 constexpr int64_t kSmallMaxM = 32;
+constexpr int64_t kTmemMaxM = 384;
 
 // 0: warp-MMA small-M kernel (16 rows per launch), 1: tensor-core tiled
-// kernel, 2: tensor-memory small-M kernel (16 rows per launch).
+// kernel with dequantised weights in shared memory, 2: tensor-memory
+// small-M kernel (16 rows per launch), 3: tensor-core tiled kernel with
+// dequantised weights in tensor memory.
 int pick_regime(int64_t M) {
   const int f = g_force_regime.load();
-  if (f >= 0 && f <= 2) return f;
-  return M <= kSmallMaxM ? 0 : 1;
+  if (f >= 0 && f <= 3) return f;
+  // measured crossovers (K = 2560, N = 9728): the tensor-memory kernel's
+  // 128-column tiles fill the GPU at small M; from M = 512 the 256-column
+  // tiles of kernel 1 (half the L2 traffic of X) are faster
+  return M <= kSmallMaxM ? 0 : M <= kTmemMaxM ? 3 : 1;
 }
 thread_local cudaError_t t_last_cuda = cudaSuccess;
 
@@ -125,6 +131,12 @@ wq_status gemm_common(int bits, const void* X, const uint32_t* Wp,
   a.diag = diag_for(d);
   int regime = pick_regime(M);
   if (regime == 0 && !wq::gemm_small_fits(bits, K, N, a.split_hint)) regime = 1;
+  if (regime == 3 && !wq::gemm_wt_fits(bits, M, K, N)) regime = 1;
+  if (regime == 3) {
+    cudaError_t e = wq::launch_gemm_wt(a, stream);
+    if (e == cudaErrorNotSupported) return WQ_ERR_UNSUPPORTED;
+    return cuda_status(e);
+  }
   if (regime == 1) {
     cudaError_t e = wq::launch_gemm_tc(a, stream);
     if (e == cudaErrorNotSupported) return WQ_ERR_UNSUPPORTED;
@@ -262,7 +274,7 @@ void wq_debug_set_split(int cs) { g_split_hint.store(cs < 0 || cs > 8 ? 0 : cs);
 void wq_set_programmatic_launch(int on) { g_pdl.store(on ? 1 : 0); }
 
 void wq_debug_force_regime(int regime) {
-  g_force_regime.store(regime >= 0 && regime <= 2 ? regime : -1);
+  g_force_regime.store(regime >= 0 && regime <= 3 ? regime : -1);
 }
 
 int wq_gemm_regime(int bits, int64_t M, int64_t N, int64_t K) {
@@ -271,6 +283,7 @@ int wq_gemm_regime(int bits, int64_t M, int64_t N, int64_t K) {
   if (r == 2 && (bits == 4 ? K * N / 256 : K * N / 128) > INT32_MAX) r = 0;
   // shapes whose X slice does not fit the small-M kernel run on the tiled one
   if (r == 0 && !wq::gemm_small_fits(bits, K, N, g_split_hint.load())) r = 1;
+  if (r == 3 && !wq::gemm_wt_fits(bits, M, K, N)) r = 1;
   return r;
 }
 

@@ -1,0 +1,565 @@
+// wq_gemm_wt.cu -- tcgen05 W4A16 / W8A16 GEMM for large M with the
+// dequantised weights in tensor memory.
+//
+// Y[M,N] = X[M,K] . (s (.) q)[K,N] ("Quantize the Target, Quantize the
+// Drafter": the INT4 target's prefill of a long prompt), computed as
+// Y^T = W^T . X^T so that the dequantised weights are the tcgen05.mma A
+// operand (M = 128 weight columns, one per TMEM lane) written straight
+// from registers into tensor memory, and X is the B operand (N = 128
+// tokens) read from shared memory.  The weights never pass through shared
+// memory as bf16, which is what bounds a kernel that stages dequantised
+// weights there: only X tiles (TMA) and packed codes (TMA) are stored in
+// shared memory, and only the MMA and the dequant warps read it.
+//
+//  * Persistent: one CTA per SM walks tiles of 128 weight columns x 128
+//    tokens; the fp32 accumulator is double-buffered in tensor memory so the
+//    epilogue of a tile overlaps the next tile's MMAs.
+//  * Producer (warp 0): packed cells of four (INT4) or two (INT8) groups of
+//    both 64-column cell columns per TMA (the packed buffer seen as rows of
+//    128 bytes, 128-byte swizzle) plus their scales (cp.async), one chunk
+//    ahead; X in 64-deep stages (TMA, 128-byte swizzle).
+//  * MMA (warp 1, one thread): per 64-deep stage, four 128x128x16 MMAs
+//    with A from tensor memory and B from the X stage.
+//  * Dequant (warps 2-17, four per TMEM lane quadrant): a thread owns one
+//    weight column of one group: LOP3 extraction of the codes, an exact
+//    bf16x2 subtraction of the offset and one bf16x2 multiply by the scale
+//    give bf16(s*q), stored with two tcgen05.st into its lane.
+//  * Epilogue (warps 18-21): tcgen05.ld of the accumulator, bf16 stores.
+//  Every wait is bounded; an abort drains copies and MMAs and frees TMEM.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "wq_device.cuh"
+#include "wq_internal.h"
+#include "wq_tcgen05.cuh"
+
+namespace wq {
+namespace {
+
+constexpr int kTN = 128;          // weight columns per tile (MMA M, TMEM lanes)
+constexpr int kTM = 128;          // tokens per tile (MMA N)
+constexpr int kNB = 8;            // X stages (64 deep) in shared memory
+constexpr int kGA = 4;            // groups of A in tensor memory
+constexpr int kNQ = 2;            // packed chunks in flight
+constexpr int kDequantWarps = 16;
+constexpr int kFirstDequantWarp = 2;
+constexpr int kFirstEpiWarp = kFirstDequantWarp + kDequantWarps;  // 18
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = (kFirstEpiWarp + kEpiWarps) * 32;        // 704
+constexpr uint32_t kTmemCols = 512;
+constexpr int kDCols = kTM;       // one accumulator: 128 fp32 columns
+constexpr int kACol = 2 * kDCols; // A slots start after the two accumulators
+constexpr int kXStage = kTM * 128;  // 16 KiB: 128 tokens x 64 bf16
+
+template <int BITS>
+struct WtCfg {
+  static constexpr int kChunk = BITS == 4 ? 4 : 2;             // groups per packed chunk
+  static constexpr int kCellBytes = BITS == 4 ? 4096 : 8192;   // 64 columns x 128 k
+  static constexpr int kCellRows = kCellBytes / 128;
+  static constexpr int kColBytes = kChunk * kCellBytes;        // one cell column of a chunk
+  static constexpr int kScaleOff = 2 * kColBytes;
+  // + scales [group][128]; a multiple of 1024 so every slot's cells keep the
+  // 1024-byte alignment the 128-byte swizzle pattern is anchored to
+  static constexpr int kQBytes = (kScaleOff + kChunk * kTN * 2 + 1023) / 1024 * 1024;
+  static constexpr int kOffX = 0;
+  static constexpr int kOffQ = kOffX + kNB * kXStage;
+  static constexpr int kOffBar = kOffQ + kNQ * kQBytes;
+  static constexpr int kNumBars = 2 * kNB + 2 * kNQ + 2 * kGA + 4 + 2;
+  static constexpr int kSmem = kOffBar + kNumBars * 8 + 32 + 1024;  // + alignment slack
+};
+
+struct WtParams {
+  const uint16_t* S;
+  __nv_bfloat16* Y;
+  int M, N, K, G;
+  int mt, nt;  // tile counts along M and N
+  KernelDiag diag;
+};
+
+// Byte offset, within one cell of a chunk, of the 16-byte packed lane
+// 4c + t4 of column n (INT8: of k half h) after the 128-byte swizzle: chunk
+// `ch` of 128-byte row `row` sits at chunk position ch ^ (row % 8).
+template <int BITS>
+__device__ __forceinline__ uint32_t wt_lane_offset(int n, int h, int t4) {
+  const int j8 = (n >> 3) & 7, c = n & 7;
+  const int row = BITS == 4 ? j8 * 4 + (c >> 1) : (j8 * 2 + h) * 4 + (c >> 1);
+  const int ch = (4 * (c & 1) + t4) ^ (row & 7);
+  return row * 128 + ch * 16;
+}
+
+// Dequantise one group (128 k) of this thread's column into bf16(s * q)
+// and store it into TMEM columns [taddr, taddr + 64) of its lane: column j
+// holds k = 2j, 2j + 1 (low half k = 2j).
+template <int BITS>
+__device__ __forceinline__ void dequant_group_to_tmem(uint32_t cell, int n, uint32_t s2,
+                                                      uint32_t taddr) {
+  constexpr uint32_t kMask = 0x000F000Fu;
+  constexpr uint32_t kLo = 0x43004300u;  // bf16 128
+  constexpr uint32_t kHi = 0x45004500u;  // bf16 2048
+  if constexpr (BITS == 4) {
+    constexpr uint32_t kB4 = 0x43084308u;  // 136
+    // lane 4c + t4 holds words kb = 0..3 of k = 32 kb + 8 t4 + 0..7
+    uint4 w[4];
+#pragma unroll
+    for (int t4 = 0; t4 < 4; ++t4) w[t4] = ld_shared_v4(cell + wt_lane_offset<4>(n, 0, t4));
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t r[32];
+#pragma unroll
+      for (int t4 = 0; t4 < 4; ++t4) {
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const int kb = 2 * h + b;
+          const uint32_t word = kb == 0 ? w[t4].x : kb == 1 ? w[t4].y : kb == 2 ? w[t4].z : w[t4].w;
+          const int col = 4 * (4 * b + t4);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            r[col + j] = bf16x2_mul(bf16x2_sub(lop3_and_or(word >> (4 * j), kMask, kLo), kB4), s2);
+        }
+      }
+      tmem_st_32x32b_x32(taddr + 32 * h, r);
+    }
+  } else {
+    constexpr uint32_t kB8Lo = 0x43004300u;  // 128
+    constexpr uint32_t kB8Hi = 0x45084508u;  // 2176 = 2048 + 128
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      // half h: lane 4c + t4 holds words wi = 0..3,
+      // k = 32 (2h + wi/2) + 8 t4 + 4 (wi & 1) + 0..3
+      uint32_t r[32];
+#pragma unroll
+      for (int t4 = 0; t4 < 4; ++t4) {
+        const uint4 w = ld_shared_v4(cell + wt_lane_offset<8>(n, h, t4));
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+          const uint32_t word = wi == 0 ? w.x : wi == 1 ? w.y : wi == 2 ? w.z : w.w;
+          const int col = 4 * (4 * (wi >> 1) + t4) + 2 * (wi & 1);
+          const uint32_t lo01 = bf16x2_sub(lop3_and_or(word, kMask, kLo), kB8Lo);
+          const uint32_t hi01 = bf16x2_sub(lop3_and_or(word >> 4, kMask, kHi), kB8Hi);
+          const uint32_t lo23 = bf16x2_sub(lop3_and_or(word >> 8, kMask, kLo), kB8Lo);
+          const uint32_t hi23 = bf16x2_sub(lop3_and_or(word >> 12, kMask, kHi), kB8Hi);
+          r[col] = bf16x2_mul(bf16x2_add(hi01, lo01), s2);
+          r[col + 1] = bf16x2_mul(bf16x2_add(hi23, lo23), s2);
+        }
+      }
+      tmem_st_32x32b_x32(taddr + 32 * h, r);
+    }
+  }
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wt_wait(uint64_t* bar, uint32_t parity, const KernelDiag& d,
+                                        volatile int* abort_flag, uint32_t hint_ns = 0) {
+  const uint32_t a = smem_addr(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (hint_ns ? mbar_try_wait_sleep(a, parity, hint_ns) : mbar_try_wait(a, parity))
+        return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > d.wait_limit_ns) {
+      atomicMax(d.err, kErrTimeout);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
+               const WtParams p) {
+  using C = WtCfg<BITS>;
+  constexpr int kChunk = C::kChunk;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* b_full = bars;                 // [kNB] X stage landed
+  uint64_t* b_empty = b_full + kNB;        // [kNB] MMAs done with it
+  uint64_t* q_full = b_empty + kNB;        // [kNQ] packed chunk + scales landed
+  uint64_t* q_empty = q_full + kNQ;        // [kNQ] chunk dequantised
+  uint64_t* a_full = q_empty + kNQ;        // [kGA] group of A written
+  uint64_t* a_empty = a_full + kGA;        // [kGA] MMAs done with it
+  uint64_t* d_full = a_empty + kGA;        // [2] accumulator finished
+  uint64_t* d_empty = d_full + 2;          // [2] accumulator read out
+  uint64_t* mma_done = d_empty + 2;       // every MMA of this CTA has completed
+  uint64_t* never_bar = mma_done + 1;      // test hook
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nch = p.G / kChunk;            // chunks per tile
+  // Tiles: this CTA takes tiles t = blockIdx.x + k gridDim.x: token tile
+  // t % mt, column tile t / mt.
+  const int cl = blockIdx.x, ncl = gridDim.x;
+  const int ptiles = p.mt * p.nt;
+  const int my_tiles = ptiles > cl ? (ptiles - 1 - cl) / ncl + 1 : 0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNB; ++i) {
+      mbar_init(&b_full[i], 1);
+      mbar_init(&b_empty[i], 1);
+    }
+    mbar_init(mma_done, 1);
+    for (int i = 0; i < kNQ; ++i) {
+      mbar_init(&q_full[i], 1 + 32);       // TMA arrival + one per producer lane (cp.async)
+      mbar_init(&q_empty[i], 4 * kChunk);  // every dequant warp that reads the chunk
+    }
+    for (int i = 0; i < kGA; ++i) {
+      mbar_init(&a_full[i], 4);            // one warp per TMEM lane quadrant
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&d_full[i], 1);
+      mbar_init(&d_empty[i], kEpiWarps);
+    }
+    mbar_init(never_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  if (p.diag.force_timeout == 1) mbar_wait_bounded(never_bar, 0, p.diag);
+
+  int issued_q = 0, issued_b = 0, mma_last_stage = -1;
+  if (warp == 0) {
+    // ------------------------------------------------------- producer ---
+    if (lane == 0) {
+      prefetch_tensor_map(&tmx);
+      prefetch_tensor_map(&tmw);
+    }
+    pdl_wait_primary();
+    const int total_q = my_tiles * nch;
+    bool ok = true;
+    // chunk qc (global over this CTA's tiles) -> tile and first group
+    auto issue_q = [&](int qc) -> bool {
+      const int slot = qc % kNQ;
+      const int t2 = cl + (qc / nch) * ncl;
+      const int g0 = (qc % nch) * kChunk;
+      const int nt = t2 / p.mt;
+      const int ncells = min(2, (p.N - nt * kTN) / 64);
+      int okw = 1;
+      if (lane == 0) {
+        if (qc >= kNQ) okw = wt_wait(&q_empty[slot], ((qc / kNQ) - 1) & 1, p.diag, abort_flag);
+        if (okw) {
+          uint8_t* dst = smem + C::kOffQ + slot * C::kQBytes;
+          mbar_arrive_expect_tx(&q_full[slot], ncells * C::kColBytes);
+          for (int ci = 0; ci < ncells; ++ci)
+            tma_load_2d(dst + ci * C::kColBytes, &tmw, 0,
+                        ((nt * 2 + ci) * p.G + g0) * C::kCellRows, &q_full[slot]);
+        }
+      }
+      okw = __shfl_sync(0xffffffffu, okw, 0);
+      if (!okw) return false;
+      // scales: kChunk groups x 128 columns, 16-byte pieces (8 columns)
+      const uint32_t sdst = smem_addr(smem + C::kOffQ + slot * C::kQBytes + C::kScaleOff);
+      for (int piece = lane; piece < kChunk * 16; piece += 32) {
+        const int gi = piece >> 4, col = (piece & 15) * 8;
+        const bool live = nt * kTN + col < p.N;
+        const uint16_t* src = live ? p.S + static_cast<size_t>(g0 + gi) * p.N + nt * kTN + col : p.S;
+        cp_async_16(sdst + (gi * kTN + col) * 2, src, live ? 16u : 0u);
+      }
+      cp_async_mbar_arrive_noinc(&q_full[slot]);
+      return true;
+    };
+    // X stages of chunk qc: 2 per group
+    auto issue_x = [&](int qc) -> bool {
+      const int t2 = cl + (qc / nch) * ncl;
+      const int g0 = (qc % nch) * kChunk;
+      const int m0 = (t2 % p.mt) * kTM;
+      for (int s = 0; s < 2 * kChunk; ++s) {
+        const int si = qc * 2 * kChunk + s;
+        const int slot = si % kNB;
+        int okx = 1;
+        if (lane == 0) {
+          if (si >= kNB) okx = wt_wait(&b_empty[slot], ((si / kNB) - 1) & 1, p.diag, abort_flag);
+          if (okx) {
+            mbar_arrive_expect_tx(&b_full[slot], kXStage);
+            tma_load_2d(smem + C::kOffX + slot * kXStage, &tmx, g0 * 128 + s * 64, m0,
+                        &b_full[slot]);
+          }
+        }
+        okx = __shfl_sync(0xffffffffu, okx, 0);
+        if (!okx) return false;
+        issued_b = si + 1;
+      }
+      return true;
+    };
+    for (int qc = 0; qc < min(kNQ, total_q) && ok; ++qc) {
+      ok = issue_q(qc);
+      if (ok) issued_q = qc + 1;
+    }
+    for (int qc = 0; qc < total_q && ok; ++qc) {
+      ok = issue_x(qc);
+      if (ok && qc + kNQ < total_q) {
+        ok = issue_q(qc + kNQ);
+        if (ok) issued_q = qc + kNQ + 1;
+      }
+    }
+    cp_async_wait_all();
+  } else if (warp == 1) {
+    // ---------------------------------------------------- MMA issuer ---
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kTN, kTM);
+      int u = 0;  // global group index of this CTA
+      bool ok = true;
+      for (int tl = 0; ok && tl < my_tiles; ++tl) {
+        const int buf = tl & 1;
+        if (tl >= 2 && !wt_wait(&d_empty[buf], ((tl >> 1) - 1) & 1, p.diag, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * kDCols;
+        for (int g = 0; g < p.G; ++g, ++u) {
+          const int as = u % kGA;
+          const bool hook = p.diag.force_timeout == 2 && tl == 0 && g == p.G / 2;
+          if (!wt_wait(hook ? never_bar : &a_full[as], hook ? 0u : (u / kGA) & 1, p.diag,
+                       abort_flag)) {
+            ok = false;
+            break;
+          }
+          for (int h = 0; h < 2; ++h) {
+            const int si = 2 * u + h;
+            const int bs = si % kNB;
+            if (!wt_wait(&b_full[bs], (si / kNB) & 1, p.diag, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t b_desc = smem_desc_sw128(smem_addr(smem + C::kOffX + bs * kXStage));
+            const uint32_t a_tmem = tmem_base + kACol + as * 64 + h * 32;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              umma_bf16_ts(d_tmem, a_tmem + 8 * j, b_desc + 2 * j, idesc, (g | h | j) != 0);
+            umma_commit(&b_empty[bs]);
+            mma_last_stage = si;
+          }
+          if (!ok) break;
+          umma_commit(&a_empty[as]);
+        }
+        if (ok) umma_commit(&d_full[buf]);
+      }
+      // every MMA has completed before shared and tensor memory are released
+      umma_commit(mma_done);
+      KernelDiag drain = p.diag;
+      if (drain.wait_limit_ns < 1000000000ull) drain.wait_limit_ns = 1000000000ull;
+      mbar_wait_bounded(mma_done, 0, drain);
+    }
+  } else if (warp < kFirstEpiWarp) {
+    // ------------------------------------------------- dequant warps ---
+    // Quadrant q = warp % 4 (the TMEM lanes this warp may write); warp r =
+    // (warp - 2) / 4 takes the groups whose A slot is r.
+    const int q = warp & 3, r = (warp - kFirstDequantWarp) >> 2;
+    const int n = 32 * q + lane;  // weight column within the tile = TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+    const int total_q = my_tiles * nch;
+    bool ok = true;
+    for (int qc = 0; qc < total_q && ok; ++qc) {
+      // groups u = qc * kChunk + pos, A slot u % kGA; this warp takes slot r
+      const int pos = r - (qc * kChunk) % kGA;
+      if (pos < 0 || pos >= kChunk) continue;  // not this warp's chunk
+      const int slot = qc % kNQ;
+      const int u = qc * kChunk + pos;
+      if (!wt_wait(&q_full[slot], (qc / kNQ) & 1, p.diag, abort_flag) ||
+          (u >= kGA && !wt_wait(&a_empty[r], ((u / kGA) - 1) & 1, p.diag, abort_flag))) {
+        ok = false;
+        break;
+      }
+      const uint32_t qbase = smem_addr(smem + C::kOffQ + slot * C::kQBytes);
+      const uint32_t s1 = ld_shared_u16(qbase + C::kScaleOff + (pos * kTN + n) * 2);
+      dequant_group_to_tmem<BITS>(qbase + (n >> 6) * C::kColBytes + pos * C::kCellBytes, n,
+                                  s1 | (s1 << 16), tmem_base + lane_addr + kACol + r * 64);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&a_full[r]);
+        mbar_arrive(&q_empty[slot]);
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue warps ---
+    pdl_wait_primary();  // these warps store Y
+    const int lane_base = 32 * (warp & 3);
+    for (int tl = 0; tl < my_tiles; ++tl) {
+      const int buf = tl & 1;
+      if (!wt_wait(&d_full[buf], (tl >> 1) & 1, p.diag, abort_flag, 20000)) break;
+      tc_fence_after();
+      const int t2 = cl + tl * ncl;
+      const int m0 = (t2 % p.mt) * kTM;
+      const int n = (t2 / p.mt) * kTN + lane_base + lane;
+#pragma unroll 1
+      for (int c = 0; c < kTM / 32; ++c) {
+        if (m0 + 32 * c >= p.M) break;
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(lane_base) << 16) + buf * kDCols + 32 * c, v);
+        tmem_ld_wait();
+        if (n < p.N) {
+          __nv_bfloat16* dst = p.Y + static_cast<size_t>(m0 + 32 * c) * p.N + n;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (m0 + 32 * c + i < p.M) dst[static_cast<size_t>(i) * p.N] = __float2bfloat16_rn(__uint_as_float(v[i]));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&d_empty[buf]);
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    // Let every issued copy land and every issued MMA finish (bounded, at
+    // least 1 s) before shared and tensor memory are released.
+    KernelDiag drain = p.diag;
+    if (drain.wait_limit_ns < 1000000000ull) drain.wait_limit_ns = 1000000000ull;
+    if (warp == 0 && lane == 0) {
+      for (int s = 0; s < kNQ && s < issued_q; ++s) {
+        const int last = s + ((issued_q - 1 - s) / kNQ) * kNQ;
+        mbar_wait_bounded(&q_full[s], (last / kNQ) & 1, drain);
+      }
+      for (int s = 0; s < kNB && s < issued_b; ++s) {
+        const int last = s + ((issued_b - 1 - s) / kNB) * kNB;
+        mbar_wait_bounded(&b_full[s], (last / kNB) & 1, drain);
+      }
+    }
+    (void)mma_last_stage;  // the MMA thread waited for mma_done
+    __syncthreads();
+  }
+  pdl_launch_dependents();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------ host side ---
+typedef CUresult (*WtEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                               const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                               const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                               CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+WtEncodeFn wt_encode_fn() {
+  static WtEncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<WtEncodeFn>(f);
+  });
+  return fn;
+}
+
+template <int BITS>
+struct WtInit {
+  std::atomic<uint64_t> done{0};
+  std::mutex mu;
+  cudaError_t ensure(int device) {
+    const uint64_t bit = 1ull << (device & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    std::lock_guard<std::mutex> lk(mu);
+    if (done.load() & bit) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(gemm_wt_kernel<BITS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         WtCfg<BITS>::kSmem);
+    if (e != cudaSuccess) return e;
+    done.fetch_or(bit, std::memory_order_release);
+    return cudaSuccess;
+  }
+};
+WtInit<4> g_wt4;
+WtInit<8> g_wt8;
+
+template <int BITS>
+cudaError_t launch_wt(const GemmArgs& a, cudaStream_t stream, WtEncodeFn enc) {
+  using C = WtCfg<BITS>;
+  cudaError_t e = BITS == 4 ? g_wt4.ensure(a.device) : g_wt8.ensure(a.device);
+  if (e != cudaSuccess) return e;
+
+  // X as a 2-D bf16 tensor [M rows, K cols]; box 64 x 128, 128-byte swizzle;
+  // rows past M read as zeros.
+  CUtensorMap tmx;
+  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(a.M)};
+  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(a.K) * 2};
+  const cuuint32_t box[2] = {64, kTM};
+  const cuuint32_t estride[2] = {1, 1};
+  CUresult r = enc(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.X), gdim,
+                   gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  // The packed weights as a 2-D u32 tensor of 128-byte rows; one box is the
+  // kChunk consecutive cells of one cell column.
+  CUtensorMap tmw;
+  const int64_t words = BITS == 4 ? a.K * a.N / 8 : a.K * a.N / 4;
+  const cuuint64_t wdim[2] = {32, static_cast<cuuint64_t>(words / 32)};
+  const cuuint64_t wstride[1] = {128};
+  const cuuint32_t wbox[2] = {32, static_cast<cuuint32_t>(C::kChunk * C::kCellRows)};
+  r = enc(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(a.Wp), wdim, wstride,
+          wbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+
+  WtParams p;
+  p.S = static_cast<const uint16_t*>(a.S);
+  p.Y = static_cast<__nv_bfloat16*>(a.Y);
+  p.M = static_cast<int>(a.M);
+  p.N = static_cast<int>(a.N);
+  p.K = static_cast<int>(a.K);
+  p.G = static_cast<int>(a.K / 128);
+  p.mt = static_cast<int>((a.M + kTM - 1) / kTM);
+  p.nt = static_cast<int>((a.N + kTN - 1) / kTN);
+  p.diag.err = a.diag.err;
+  p.diag.wait_limit_ns = a.diag.wait_limit_ns;
+  p.diag.force_timeout = a.diag.force_timeout;
+  const int64_t tiles = static_cast<int64_t>(p.mt) * p.nt;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles < a.num_sms ? tiles : a.num_sms));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = a.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemm_wt_kernel<BITS>, tmx, tmw, p);
+}
+
+}  // namespace
+
+bool gemm_wt_fits(int bits, int64_t M, int64_t K, int64_t N) {
+  const int64_t chunk = bits == 4 ? 4 : 2;
+  if ((K / 128) % chunk != 0) return false;
+  // tile counts and TMA row coordinates stay within 32-bit signed range
+  if ((M + kTM - 1) / kTM * ((N + kTN - 1) / kTN) > INT32_MAX) return false;
+  return (bits == 4 ? K * N / 256 : K * N / 128) <= INT32_MAX;
+}
+
+cudaError_t launch_gemm_wt(const GemmArgs& a, cudaStream_t stream) {
+  if (!gemm_wt_fits(a.bits, a.M, a.K, a.N)) return cudaErrorNotSupported;
+  WtEncodeFn enc = wt_encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  return a.bits == 4 ? launch_wt<4>(a, stream, enc) : launch_wt<8>(a, stream, enc);
+}
+
+}  // namespace wq

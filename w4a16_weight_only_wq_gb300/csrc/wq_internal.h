@@ -45,7 +45,13 @@ bool gemm_small_fits(int bits, int64_t K, int64_t N, int split_hint);
 // Tensor-memory GEMM for M <= 16 (wq_gemm_skinny.cu).
 cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t stream);
 
-// Tensor-core GEMM for large M (wq_gemm_tc.cu).
+// Tensor-core GEMM for large M, dequantised weights staged in shared
+// memory (wq_gemm_tc.cu).
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t stream);
+
+// Tensor-core GEMM for large M, dequantised weights in tensor memory
+// (wq_gemm_wt.cu).  Needs K / 128 to be a multiple of 4 (INT4) or 2 (INT8).
+cudaError_t launch_gemm_wt(const GemmArgs& a, cudaStream_t stream);
+bool gemm_wt_fits(int bits, int64_t M, int64_t K, int64_t N);
 
 }  // namespace wq
