@@ -167,7 +167,8 @@ WQ_API void wq_set_programmatic_launch(int on);
    tiled tensor-core kernel with dequantised weights in tensor memory, which
    needs K/128 to be a multiple of 4 (INT4) or 2 (INT8) and otherwise falls
    back to 1; any other value restores the automatic choice: M <= 32
-   kernel 0 in 16-row slices, 32 < M <= 384 kernel 3, larger M kernel 1). */
+   kernel 0 in 16-row slices, larger M kernel 3, or kernel 1 where kernel 3
+   does not apply). */
 WQ_API void wq_debug_force_regime(int regime);
 
 /* Which kernel family a GEMM of this shape runs (numbering as in

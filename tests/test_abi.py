@@ -79,7 +79,7 @@ def test_regime_selection_is_host_logic(wq):
         assert wq.wq_gemm_regime(bits, M, N, K) in (0, 1, 3)
     assert wq.wq_gemm_regime(4, 16, 9728, 2560) == 0
     assert wq.wq_gemm_regime(4, 128, 9728, 2560) == 3
-    assert wq.wq_gemm_regime(4, 8192, 9728, 2560) == 1
+    assert wq.wq_gemm_regime(4, 8192, 9728, 2560) == 3
     # K / 128 = 5 is not a multiple of the INT4 chunk: kernel 1 takes it
     assert wq.wq_gemm_regime(4, 128, 9728, 640) == 1
     assert wq.wq_gemm_regime(4, 16, 96, 128) == -1

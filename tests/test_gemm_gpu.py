@@ -68,7 +68,7 @@ def test_small_m_long_k_falls_back_to_tiled(wq, bits):
 
 
 def test_default_kernel_choice(wq):
-    for M, want in [(1, 0), (16, 0), (32, 0), (33, 3), (384, 3), (385, 1), (8192, 1)]:
+    for M, want in [(1, 0), (16, 0), (32, 0), (33, 3), (384, 3), (8192, 3)]:
         assert wq.wq_gemm_regime(4, M, 2560, 2560) == want
 
 
@@ -267,6 +267,34 @@ def test_wt_ragged_shapes(wq, wt_regime, bits, M, K, N):
     assert wq.wq_gemm_regime(bits, M, N, K) == 3
     X, q, s = synth.small_case(M, K, N, bits, seed=M + K + N + 3 * bits)
     _run_codes_case(wq, X, q, s, bits)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M,K,N", [(512, 512, 320), (700, 1024, 576), (640, 2560, 1024),
+                                   (513, 512, 64)])
+def test_wt_wide_tiles_ragged(wq, wt_regime, bits, M, K, N):
+    """M >= 512 takes tiles of 256 weight columns (two 128-lane halves
+    sharing each X stage); N = 320, 576 and 64 leave partial tiles."""
+    assert wq.wq_gemm_regime(bits, M, N, K) == 3
+    X, q, s = synth.small_case(M, K, N, bits, seed=M + 2 * K + N + bits)
+    _run_codes_case(wq, X, q, s, bits)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_wt_wide_integer_exact_bit_exact(wq, wt_regime, bits):
+    M, K, N = 600, 512, 768
+    rng = np.random.default_rng(43 + bits)
+    lo, hi = (-8, 7) if bits == 4 else (-128, 127)
+    q = rng.integers(lo, hi + 1, size=(K, N)).astype(np.int8)
+    s = oracle.f32_to_bf16_bits(
+        (2.0 ** rng.integers(-8, -2, size=(K // 128, N))).astype(np.float32))
+    X = oracle.f32_to_bf16_bits(rng.integers(-4, 5, size=(M, K)).astype(np.float32))
+    Wp = wq.pack_codes(i8_to_dev(q), bits)
+    Y = _gemm(wq, bits, bf16_to_dev(X), Wp, bf16_to_dev(s))
+    torch.cuda.synchronize()
+    Yref = oracle.gemm(X, oracle.pack(q, bits), s, K, N, bits)
+    want = oracle.f32_to_bf16_bits(Yref.astype(np.float32))
+    assert np.array_equal(bf16_to_host_bits(Y), want)
 
 
 @pytest.mark.parametrize("bits", [4, 8])

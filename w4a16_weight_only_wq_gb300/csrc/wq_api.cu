@@ -24,7 +24,6 @@ std::atomic<int> g_force_regime{-1};
 // Rows up to which the small-M kernel (16 rows per launch) is used; larger
 // M runs on the tensor-core kernel.
 constexpr int64_t kSmallMaxM = 32;
-constexpr int64_t kTmemMaxM = 384;
 
 // 0: warp-MMA small-M kernel (16 rows per launch), 1: tensor-core tiled
 // kernel with dequantised weights in shared memory, 2: tensor-memory
@@ -33,10 +32,9 @@ constexpr int64_t kTmemMaxM = 384;
 int pick_regime(int64_t M) {
   const int f = g_force_regime.load();
   if (f >= 0 && f <= 3) return f;
-  // measured crossovers (K = 2560, N = 9728): the tensor-memory kernel's
-  // 128-column tiles fill the GPU at small M; from M = 512 the 256-column
-  // tiles of kernel 1 (half the L2 traffic of X) are faster
-  return M <= kSmallMaxM ? 0 : M <= kTmemMaxM ? 3 : 1;
+  // measured at K = 2560, N = 9728: kernel 3 is faster than kernel 1 at
+  // every M from 64 to 8192; kernel 1 takes the shapes kernel 3 cannot
+  return M <= kSmallMaxM ? 0 : 3;
 }
 thread_local cudaError_t t_last_cuda = cudaSuccess;
 

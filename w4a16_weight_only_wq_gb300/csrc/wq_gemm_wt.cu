@@ -2,7 +2,8 @@
 // dequantised weights in tensor memory.
 //
 // Y[M,N] = X[M,K] . (s (.) q)[K,N] ("Quantize the Target, Quantize the
-// Drafter": the INT4 target's prefill of a long prompt), computed as
+// Drafter": the INT4 target's prefill of a long prompt and batched
+// verification of several draft blocks), computed as
 // Y^T = W^T . X^T so that the dequantised weights are the tcgen05.mma A
 // operand (M = 128 weight columns, one per TMEM lane) written straight
 // from registers into tensor memory, and X is the B operand (N = 128
@@ -11,9 +12,11 @@
 // weights there: only X tiles (TMA) and packed codes (TMA) are stored in
 // shared memory, and only the MMA and the dequant warps read it.
 //
-//  * Persistent: one CTA per SM walks tiles of 128 weight columns x 128
-//    tokens; the fp32 accumulator is double-buffered in tensor memory so the
-//    epilogue of a tile overlaps the next tile's MMAs.
+//  * Persistent: one CTA per SM walks tiles of 128 tokens x 128 weight
+//    columns (M < 512: double-buffered accumulator, so the epilogue of a
+//    tile overlaps the next tile's MMAs) or x 256 weight columns as two
+//    128-lane halves that share every X stage (M >= 512: half the L2
+//    traffic of X per FLOP, one accumulator of 2 x 128 columns).
 //  * Producer (warp 0): packed cells of four (INT4) or two (INT8) groups of
 //    both 64-column cell columns per TMA (the packed buffer seen as rows of
 //    128 bytes, 128-byte swizzle) plus their scales (cp.async), one chunk
@@ -24,7 +27,9 @@
 //    weight column of one group: LOP3 extraction of the codes, an exact
 //    bf16x2 subtraction of the offset and one bf16x2 multiply by the scale
 //    give bf16(s*q), stored with two tcgen05.st into its lane.
-//  * Epilogue (warps 18-21): tcgen05.ld of the accumulator, bf16 stores.
+//  * Epilogue (warps 18-21): tcgen05.ld of the accumulator; a thread holds
+//    one weight column of 32 tokens, so each warp transposes its 32 x 32
+//    block through shared memory and stores Y rows with 16-byte stores.
 //  Every wait is bounded; an abort drains copies and MMAs and frees TMEM.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -39,10 +44,8 @@
 namespace wq {
 namespace {
 
-constexpr int kTN = 128;          // weight columns per tile (MMA M, TMEM lanes)
 constexpr int kTM = 128;          // tokens per tile (MMA N)
 constexpr int kNB = 8;            // X stages (64 deep) in shared memory
-constexpr int kGA = 4;            // groups of A in tensor memory
 constexpr int kNQ = 2;            // packed chunks in flight
 constexpr int kDequantWarps = 16;
 constexpr int kFirstDequantWarp = 2;
@@ -50,24 +53,34 @@ constexpr int kFirstEpiWarp = kFirstDequantWarp + kDequantWarps;  // 18
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = (kFirstEpiWarp + kEpiWarps) * 32;        // 704
 constexpr uint32_t kTmemCols = 512;
-constexpr int kDCols = kTM;       // one accumulator: 128 fp32 columns
-constexpr int kACol = 2 * kDCols; // A slots start after the two accumulators
+constexpr int kACol = 256;        // A slots: TMEM columns 256..511
 constexpr int kXStage = kTM * 128;  // 16 KiB: 128 tokens x 64 bf16
 
-template <int BITS>
+// HALVES = 1: tiles of 128 weight columns, the accumulator (128 columns)
+// double-buffered, four groups of A in flight.  HALVES = 2: tiles of 256
+// weight columns as two 128-lane halves that share every X stage (half the
+// L2 traffic of X per FLOP), one accumulator of 2 x 128 columns, two groups
+// of A in flight; the epilogue of a tile briefly holds up the next one.
+template <int BITS, int HALVES>
 struct WtCfg {
-  static constexpr int kChunk = BITS == 4 ? 4 : 2;             // groups per packed chunk
+  static constexpr int kTN = 128 * HALVES;                     // weight columns per tile
+  static constexpr int kGA = HALVES == 1 ? 4 : 2;              // groups of A in TMEM
+  static constexpr int kAGroupCols = 64 * HALVES;              // TMEM columns per group of A
+  static constexpr int kDBufs = HALVES == 1 ? 2 : 1;           // accumulators
+  static constexpr int kChunk = (BITS == 4 ? 4 : 2) / HALVES;  // groups per packed chunk
+  static constexpr int kCellCols = 2 * HALVES;                 // 64-column cell columns per tile
   static constexpr int kCellBytes = BITS == 4 ? 4096 : 8192;   // 64 columns x 128 k
   static constexpr int kCellRows = kCellBytes / 128;
   static constexpr int kColBytes = kChunk * kCellBytes;        // one cell column of a chunk
-  static constexpr int kScaleOff = 2 * kColBytes;
+  static constexpr int kScaleOff = kCellCols * kColBytes;
   // + scales [group][128]; a multiple of 1024 so every slot's cells keep the
   // 1024-byte alignment the 128-byte swizzle pattern is anchored to
   static constexpr int kQBytes = (kScaleOff + kChunk * kTN * 2 + 1023) / 1024 * 1024;
   static constexpr int kOffX = 0;
   static constexpr int kOffQ = kOffX + kNB * kXStage;
-  static constexpr int kOffBar = kOffQ + kNQ * kQBytes;
-  static constexpr int kNumBars = 2 * kNB + 2 * kNQ + 2 * kGA + 4 + 2;
+  static constexpr int kOffT = kOffQ + kNQ * kQBytes;              // epilogue transposes
+  static constexpr int kOffBar = kOffT + kEpiWarps * 32 * 64;
+  static constexpr int kNumBars = 2 * kNB + 2 * kNQ + 2 * 4 + 4 + 2;
   static constexpr int kSmem = kOffBar + kNumBars * 8 + 32 + 1024;  // + alignment slack
 };
 
@@ -170,12 +183,14 @@ __device__ __forceinline__ bool wt_wait(uint64_t* bar, uint32_t parity, const Ke
   }
 }
 
-template <int BITS>
+template <int BITS, int HALVES>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                const WtParams p) {
-  using C = WtCfg<BITS>;
+  using C = WtCfg<BITS, HALVES>;
   constexpr int kChunk = C::kChunk;
+  constexpr int kGA = C::kGA;
+  constexpr int kTN = C::kTN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
 
@@ -185,8 +200,8 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
   uint64_t* q_full = b_empty + kNB;        // [kNQ] packed chunk + scales landed
   uint64_t* q_empty = q_full + kNQ;        // [kNQ] chunk dequantised
   uint64_t* a_full = q_empty + kNQ;        // [kGA] group of A written
-  uint64_t* a_empty = a_full + kGA;        // [kGA] MMAs done with it
-  uint64_t* d_full = a_empty + kGA;        // [2] accumulator finished
+  uint64_t* a_empty = a_full + 4;          // [kGA] MMAs done with it
+  uint64_t* d_full = a_empty + 4;          // [kDBufs] accumulator finished
   uint64_t* d_empty = d_full + 2;          // [2] accumulator read out
   uint64_t* mma_done = d_empty + 2;       // every MMA of this CTA has completed
   uint64_t* never_bar = mma_done + 1;      // test hook
@@ -210,10 +225,10 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
     mbar_init(mma_done, 1);
     for (int i = 0; i < kNQ; ++i) {
       mbar_init(&q_full[i], 1 + 32);       // TMA arrival + one per producer lane (cp.async)
-      mbar_init(&q_empty[i], 4 * kChunk);  // every dequant warp that reads the chunk
+      mbar_init(&q_empty[i], 4 * HALVES * kChunk);  // every dequant warp that reads the chunk
     }
     for (int i = 0; i < kGA; ++i) {
-      mbar_init(&a_full[i], 4);            // one warp per TMEM lane quadrant
+      mbar_init(&a_full[i], 4 * HALVES);   // one warp per TMEM lane quadrant and half
       mbar_init(&a_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -250,7 +265,7 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
       const int t2 = cl + (qc / nch) * ncl;
       const int g0 = (qc % nch) * kChunk;
       const int nt = t2 / p.mt;
-      const int ncells = min(2, (p.N - nt * kTN) / 64);
+      const int ncells = min(C::kCellCols, (p.N - nt * kTN) / 64);
       int okw = 1;
       if (lane == 0) {
         if (qc >= kNQ) okw = wt_wait(&q_empty[slot], ((qc / kNQ) - 1) & 1, p.diag, abort_flag);
@@ -259,15 +274,15 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
           mbar_arrive_expect_tx(&q_full[slot], ncells * C::kColBytes);
           for (int ci = 0; ci < ncells; ++ci)
             tma_load_2d(dst + ci * C::kColBytes, &tmw, 0,
-                        ((nt * 2 + ci) * p.G + g0) * C::kCellRows, &q_full[slot]);
+                        ((nt * C::kCellCols + ci) * p.G + g0) * C::kCellRows, &q_full[slot]);
         }
       }
       okw = __shfl_sync(0xffffffffu, okw, 0);
       if (!okw) return false;
-      // scales: kChunk groups x 128 columns, 16-byte pieces (8 columns)
+      // scales: kChunk groups x kTN columns, 16-byte pieces (8 columns)
       const uint32_t sdst = smem_addr(smem + C::kOffQ + slot * C::kQBytes + C::kScaleOff);
-      for (int piece = lane; piece < kChunk * 16; piece += 32) {
-        const int gi = piece >> 4, col = (piece & 15) * 8;
+      for (int piece = lane; piece < kChunk * (kTN / 8); piece += 32) {
+        const int gi = piece / (kTN / 8), col = (piece % (kTN / 8)) * 8;
         const bool live = nt * kTN + col < p.N;
         const uint16_t* src = live ? p.S + static_cast<size_t>(g0 + gi) * p.N + nt * kTN + col : p.S;
         cp_async_16(sdst + (gi * kTN + col) * 2, src, live ? 16u : 0u);
@@ -313,17 +328,16 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
   } else if (warp == 1) {
     // ---------------------------------------------------- MMA issuer ---
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kTN, kTM);
+      constexpr uint32_t idesc = idesc_bf16_f32(128, kTM);
       int u = 0;  // global group index of this CTA
       bool ok = true;
       for (int tl = 0; ok && tl < my_tiles; ++tl) {
-        const int buf = tl & 1;
-        if (tl >= 2 && !wt_wait(&d_empty[buf], ((tl >> 1) - 1) & 1, p.diag, abort_flag)) {
+        const int buf = tl % C::kDBufs, use = tl / C::kDBufs;
+        if (tl >= C::kDBufs && !wt_wait(&d_empty[buf], (use - 1) & 1, p.diag, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * kDCols;
         for (int g = 0; g < p.G; ++g, ++u) {
           const int as = u % kGA;
           const bool hook = p.diag.force_timeout == 2 && tl == 0 && g == p.G / 2;
@@ -341,10 +355,15 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
             }
             tc_fence_after();
             const uint64_t b_desc = smem_desc_sw128(smem_addr(smem + C::kOffX + bs * kXStage));
-            const uint32_t a_tmem = tmem_base + kACol + as * 64 + h * 32;
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              umma_bf16_ts(d_tmem, a_tmem + 8 * j, b_desc + 2 * j, idesc, (g | h | j) != 0);
+            for (int hf = 0; hf < HALVES; ++hf) {
+              // half hf of the weight columns: its own accumulator and A
+              const uint32_t d_tmem = tmem_base + (HALVES == 1 ? buf : hf) * 128;
+              const uint32_t a_tmem = tmem_base + kACol + as * C::kAGroupCols + hf * 64 + h * 32;
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                umma_bf16_ts(d_tmem, a_tmem + 8 * j, b_desc + 2 * j, idesc, (g | h | j) != 0);
+            }
             umma_commit(&b_empty[bs]);
             mma_last_stage = si;
           }
@@ -361,33 +380,37 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
     }
   } else if (warp < kFirstEpiWarp) {
     // ------------------------------------------------- dequant warps ---
-    // Quadrant q = warp % 4 (the TMEM lanes this warp may write); warp r =
-    // (warp - 2) / 4 takes the groups whose A slot is r.
+    // Quadrant q = warp % 4 (the TMEM lanes this warp may write); with
+    // r = (warp - 2) / 4, the warp takes half hf of the columns of the
+    // groups whose A slot is r (HALVES = 1) or r / 2 (HALVES = 2).
     const int q = warp & 3, r = (warp - kFirstDequantWarp) >> 2;
-    const int n = 32 * q + lane;  // weight column within the tile = TMEM lane
+    const int hf = HALVES == 1 ? 0 : (r & 1);
+    const int aslot = HALVES == 1 ? r : (r >> 1);
+    const int n = hf * 128 + 32 * q + lane;  // weight column within the tile
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
     const int total_q = my_tiles * nch;
     bool ok = true;
     for (int qc = 0; qc < total_q && ok; ++qc) {
-      // groups u = qc * kChunk + pos, A slot u % kGA; this warp takes slot r
-      const int pos = r - (qc * kChunk) % kGA;
+      // groups u = qc * kChunk + pos, A slot u % kGA; this warp takes aslot
+      const int pos = aslot - (qc * kChunk) % kGA;
       if (pos < 0 || pos >= kChunk) continue;  // not this warp's chunk
       const int slot = qc % kNQ;
       const int u = qc * kChunk + pos;
       if (!wt_wait(&q_full[slot], (qc / kNQ) & 1, p.diag, abort_flag) ||
-          (u >= kGA && !wt_wait(&a_empty[r], ((u / kGA) - 1) & 1, p.diag, abort_flag))) {
+          (u >= kGA && !wt_wait(&a_empty[aslot], ((u / kGA) - 1) & 1, p.diag, abort_flag))) {
         ok = false;
         break;
       }
       const uint32_t qbase = smem_addr(smem + C::kOffQ + slot * C::kQBytes);
       const uint32_t s1 = ld_shared_u16(qbase + C::kScaleOff + (pos * kTN + n) * 2);
       dequant_group_to_tmem<BITS>(qbase + (n >> 6) * C::kColBytes + pos * C::kCellBytes, n,
-                                  s1 | (s1 << 16), tmem_base + lane_addr + kACol + r * 64);
+                                  s1 | (s1 << 16),
+                                  tmem_base + lane_addr + kACol + aslot * C::kAGroupCols + hf * 64);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&a_full[r]);
+        mbar_arrive(&a_full[aslot]);
         mbar_arrive(&q_empty[slot]);
       }
     }
@@ -396,24 +419,38 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
     pdl_wait_primary();  // these warps store Y
     const int lane_base = 32 * (warp & 3);
     for (int tl = 0; tl < my_tiles; ++tl) {
-      const int buf = tl & 1;
-      if (!wt_wait(&d_full[buf], (tl >> 1) & 1, p.diag, abort_flag, 20000)) break;
+      const int buf = tl % C::kDBufs, use = tl / C::kDBufs;
+      if (!wt_wait(&d_full[buf], use & 1, p.diag, abort_flag, 20000)) break;
       tc_fence_after();
       const int t2 = cl + tl * ncl;
       const int m0 = (t2 % p.mt) * kTM;
-      const int n = (t2 / p.mt) * kTN + lane_base + lane;
 #pragma unroll 1
-      for (int c = 0; c < kTM / 32; ++c) {
-        if (m0 + 32 * c >= p.M) break;
+      for (int cc = 0; cc < HALVES * (kTM / 32); ++cc) {
+        const int hf = cc / (kTM / 32), c = cc % (kTM / 32);
+        if (m0 + 32 * c >= p.M) continue;
         uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(lane_base) << 16) + buf * kDCols + 32 * c, v);
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(lane_base) << 16) +
+                               (HALVES == 1 ? buf : hf) * 128 + 32 * c,
+                           v);
         tmem_ld_wait();
-        if (n < p.N) {
-          __nv_bfloat16* dst = p.Y + static_cast<size_t>(m0 + 32 * c) * p.N + n;
+        // transpose: T[token i][column lane] (bf16, rows of 64 bytes), then
+        // lane l stores 16 bytes (8 columns) of rows l/4 + 8k
+        const uint32_t tb = smem_addr(smem + C::kOffT + (warp - kFirstEpiWarp) * 32 * 64);
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (m0 + 32 * c + i < p.M) dst[static_cast<size_t>(i) * p.N] = __float2bfloat16_rn(__uint_as_float(v[i]));
+        for (int i = 0; i < 32; ++i)
+          st_shared_u16(tb + i * 64 + lane * 2,
+                        __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i]))));
+        __syncwarp();
+        const int ncol0 = (t2 / p.mt) * kTN + hf * 128 + lane_base;  // first column of the block
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int row = (lane >> 2) + 8 * k, seg = lane & 3;
+          const uint4 w = ld_shared_v4(tb + row * 64 + seg * 16);
+          const int m = m0 + 32 * c + row, nc = ncol0 + seg * 8;
+          if (m < p.M && nc < p.N)  // N is a multiple of 64: a segment is all in or all out
+            st_global_v4(p.Y + static_cast<size_t>(m) * p.N + nc, w.x, w.y, w.z, w.w);
         }
+        __syncwarp();  // the block is read before the next chunk overwrites it
       }
       tc_fence_before();
       __syncwarp();
@@ -468,7 +505,7 @@ WtEncodeFn wt_encode_fn() {
   return fn;
 }
 
-template <int BITS>
+template <int BITS, int HALVES>
 struct WtInit {
   std::atomic<uint64_t> done{0};
   std::mutex mu;
@@ -477,21 +514,25 @@ struct WtInit {
     if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
     std::lock_guard<std::mutex> lk(mu);
     if (done.load() & bit) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(gemm_wt_kernel<BITS>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_wt_kernel<BITS, HALVES>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         WtCfg<BITS>::kSmem);
+                                         WtCfg<BITS, HALVES>::kSmem);
     if (e != cudaSuccess) return e;
     done.fetch_or(bit, std::memory_order_release);
     return cudaSuccess;
   }
 };
-WtInit<4> g_wt4;
-WtInit<8> g_wt8;
+WtInit<4, 1> g_wt4;
+WtInit<8, 1> g_wt8;
+WtInit<4, 2> g_wt4w;
+WtInit<8, 2> g_wt8w;
 
-template <int BITS>
+template <int BITS, int HALVES>
 cudaError_t launch_wt(const GemmArgs& a, cudaStream_t stream, WtEncodeFn enc) {
-  using C = WtCfg<BITS>;
-  cudaError_t e = BITS == 4 ? g_wt4.ensure(a.device) : g_wt8.ensure(a.device);
+  using C = WtCfg<BITS, HALVES>;
+  constexpr int kTN = C::kTN;
+  cudaError_t e = BITS == 4 ? (HALVES == 2 ? g_wt4w.ensure(a.device) : g_wt4.ensure(a.device))
+                            : (HALVES == 2 ? g_wt8w.ensure(a.device) : g_wt8.ensure(a.device));
   if (e != cudaSuccess) return e;
 
   // X as a 2-D bf16 tensor [M rows, K cols]; box 64 x 128, 128-byte swizzle;
@@ -542,16 +583,20 @@ cudaError_t launch_wt(const GemmArgs& a, cudaStream_t stream, WtEncodeFn enc) {
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = a.pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gemm_wt_kernel<BITS>, tmx, tmw, p);
+  return cudaLaunchKernelEx(&cfg, gemm_wt_kernel<BITS, HALVES>, tmx, tmw, p);
 }
 
 }  // namespace
+
+// Tiles of 256 weight columns from this M on (measured at K = 2560,
+// N = 9728: below it the 128-column tiles fill the GPU better).
+constexpr int64_t kWideMinM = 512;
 
 bool gemm_wt_fits(int bits, int64_t M, int64_t K, int64_t N) {
   const int64_t chunk = bits == 4 ? 4 : 2;
   if ((K / 128) % chunk != 0) return false;
   // tile counts and TMA row coordinates stay within 32-bit signed range
-  if ((M + kTM - 1) / kTM * ((N + kTN - 1) / kTN) > INT32_MAX) return false;
+  if ((M + kTM - 1) / kTM * ((N + 127) / 128) > INT32_MAX) return false;
   return (bits == 4 ? K * N / 256 : K * N / 128) <= INT32_MAX;
 }
 
@@ -559,7 +604,9 @@ cudaError_t launch_gemm_wt(const GemmArgs& a, cudaStream_t stream) {
   if (!gemm_wt_fits(a.bits, a.M, a.K, a.N)) return cudaErrorNotSupported;
   WtEncodeFn enc = wt_encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
-  return a.bits == 4 ? launch_wt<4>(a, stream, enc) : launch_wt<8>(a, stream, enc);
+  const bool wide = a.M >= kWideMinM;
+  if (a.bits == 4) return wide ? launch_wt<4, 2>(a, stream, enc) : launch_wt<4, 1>(a, stream, enc);
+  return wide ? launch_wt<8, 2>(a, stream, enc) : launch_wt<8, 1>(a, stream, enc);
 }
 
 }  // namespace wq
