@@ -163,7 +163,8 @@ WQ_API void wq_set_programmatic_launch(int on);
 
 /* Test hook: run every GEMM on one kernel family regardless of M (0 the
    warp-MMA small-M kernel, 1 the tiled tensor-core kernel with dequantised
-   weights in shared memory, 2 the tensor-memory small-M kernel, 3 the
+   weights in shared memory, 2 the tensor-memory small-M kernel, which needs
+   K/128 to be even and otherwise falls back to 0, 3 the
    tiled tensor-core kernel with dequantised weights in tensor memory, which
    needs K/128 to be a multiple of 4 (INT4) or 2 (INT8) and otherwise falls
    back to 1; any other value restores the automatic choice: M <= 32

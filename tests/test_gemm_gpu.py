@@ -52,7 +52,9 @@ def small_kernel(wq, request):
 @pytest.mark.parametrize("M", [1, 5, 16, 17, 40])
 @pytest.mark.parametrize("K,N", [(128, 64), (640, 192), (1280, 576), (3840, 128)])
 def test_small_shapes(wq, small_kernel, bits, M, K, N):
-    assert wq.wq_gemm_regime(bits, M, N, K) == small_kernel
+    # the tensor-memory kernel takes whole two-group chunks only
+    want = small_kernel if small_kernel != 2 or (K // 128) % 2 == 0 else 0
+    assert wq.wq_gemm_regime(bits, M, N, K) == want
     X, q, s = synth.small_case(M, K, N, bits, seed=M * 7 + K + N + bits)
     _run_codes_case(wq, X, q, s, bits)
 
@@ -65,6 +67,37 @@ def test_small_m_long_k_falls_back_to_tiled(wq, bits):
     assert wq.wq_gemm_regime(bits, M, N, K) == 1
     X, q, s = synth.small_case(M, K, N, bits, seed=91 + bits)
     _run_codes_case(wq, X, q, s, bits)
+
+
+@pytest.fixture
+def skinny_regime(wq):
+    wq.wq_debug_force_regime(2)
+    yield
+    wq.wq_debug_force_regime(-1)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M", [1, 7, 16, 24])
+@pytest.mark.parametrize("K,N", [(256, 64), (512, 192), (1280, 576), (3840, 128),
+                                 (9728, 2560)])
+def test_tmem_small_m_shapes(wq, skinny_regime, bits, M, K, N):
+    """The tensor-memory small-M kernel on ragged tiles, every split the
+    occupancy rule picks, and M > 16 in 16-row slices."""
+    assert wq.wq_gemm_regime(bits, M, N, K) == 2
+    X, q, s = synth.small_case(M, K, N, bits, seed=M * 3 + K + N + bits)
+    _run_codes_case(wq, X, q, s, bits)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_tmem_small_m_every_split(wq, skinny_regime, bits):
+    M, K, N = 11, 2048, 320   # 8 chunks, 3 column tiles (the last one half)
+    X, q, s = synth.small_case(M, K, N, bits, seed=66)
+    try:
+        for cs in range(1, 9):
+            wq.wq_debug_set_split(cs)
+            _run_codes_case(wq, X, q, s, bits)
+    finally:
+        wq.wq_debug_set_split(0)
 
 
 def test_default_kernel_choice(wq):

@@ -278,7 +278,7 @@ void wq_debug_force_regime(int regime) {
 int wq_gemm_regime(int bits, int64_t M, int64_t N, int64_t K) {
   if ((bits != 4 && bits != 8) || M < 0 || check_kn(K, N) != WQ_OK) return -1;
   int r = pick_regime(M);
-  if (r == 2 && (bits == 4 ? K * N / 256 : K * N / 128) > INT32_MAX) r = 0;
+  if (r == 2 && !wq::gemm_skinny_fits(bits, K, N)) r = 0;
   // shapes whose X slice does not fit the small-M kernel run on the tiled one
   if (r == 0 && !wq::gemm_small_fits(bits, K, N, g_split_hint.load())) r = 1;
   if (r == 3 && !wq::gemm_wt_fits(bits, M, K, N)) r = 1;

@@ -177,6 +177,15 @@ __device__ __forceinline__ float dsmem_ld_f32(uint32_t cluster_addr) {
   return v;
 }
 
+// 16-byte store to shared memory of a CTA of the cluster (address 16-byte
+// aligned).
+__device__ __forceinline__ void dsmem_st_v4_f32(uint32_t cluster_addr, float a, float b, float c,
+                                                float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(a),
+               "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
 __device__ __forceinline__ void dsmem_st_f32(uint32_t cluster_addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
 }

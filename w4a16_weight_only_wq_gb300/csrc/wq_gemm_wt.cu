@@ -40,6 +40,7 @@
 #include "wq_device.cuh"
 #include "wq_internal.h"
 #include "wq_tcgen05.cuh"
+#include "wq_tmem_dequant.cuh"
 
 namespace wq {
 namespace {
@@ -91,97 +92,6 @@ struct WtParams {
   int mt, nt;  // tile counts along M and N
   KernelDiag diag;
 };
-
-// Byte offset, within one cell of a chunk, of the 16-byte packed lane
-// 4c + t4 of column n (INT8: of k half h) after the 128-byte swizzle: chunk
-// `ch` of 128-byte row `row` sits at chunk position ch ^ (row % 8).
-template <int BITS>
-__device__ __forceinline__ uint32_t wt_lane_offset(int n, int h, int t4) {
-  const int j8 = (n >> 3) & 7, c = n & 7;
-  const int row = BITS == 4 ? j8 * 4 + (c >> 1) : (j8 * 2 + h) * 4 + (c >> 1);
-  const int ch = (4 * (c & 1) + t4) ^ (row & 7);
-  return row * 128 + ch * 16;
-}
-
-// Dequantise one group (128 k) of this thread's column into bf16(s * q)
-// and store it into TMEM columns [taddr, taddr + 64) of its lane: column j
-// holds k = 2j, 2j + 1 (low half k = 2j).
-template <int BITS>
-__device__ __forceinline__ void dequant_group_to_tmem(uint32_t cell, int n, uint32_t s2,
-                                                      uint32_t taddr) {
-  constexpr uint32_t kMask = 0x000F000Fu;
-  constexpr uint32_t kLo = 0x43004300u;  // bf16 128
-  constexpr uint32_t kHi = 0x45004500u;  // bf16 2048
-  if constexpr (BITS == 4) {
-    constexpr uint32_t kB4 = 0x43084308u;  // 136
-    // lane 4c + t4 holds words kb = 0..3 of k = 32 kb + 8 t4 + 0..7
-    uint4 w[4];
-#pragma unroll
-    for (int t4 = 0; t4 < 4; ++t4) w[t4] = ld_shared_v4(cell + wt_lane_offset<4>(n, 0, t4));
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t r[32];
-#pragma unroll
-      for (int t4 = 0; t4 < 4; ++t4) {
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          const int kb = 2 * h + b;
-          const uint32_t word = kb == 0 ? w[t4].x : kb == 1 ? w[t4].y : kb == 2 ? w[t4].z : w[t4].w;
-          const int col = 4 * (4 * b + t4);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            r[col + j] = bf16x2_mul(bf16x2_sub(lop3_and_or(word >> (4 * j), kMask, kLo), kB4), s2);
-        }
-      }
-      tmem_st_32x32b_x32(taddr + 32 * h, r);
-    }
-  } else {
-    constexpr uint32_t kB8Lo = 0x43004300u;  // 128
-    constexpr uint32_t kB8Hi = 0x45084508u;  // 2176 = 2048 + 128
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      // half h: lane 4c + t4 holds words wi = 0..3,
-      // k = 32 (2h + wi/2) + 8 t4 + 4 (wi & 1) + 0..3
-      uint32_t r[32];
-#pragma unroll
-      for (int t4 = 0; t4 < 4; ++t4) {
-        const uint4 w = ld_shared_v4(cell + wt_lane_offset<8>(n, h, t4));
-#pragma unroll
-        for (int wi = 0; wi < 4; ++wi) {
-          const uint32_t word = wi == 0 ? w.x : wi == 1 ? w.y : wi == 2 ? w.z : w.w;
-          const int col = 4 * (4 * (wi >> 1) + t4) + 2 * (wi & 1);
-          const uint32_t lo01 = bf16x2_sub(lop3_and_or(word, kMask, kLo), kB8Lo);
-          const uint32_t hi01 = bf16x2_sub(lop3_and_or(word >> 4, kMask, kHi), kB8Hi);
-          const uint32_t lo23 = bf16x2_sub(lop3_and_or(word >> 8, kMask, kLo), kB8Lo);
-          const uint32_t hi23 = bf16x2_sub(lop3_and_or(word >> 12, kMask, kHi), kB8Hi);
-          r[col] = bf16x2_mul(bf16x2_add(hi01, lo01), s2);
-          r[col + 1] = bf16x2_mul(bf16x2_add(hi23, lo23), s2);
-        }
-      }
-      tmem_st_32x32b_x32(taddr + 32 * h, r);
-    }
-  }
-}
-
-// Bounded wait that also gives up as soon as another role has aborted.
-__device__ __forceinline__ bool wt_wait(uint64_t* bar, uint32_t parity, const KernelDiag& d,
-                                        volatile int* abort_flag, uint32_t hint_ns = 0) {
-  const uint32_t a = smem_addr(bar);
-  if (mbar_try_wait(a, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 16; ++i)
-      if (hint_ns ? mbar_try_wait_sleep(a, parity, hint_ns) : mbar_try_wait(a, parity))
-        return true;
-    if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > d.wait_limit_ns) {
-      atomicMax(d.err, kErrTimeout);
-      *abort_flag = 1;
-      return false;
-    }
-  }
-}
 
 template <int BITS, int HALVES>
 __global__ void __launch_bounds__(kThreads, 1)

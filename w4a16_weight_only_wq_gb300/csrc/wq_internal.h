@@ -42,8 +42,10 @@ struct GemmArgs {
 cudaError_t launch_gemm_small(const GemmArgs& a, cudaStream_t stream);
 bool gemm_small_fits(int bits, int64_t K, int64_t N, int split_hint);
 
-// Tensor-memory GEMM for M <= 16 (wq_gemm_skinny.cu).
+// Tensor-memory GEMM for M <= 16 (wq_gemm_skinny.cu).  Needs K / 128 to
+// be even.
 cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t stream);
+bool gemm_skinny_fits(int bits, int64_t K, int64_t N);
 
 // Tensor-core GEMM for large M, dequantised weights staged in shared
 // memory (wq_gemm_tc.cu).
