@@ -319,6 +319,9 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       }
     }
   }
+  // Roles that ran on one lane (MMA issue, copy issue) rejoin their warp
+  // before the block-wide barrier, which a diverged warp must not reach.
+  __syncwarp();
   __syncthreads();
   if (*abort_flag) {
     // Let every issued copy land and every issued MMA finish (bounded, at
@@ -336,6 +339,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       }
     }
     if (warp == 1 && lane == 0) mbar_wait_bounded(d_full, 0, drain);
+    __syncwarp();
     __syncthreads();
   }
   if (cs == 1) {

@@ -291,6 +291,9 @@ gemm_small_kernel(const SmallParams p) {
       }
     }
   }
+  // Roles that ran on one lane (MMA issue, copy issue) rejoin their warp
+  // before the block-wide barrier, which a diverged warp must not reach.
+  __syncwarp();
   __syncthreads();
   if (s_err) {
     // Some wait gave up: let every issued copy land (bounded, at least 1 s)
@@ -304,6 +307,7 @@ gemm_small_kernel(const SmallParams p) {
       }
       mbar_wait_bounded(xfull, 0, drain);
     }
+    __syncwarp();
     __syncthreads();
   }
 

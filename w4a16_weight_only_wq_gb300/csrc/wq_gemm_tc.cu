@@ -380,6 +380,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const TcParams p) {
     }
   }
 
+  // Roles that ran on one lane (MMA issue, copy issue) rejoin their warp
+  // before the block-wide barrier, which a diverged warp must not reach.
+  __syncwarp();
   __syncthreads();
   if (*abort_flag) {
     // Let every issued copy land and every issued MMA finish (bounded, at
@@ -401,6 +404,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const TcParams p) {
       const int last = mma_issued - 1;
       mbar_wait_bounded(&a_empty[last % kAStages], (last / kAStages) & 1, drain);
     }
+    __syncwarp();
     __syncthreads();
   }
   pdl_launch_dependents();

@@ -368,6 +368,9 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
     }
   }
 
+  // Roles that ran on one lane (MMA issue, copy issue) rejoin their warp
+  // before the block-wide barrier, which a diverged warp must not reach.
+  __syncwarp();
   __syncthreads();
   if (*abort_flag) {
     // Let every issued copy land and every issued MMA finish (bounded, at
@@ -385,6 +388,7 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
       }
     }
     (void)mma_last_stage;  // the MMA thread waited for mma_done
+    __syncwarp();
     __syncthreads();
   }
   pdl_launch_dependents();
