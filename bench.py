@@ -86,6 +86,23 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(ms, dev, pg):
+    """The slowest rank's time: every rank's timed region ends only when all
+    ranks have finished their share (replicas, weak scaling)."""
+    if pg is None:
+        return ms
+    import torch
+    t = torch.tensor([float(ms)], device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step, steps, world, ms):
+    """Whole-job throughput: the bytes every rank moved over the slowest
+    rank's time."""
+    return bytes_per_step * steps * world / (ms * 1e-3) / 1e9
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -349,13 +366,10 @@ def run_wq(args):
         soak.stop()
         csum = soak.summary()
         clock_note = "timed region too short; sampled during a 1 s soak of the same graph"
-    if pg is not None:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev, pg)
 
     ms_step = ms / args.steps
-    value = BYTES_STEP * args.steps * world / (ms * 1e-3) / 1e9
+    value = whole_job_gbs(BYTES_STEP, args.steps, world, ms)
 
     # Per-GEMM averages: separate graphs of one projection only.
     def time_single(which, n=400):
