@@ -106,6 +106,20 @@ WQ_API wq_status wq_pack_symmetric(const void* W, wq_dtype wdt, int64_t K, int64
 WQ_API wq_status wq_pack_codes(const int8_t* codes, int64_t K, int64_t N, int bits,
                         uint32_t* packed, cudaStream_t stream);
 
+/* The effective weight of a packed layer, W[k][n] = bf16(s[k/128][n] *
+   q[k][n]) as a row-major bf16 [K,N] matrix (s times q is exact in fp32 and
+   rounded once, ties to even).  This is what the fused-KV patch of the
+   "naveenrajk/Qwen3.5-4B-DFlash-W8A16" card ("Required vLLM patches",
+   item 2) recovers by running an identity matrix through the quantized
+   projection; this call returns it without a GEMM.  `packed` and `scales`
+   are as for the GEMMs (bits 4 or 8, group 128); `W` is caller-owned device
+   memory of K*N bf16.  Errors: WQ_ERR_NULL, WQ_ERR_UNSUPPORTED (bits),
+   WQ_ERR_SHAPE (group != 128, K % 128, N % 64), WQ_ERR_ALIGN (16 bytes),
+   WQ_ERR_CUDA.  Stream-ordered; allocates nothing. */
+WQ_API wq_status wq_dequantize(const uint32_t* packed, const uint16_t* scales, int bits,
+                               int64_t K, int64_t N, int group, uint16_t* W,
+                               cudaStream_t stream);
+
 /* Inverse of the interleave: int8 codes [K,N] from a packed weight. */
 WQ_API wq_status wq_unpack(const uint32_t* packed, int bits, int64_t K, int64_t N,
                     int8_t* codes, cudaStream_t stream);

@@ -114,3 +114,33 @@ def test_pack_drafter_int8_rtn_bit_exact(wq, n):
     assert np.array_equal(bf16_to_host_bits(s), s_ref)
     assert np.array_equal(words_to_host(packed), p_ref)
     assert q_ref.min() >= -127 and q_ref.max() <= 127
+
+
+# ------------------------------------------------------ effective weight ---
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("K,N", [(128, 64), (384, 192), (1280, 576)])
+def test_dequantize_bit_exact(wq, bits, K, N):
+    """bf16(s * q) for every weight, against the oracle's exact fp32 dequant
+    rounded once."""
+    _, q, s = synth.small_case(1, K, N, bits, seed=K + N + bits)
+    Wp = wq.pack_codes(i8_to_dev(q), bits)
+    W = wq.dequantize(Wp, bf16_to_dev(s), bits)
+    torch.cuda.synchronize()
+    want = oracle.f32_to_bf16_bits(oracle.dequant(q, s))
+    assert np.array_equal(bf16_to_host_bits(W), want)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_dequantize_equals_identity_probe(wq, bits):
+    """The effective weight equals what an identity matrix run through the
+    quantized GEMM returns (the W8A16 card's fused-KV extraction)."""
+    K, N = 256, 320
+    _, q, s = synth.small_case(1, K, N, bits, seed=40 + bits)
+    Wp = wq.pack_codes(i8_to_dev(q), bits)
+    st = bf16_to_dev(s)
+    W = wq.dequantize(Wp, st, bits)
+    eye = torch.eye(K, dtype=torch.bfloat16, device="cuda")
+    fn = wq.gemm_w4a16 if bits == 4 else wq.gemm_w8a16
+    Y = fn(eye, Wp, st)
+    torch.cuda.synchronize()
+    assert torch.equal(W, Y)

@@ -34,7 +34,7 @@ WQ_BF16 = 1
 GROUP = 128
 
 EXPORTED = (
-    "wq_packed_words", "wq_pack_symmetric", "wq_pack_codes", "wq_unpack",
+    "wq_packed_words", "wq_pack_symmetric", "wq_pack_codes", "wq_unpack", "wq_dequantize",
     "wq_gemm_w4a16", "wq_gemm_w8a16", "wq_last_device_error",
     "wq_clear_device_error", "wq_status_string", "wq_debug_set_wait_limit_ns",
     "wq_debug_force_timeout", "wq_gemm_regime", "wq_debug_set_split",
@@ -63,6 +63,7 @@ def _load() -> ctypes.CDLL:
         "wq_pack_symmetric": ([P, I, I64, I64, I, I, P, P, P, P], I),
         "wq_pack_codes": ([P, I64, I64, I, P, P], I),
         "wq_unpack": ([P, I, I64, I64, P, P], I),
+        "wq_dequantize": ([P, P, I, I64, I64, I, P, P], I),
         "wq_gemm_w4a16": ([P, P, P, P, I64, I64, I64, I, P], I),
         "wq_gemm_w8a16": ([P, P, P, P, I64, I64, I64, I, P], I),
         "wq_last_device_error": ([], I),
@@ -103,6 +104,10 @@ def wq_pack_codes(codes, K, N, bits, packed, stream) -> int:
 
 def wq_unpack(packed, bits, K, N, codes, stream) -> int:
     return _lib.wq_unpack(packed, bits, K, N, codes, stream)
+
+
+def wq_dequantize(packed, scales, bits, K, N, group, W, stream) -> int:
+    return _lib.wq_dequantize(packed, scales, bits, K, N, group, W, stream)
 
 
 def wq_gemm_w4a16(X, Wp, scales, Y, M, N, K, group, stream) -> int:
@@ -214,6 +219,18 @@ def unpack(packed: torch.Tensor, K: int, N: int, bits: int,
     _check(wq_unpack(_ptr(packed), bits, K, N, _ptr(codes), _stream(stream)),
            "wq_unpack")
     return codes
+
+
+def dequantize(packed: torch.Tensor, scales: torch.Tensor, bits: int,
+               stream=None) -> torch.Tensor:
+    """The effective bf16 weight [K, N] = bf16(s * q) of a packed layer."""
+    if scales.dtype != torch.bfloat16:
+        raise ValueError("scales must be bfloat16")
+    K, N = scales.shape[0] * GROUP, scales.shape[1]
+    W = torch.empty((K, N), dtype=torch.bfloat16, device=packed.device)
+    _check(wq_dequantize(_ptr(packed), _ptr(scales), bits, K, N, GROUP, _ptr(W),
+                         _stream(stream)), "wq_dequantize")
+    return W
 
 
 def _gemm(fn, name, X, Wp, scales, N, Y=None, stream=None):

@@ -203,6 +203,21 @@ wq_status wq_pack_codes(const int8_t* codes, int64_t K, int64_t N, int bits,
   return cuda_status(e);
 }
 
+wq_status wq_dequantize(const uint32_t* packed, const uint16_t* scales, int bits, int64_t K,
+                        int64_t N, int group, uint16_t* W, cudaStream_t stream) {
+  if (!packed || !scales || !W) return WQ_ERR_NULL;
+  if (bits != 4 && bits != 8) return WQ_ERR_UNSUPPORTED;
+  if (group != 128) return WQ_ERR_SHAPE;
+  wq_status st = check_kn(K, N);
+  if (st != WQ_OK) return st;
+  if (!aligned16(packed) || !aligned16(scales) || !aligned16(W)) return WQ_ERR_ALIGN;
+  int dev;
+  DeviceInfo d;
+  st = device_info(&dev, &d);
+  if (st != WQ_OK) return st;
+  return cuda_status(wq::launch_dequantize(packed, scales, bits, K, N, W, stream));
+}
+
 wq_status wq_unpack(const uint32_t* packed, int bits, int64_t K, int64_t N,
                     int8_t* codes, cudaStream_t stream) {
   if (!codes || !packed) return WQ_ERR_NULL;

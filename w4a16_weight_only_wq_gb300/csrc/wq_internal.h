@@ -23,6 +23,8 @@ cudaError_t launch_pack_codes(const int8_t* codes, int64_t K, int64_t N,
                               int bits, uint32_t* packed, cudaStream_t stream);
 cudaError_t launch_unpack(const uint32_t* packed, int bits, int64_t K,
                           int64_t N, int8_t* codes, cudaStream_t stream);
+cudaError_t launch_dequantize(const uint32_t* packed, const uint16_t* scales, int bits,
+                              int64_t K, int64_t N, uint16_t* W, cudaStream_t stream);
 
 // Small-M split-K GEMM (wq_gemm_small.cu).
 struct GemmArgs {

@@ -172,6 +172,42 @@ unpack_kernel(const uint32_t* __restrict__ packed, int64_t K, int64_t N,
   }
 }
 
+// Dequantise one packed cell: W[k][n] = bf16(fp32(s[k/128][n]) * q[k][n]),
+// the product exact in fp32 and rounded once (ties to even).  Codes are
+// scattered into a shared tile by the packed layout, then rows of 64
+// columns are written as bf16 pairs.
+template <int BITS>
+__global__ void __launch_bounds__(kPackThreads)
+dequantize_kernel(const uint32_t* __restrict__ packed, const uint16_t* __restrict__ scales,
+                  int64_t K, int64_t N, uint32_t* __restrict__ W) {
+  using F = Fmt<BITS>;
+  __shared__ int8_t tile[128][64 + 4];
+  __shared__ float s[64];
+  const int64_t nt = blockIdx.x, g = blockIdx.y;
+  const int tid = threadIdx.x;
+  constexpr uint32_t kMask = BITS == 4 ? 0xFu : 0xFFu;
+  const uint32_t* in = packed + (nt * (K / 128) + g) * F::kWords;
+  if (tid < 64) s[tid] = widen_bf16(scales[g * N + nt * 64 + tid]);
+  for (int i = tid; i < F::kWords; i += kPackThreads) {
+    const uint32_t word = in[i];
+#pragma unroll
+    for (int p = 0; p < F::kPerWord; ++p) {
+      int kl, nl, sh;
+      cell_slot<BITS>(i, p, kl, nl, sh);
+      tile[kl][nl] = static_cast<int8_t>(static_cast<int>((word >> sh) & kMask) - F::kOff);
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < 128 * 32; e += kPackThreads) {
+    const int r = e >> 5, c = (e & 31) * 2;
+    const float lo = s[c] * static_cast<float>(tile[r][c]);
+    const float hi = s[c + 1] * static_cast<float>(tile[r][c + 1]);
+    const uint32_t v = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+                       (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+    W[((g * 128 + r) * N + nt * 64 + c) / 2] = v;
+  }
+}
+
 dim3 cell_grid(int64_t K, int64_t N) {
   return dim3(static_cast<unsigned>(N / 64), static_cast<unsigned>(K / 128));
 }
@@ -205,6 +241,17 @@ cudaError_t launch_pack_codes(const int8_t* codes, int64_t K, int64_t N,
     pack_codes_kernel<4><<<grid, kPackThreads, 0, stream>>>(codes, K, N, packed);
   else
     pack_codes_kernel<8><<<grid, kPackThreads, 0, stream>>>(codes, K, N, packed);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize(const uint32_t* packed, const uint16_t* scales, int bits,
+                              int64_t K, int64_t N, uint16_t* W, cudaStream_t stream) {
+  const dim3 grid = cell_grid(K, N);
+  uint32_t* out = reinterpret_cast<uint32_t*>(W);
+  if (bits == 4)
+    dequantize_kernel<4><<<grid, kPackThreads, 0, stream>>>(packed, scales, K, N, out);
+  else
+    dequantize_kernel<8><<<grid, kPackThreads, 0, stream>>>(packed, scales, K, N, out);
   return cudaGetLastError();
 }
 
