@@ -106,6 +106,26 @@ WQ_API wq_status wq_pack_symmetric(const void* W, wq_dtype wdt, int64_t K, int64
 WQ_API wq_status wq_pack_codes(const int8_t* codes, int64_t K, int64_t N, int bits,
                         uint32_t* packed, cudaStream_t stream);
 
+/* Import a layer stored the way its serving checkpoint stores it: output-
+   channel-major, codes packed along the input dimension.  The target model
+   is served as a compressed-tensors checkpoint ("Quantize the Target,
+   Quantize the Drafter" project README, pipeline table: pack_ct.sh; the
+   GPTQ-W4A16 drafter card: --quantization compressed-tensors); the pages do
+   not print its layout, and this call reads the format's definition:
+     qweight    [N][K * bits / 32] uint32, row-major: word j of row n holds
+                the 32/bits consecutive codes k = (32/bits) j + p of column n
+                at bits [bits p, bits p + bits), offset-binary (q + 8 for
+                INT4, q + 128 for INT8);
+     scales_nk  [N][K / 128] bf16, row-major.
+   Writes this library's packed layout (`packed`, wq_packed_words(bits, K,
+   N) words) and the scales as [K/128, N] bf16 (`scales_out`), bit-exact.
+   Errors: WQ_ERR_NULL, WQ_ERR_UNSUPPORTED (bits), WQ_ERR_SHAPE (group !=
+   128, K % 128, N % 64), WQ_ERR_ALIGN (qweight, packed, scales_out 16 bytes;
+   scales_nk 2 bytes), WQ_ERR_CUDA.  Stream-ordered; allocates nothing. */
+WQ_API wq_status wq_import_packed_nk(const uint32_t* qweight, const uint16_t* scales_nk, int bits,
+                                     int64_t K, int64_t N, int group, uint32_t* packed,
+                                     uint16_t* scales_out, cudaStream_t stream);
+
 /* The effective weight of a packed layer, W[k][n] = bf16(s[k/128][n] *
    q[k][n]) as a row-major bf16 [K,N] matrix (s times q is exact in fp32 and
    rounded once, ties to even).  This is what the fused-KV patch of the

@@ -71,6 +71,7 @@ def _bind(lib):
     lib.wqo_pack.argtypes = [P, I64, I64, I, P]
     lib.wqo_unpack.argtypes = [P, I64, I64, I, P]
     lib.wqo_dequant.argtypes = [P, P, I64, I64, I, P]
+    lib.wqo_import_nk.argtypes = [P, P, I64, I64, I, I, P, P]
     lib.wqo_gemm_rows.argtypes = [P, P, P, P, I64, I64, I64, I, I, I, P]
     lib.wqo_gemm_rows.restype = I
     return lib
@@ -190,6 +191,21 @@ def pack_symmetric(W: np.ndarray, bits: int, scales_in: np.ndarray | None = None
         np.ascontiguousarray(scales_in, dtype=np.uint16)
     q = quantize(W, s, bits, group)
     return pack(q, bits), s, q
+
+
+def import_packed_nk(qweight: np.ndarray, s_nk: np.ndarray, K: int, N: int, bits: int,
+                     group: int = GROUP):
+    """Codes q [K, N] and scales s [K/group, N] of a layer stored output-
+    channel-major with codes packed along K (qweight uint32 [N, K*bits/32],
+    offset-binary, first code in the low bits; s_nk bf16 [N, K/group])."""
+    _check_shape(K, N, group)
+    qweight = np.ascontiguousarray(qweight, dtype=np.uint32)
+    s_nk = np.ascontiguousarray(s_nk, dtype=np.uint16)
+    assert qweight.size == N * K * bits // 32 and s_nk.size == N * (K // group)
+    q = np.empty((K, N), dtype=np.int8)
+    s = np.empty((K // group, N), dtype=np.uint16)
+    _load().wqo_import_nk(_ptr(qweight), _ptr(s_nk), K, N, group, bits, _ptr(q), _ptr(s))
+    return q, s
 
 
 def dequant(q: np.ndarray, s: np.ndarray, group: int = GROUP) -> np.ndarray:

@@ -188,6 +188,35 @@ void wqo_unpack(const uint32_t* packed, int64_t K, int64_t N, int bits,
   }
 }
 
+/* ------------------------------------------------- checkpoint import -- */
+
+/* Read a layer stored output-channel-major with its codes packed along the
+   input dimension (the serving checkpoint format of the pages' target, whose
+   layout the pages do not print; this is the format's definition): word j
+   of row n of `qweight` [N][K*bits/32] holds codes k = (32/bits)*j + p,
+   p = 0 .. 32/bits-1, at bits [bits*p, bits*p + bits), offset-binary;
+   `s_nk` is [N][K/group] bf16.  Writes canonical codes q [K,N] and scales
+   s [K/group, N]. */
+void wqo_import_nk(const uint32_t* qweight, const uint16_t* s_nk, int64_t K, int64_t N,
+                   int group, int bits, int8_t* q, uint16_t* s) {
+  int per = 32 / bits;
+  int64_t row_words = K / per;
+  uint32_t mask = bits == 4 ? 0xFu : 0xFFu;
+  int off = bits == 4 ? 8 : 128;
+  int64_t G = K / group;
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t j = 0; j < row_words; ++j) {
+      uint32_t word = qweight[n * row_words + j];
+      for (int p = 0; p < per; ++p) {
+        int64_t k = (int64_t)per * j + p;
+        int u = (int)((word >> (bits * p)) & mask);
+        q[k * N + n] = (int8_t)(u - off);
+      }
+    }
+    for (int64_t g = 0; g < G; ++g) s[g * N + n] = s_nk[n * G + g];
+  }
+}
+
 /* ------------------------------------------------------------ dequant -- */
 
 /* w^[k,n] = s[k/group, n] * q[k,n], exact in fp32. */

@@ -62,6 +62,10 @@ def test_argument_errors_without_gpu(wq):
         wq.WQ_ERR_NULL
     assert wq.wq_pack_codes(A, 128, 64, 4, A + 4, s) == wq.WQ_ERR_ALIGN
     assert wq.wq_unpack(A, 4, 128, 60, A, s) == wq.WQ_ERR_SHAPE
+    assert wq.wq_import_packed_nk(A, A, 4, 128, 64, 128, None, A, s) == wq.WQ_ERR_NULL
+    assert wq.wq_import_packed_nk(A, A, 6, 128, 64, 128, A, A, s) == wq.WQ_ERR_UNSUPPORTED
+    assert wq.wq_import_packed_nk(A, A, 4, 130, 64, 128, A, A, s) == wq.WQ_ERR_SHAPE
+    assert wq.wq_import_packed_nk(A, A + 1, 4, 128, 64, 128, A, A, s) == wq.WQ_ERR_ALIGN
     assert wq.wq_dequantize(None, A, 4, 128, 64, 128, A, s) == wq.WQ_ERR_NULL
     assert wq.wq_dequantize(A, A, 5, 128, 64, 128, A, s) == wq.WQ_ERR_UNSUPPORTED
     assert wq.wq_dequantize(A, A, 4, 128, 64, 64, A, s) == wq.WQ_ERR_SHAPE

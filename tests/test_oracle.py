@@ -292,3 +292,46 @@ def test_shape_checks():
         oracle.pack(np.zeros((128, 48), np.int8), 4)
     with pytest.raises(ValueError):
         oracle.rtn_scales(np.zeros((128, 64), np.float32), 4, group=64)
+
+
+# ----------------------------------------------------- checkpoint import ---
+def _encode_nk(q, bits):
+    """Test-side writer of the output-channel-major format: word j of row n
+    holds codes k = per*j .. per*j + per - 1, offset-binary, first in the
+    low bits."""
+    K, N = q.shape
+    per, off = 32 // bits, (8 if bits == 4 else 128)
+    u = (q.astype(np.int64) + off).T.reshape(N, K // per, per)
+    shifts = (bits * np.arange(per, dtype=np.int64))[None, None, :]
+    return np.ascontiguousarray((u << shifts).sum(axis=2).astype(np.uint32))
+
+
+def test_import_nk_reads_hand_made_words():
+    """Values fixed by the format definition: consecutive codes in rising
+    nibble (byte) positions, offset 8 (128)."""
+    qw = np.full((64, 16), 0x88888888, dtype=np.uint32)
+    qw[0, 0], qw[0, 1], qw[5, 15] = 0x76543210, 0xFEDCBA98, 0x0000000F
+    s_nk = np.arange(64, dtype=np.uint16).reshape(64, 1) + 0x3F00
+    q, s = oracle.import_packed_nk(qw, s_nk, 128, 64, 4)
+    assert q[:16, 0].tolist() == list(range(-8, 8))
+    assert q[120:128, 5].tolist() == [7] + [-8] * 7
+    assert np.all(q[:, 1:5] == 0) and np.all(q[16:, 0] == 0)
+    assert np.array_equal(s, s_nk.T)
+    qw8 = np.full((64, 32), 0x80808080, dtype=np.uint32)
+    qw8[3, 0], qw8[3, 31] = 0x83828180, 0x00FF7F01
+    q8, _ = oracle.import_packed_nk(qw8, s_nk, 128, 64, 8)
+    assert q8[0:4, 3].tolist() == [0, 1, 2, 3]
+    assert q8[124:128, 3].tolist() == [-127, -1, 127, -128]
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_import_nk_round_trip(bits):
+    rng = np.random.default_rng(51 + bits)
+    K, N = 384, 128
+    lo, hi = (-8, 7) if bits == 4 else (-128, 127)
+    q = rng.integers(lo, hi + 1, size=(K, N)).astype(np.int8)
+    s = rng.integers(0x3C00, 0x3F80, size=(K // 128, N)).astype(np.uint16)
+    got_q, got_s = oracle.import_packed_nk(_encode_nk(q, bits), np.ascontiguousarray(s.T), K, N,
+                                           bits)
+    assert np.array_equal(got_q, q)
+    assert np.array_equal(got_s, s)

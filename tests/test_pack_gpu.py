@@ -144,3 +144,21 @@ def test_dequantize_equals_identity_probe(wq, bits):
     Y = fn(eye, Wp, st)
     torch.cuda.synchronize()
     assert torch.equal(W, Y)
+
+
+# ------------------------------------------------------ checkpoint import ---
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("K,N", [(128, 64), (384, 192), (2560, 576)])
+def test_import_packed_nk_bit_exact(wq, bits, K, N):
+    """An output-channel-major checkpoint layer (codes packed along K) is
+    repacked into exactly the words the oracle packs from its codes."""
+    from tests.test_oracle import _encode_nk
+    _, q, s = synth.small_case(1, K, N, bits, seed=K + N + 7 * bits)
+    qw = torch.from_numpy(_encode_nk(q, bits).view(np.int32)).cuda()
+    s_nk = torch.from_numpy(np.ascontiguousarray(s.T).view(np.int16)).view(torch.bfloat16).cuda()
+    packed, scales = wq.import_packed_nk(qw, s_nk, bits)
+    torch.cuda.synchronize()
+    q_ref, s_ref = oracle.import_packed_nk(_encode_nk(q, bits), np.ascontiguousarray(s.T), K, N,
+                                           bits)
+    assert np.array_equal(words_to_host(packed), oracle.pack(q_ref, bits))
+    assert np.array_equal(bf16_to_host_bits(scales), s_ref)

@@ -35,6 +35,7 @@ GROUP = 128
 
 EXPORTED = (
     "wq_packed_words", "wq_pack_symmetric", "wq_pack_codes", "wq_unpack", "wq_dequantize",
+    "wq_import_packed_nk",
     "wq_gemm_w4a16", "wq_gemm_w8a16", "wq_last_device_error",
     "wq_clear_device_error", "wq_status_string", "wq_debug_set_wait_limit_ns",
     "wq_debug_force_timeout", "wq_gemm_regime", "wq_debug_set_split",
@@ -64,6 +65,7 @@ def _load() -> ctypes.CDLL:
         "wq_pack_codes": ([P, I64, I64, I, P, P], I),
         "wq_unpack": ([P, I, I64, I64, P, P], I),
         "wq_dequantize": ([P, P, I, I64, I64, I, P, P], I),
+        "wq_import_packed_nk": ([P, P, I, I64, I64, I, P, P, P], I),
         "wq_gemm_w4a16": ([P, P, P, P, I64, I64, I64, I, P], I),
         "wq_gemm_w8a16": ([P, P, P, P, I64, I64, I64, I, P], I),
         "wq_last_device_error": ([], I),
@@ -104,6 +106,12 @@ def wq_pack_codes(codes, K, N, bits, packed, stream) -> int:
 
 def wq_unpack(packed, bits, K, N, codes, stream) -> int:
     return _lib.wq_unpack(packed, bits, K, N, codes, stream)
+
+
+def wq_import_packed_nk(qweight, scales_nk, bits, K, N, group, packed, scales_out,
+                        stream) -> int:
+    return _lib.wq_import_packed_nk(qweight, scales_nk, bits, K, N, group, packed,
+                                    scales_out, stream)
 
 
 def wq_dequantize(packed, scales, bits, K, N, group, W, stream) -> int:
@@ -219,6 +227,24 @@ def unpack(packed: torch.Tensor, K: int, N: int, bits: int,
     _check(wq_unpack(_ptr(packed), bits, K, N, _ptr(codes), _stream(stream)),
            "wq_unpack")
     return codes
+
+
+def import_packed_nk(qweight: torch.Tensor, scales_nk: torch.Tensor, bits: int,
+                     stream=None):
+    """Repack an output-channel-major checkpoint layer (qweight int32
+    [N, K*bits/32], scales [N, K/128] bf16) into this library's layout:
+    returns (packed words, scales [K/128, N])."""
+    if scales_nk.dtype != torch.bfloat16:
+        raise ValueError("scales must be bfloat16")
+    N, G = scales_nk.shape
+    K = G * GROUP
+    packed = torch.empty((wq_packed_words(bits, K, N),), dtype=torch.int32,
+                         device=qweight.device)
+    scales = torch.empty((G, N), dtype=torch.bfloat16, device=qweight.device)
+    _check(wq_import_packed_nk(_ptr(qweight), _ptr(scales_nk), bits, K, N, GROUP,
+                               _ptr(packed), _ptr(scales), _stream(stream)),
+           "wq_import_packed_nk")
+    return packed, scales
 
 
 def dequantize(packed: torch.Tensor, scales: torch.Tensor, bits: int,

@@ -203,6 +203,25 @@ wq_status wq_pack_codes(const int8_t* codes, int64_t K, int64_t N, int bits,
   return cuda_status(e);
 }
 
+wq_status wq_import_packed_nk(const uint32_t* qweight, const uint16_t* scales_nk, int bits,
+                              int64_t K, int64_t N, int group, uint32_t* packed,
+                              uint16_t* scales_out, cudaStream_t stream) {
+  if (!qweight || !scales_nk || !packed || !scales_out) return WQ_ERR_NULL;
+  if (bits != 4 && bits != 8) return WQ_ERR_UNSUPPORTED;
+  if (group != 128) return WQ_ERR_SHAPE;
+  wq_status st = check_kn(K, N);
+  if (st != WQ_OK) return st;
+  if (!aligned16(qweight) || !aligned16(packed) || !aligned16(scales_out) ||
+      reinterpret_cast<uintptr_t>(scales_nk) % 2 != 0)
+    return WQ_ERR_ALIGN;
+  int dev;
+  DeviceInfo d;
+  st = device_info(&dev, &d);
+  if (st != WQ_OK) return st;
+  return cuda_status(
+      wq::launch_import_nk(qweight, scales_nk, bits, K, N, packed, scales_out, stream));
+}
+
 wq_status wq_dequantize(const uint32_t* packed, const uint16_t* scales, int bits, int64_t K,
                         int64_t N, int group, uint16_t* W, cudaStream_t stream) {
   if (!packed || !scales || !W) return WQ_ERR_NULL;

@@ -23,6 +23,9 @@ cudaError_t launch_pack_codes(const int8_t* codes, int64_t K, int64_t N,
                               int bits, uint32_t* packed, cudaStream_t stream);
 cudaError_t launch_unpack(const uint32_t* packed, int bits, int64_t K,
                           int64_t N, int8_t* codes, cudaStream_t stream);
+cudaError_t launch_import_nk(const uint32_t* qweight, const uint16_t* scales_nk, int bits,
+                             int64_t K, int64_t N, uint32_t* packed, uint16_t* scales_out,
+                             cudaStream_t stream);
 cudaError_t launch_dequantize(const uint32_t* packed, const uint16_t* scales, int bits,
                               int64_t K, int64_t N, uint16_t* W, cudaStream_t stream);
 

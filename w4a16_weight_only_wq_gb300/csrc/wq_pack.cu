@@ -146,6 +146,49 @@ pack_codes_kernel(const int8_t* __restrict__ codes, int64_t K, int64_t N,
   }
 }
 
+// Import of a layer stored output-channel-major with its codes packed along
+// the input dimension: qweight[n][j] holds the 32 / BITS consecutive codes
+// k = (32 / BITS) j + p at bits BITS p, offset-binary (q + 8 / q + 128);
+// scales_nk[n][g] is the bf16 scale of group g of column n.  One CTA per
+// (64-column tile, group) cell: decode the tile's 64 rows x 128 k into the
+// shared tile, pack it as pack_codes_kernel does, and write the tile's 64
+// scales of the group into the [K/128, N] scale matrix.
+template <int BITS>
+__global__ void __launch_bounds__(kPackThreads)
+import_nk_kernel(const uint32_t* __restrict__ qweight, const uint16_t* __restrict__ scales_nk,
+                 int64_t K, int64_t N, uint32_t* __restrict__ packed,
+                 uint16_t* __restrict__ scales_out) {
+  using F = Fmt<BITS>;
+  constexpr int kPer = 32 / BITS;            // codes per external word
+  constexpr int kRowWords = 128 / kPer;      // external words of one row per group
+  constexpr uint32_t kMask = BITS == 4 ? 0xFu : 0xFFu;
+  __shared__ int8_t tile[128][64 + 4];
+  const int64_t nt = blockIdx.x, g = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int64_t row_words = K / kPer;
+  for (int e = tid; e < 64 * kRowWords; e += kPackThreads) {
+    const int nl = e / kRowWords, w = e % kRowWords;
+    const uint32_t word = qweight[(nt * 64 + nl) * row_words + g * kRowWords + w];
+#pragma unroll
+    for (int p = 0; p < kPer; ++p)
+      tile[w * kPer + p][nl] =
+          static_cast<int8_t>(static_cast<int>((word >> (BITS * p)) & kMask) - F::kOff);
+  }
+  if (tid < 64) scales_out[g * N + nt * 64 + tid] = scales_nk[(nt * 64 + tid) * (K / 128) + g];
+  __syncthreads();
+  uint32_t* out = packed + (nt * (K / 128) + g) * F::kWords;
+  for (int i = tid; i < F::kWords; i += kPackThreads) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int p = 0; p < F::kPerWord; ++p) {
+      int kl, nl, sh;
+      cell_slot<BITS>(i, p, kl, nl, sh);
+      word |= (static_cast<uint32_t>(tile[kl][nl] + F::kOff) & kMask) << sh;
+    }
+    out[i] = word;
+  }
+}
+
 template <int BITS>
 __global__ void __launch_bounds__(kPackThreads)
 unpack_kernel(const uint32_t* __restrict__ packed, int64_t K, int64_t N,
@@ -241,6 +284,19 @@ cudaError_t launch_pack_codes(const int8_t* codes, int64_t K, int64_t N,
     pack_codes_kernel<4><<<grid, kPackThreads, 0, stream>>>(codes, K, N, packed);
   else
     pack_codes_kernel<8><<<grid, kPackThreads, 0, stream>>>(codes, K, N, packed);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_import_nk(const uint32_t* qweight, const uint16_t* scales_nk, int bits,
+                             int64_t K, int64_t N, uint32_t* packed, uint16_t* scales_out,
+                             cudaStream_t stream) {
+  const dim3 grid = cell_grid(K, N);
+  if (bits == 4)
+    import_nk_kernel<4><<<grid, kPackThreads, 0, stream>>>(qweight, scales_nk, K, N, packed,
+                                                           scales_out);
+  else
+    import_nk_kernel<8><<<grid, kPackThreads, 0, stream>>>(qweight, scales_nk, K, N, packed,
+                                                           scales_out);
   return cudaGetLastError();
 }
 
