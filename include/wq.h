@@ -185,9 +185,11 @@ WQ_API const char* wq_last_cuda_error(void);
 WQ_API void wq_debug_set_wait_limit_ns(uint64_t ns);
 WQ_API void wq_debug_force_timeout(int mode);
 
-/* Tuning and test hooks for the small-M kernel: force the number of CTAs
-   of a cluster that split one tile's K range (1..8; 0 restores the
-   automatic choice), and enable programmatic dependent launch, which lets a
+/* Tuning and test hooks: force the number of CTAs of a cluster that split
+   one tile's K range in the small-M kernels and in the tensor-memory kernel
+   at M < 512 (1..8, at most the tile's packed chunks; 0 restores the
+   automatic choice; a split the tensor-memory kernel cannot take makes the
+   call report WQ_ERR_UNSUPPORTED), and enable programmatic dependent launch, which lets a
    GEMM start streaming its weights while the preceding kernel on the stream
    finishes.  With it on, the weights and scales of a GEMM must not be
    written by the kernel immediately before it on the same stream (X and Y

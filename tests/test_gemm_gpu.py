@@ -384,6 +384,67 @@ def test_wt_deterministic_and_rows_beyond_m_untouched(wq, wt_regime):
     assert torch.equal(canary[:M], Y2)
 
 
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M,N", [(64, 640), (100, 320), (128, 128)])
+def test_wt_every_k_split(wq, wt_regime, bits, M, N):
+    """A cluster of 1..8 CTAs splits each tile's K range (K = 2560: 5 packed
+    chunks for INT4, 10 for INT8); the owners of each column add the fp32
+    partials.  N = 320 leaves a half tile whose upper columns are owned but
+    never stored."""
+    K = 2560
+    X, q, s = synth.small_case(M, K, N, bits, seed=M + N + bits)
+    nchunks = (K // 128) // (4 if bits == 4 else 2)
+    try:
+        for ks in range(1, min(8, nchunks) + 1):
+            wq.wq_debug_set_split(ks)
+            _run_codes_case(wq, X, q, s, bits)
+    finally:
+        wq.wq_debug_set_split(0)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_wt_k_split_integer_exact_and_deterministic(wq, wt_regime, bits):
+    """Partial sums that fp32 holds exactly: every split gives the same bits
+    as the oracle, and a repeated call the same bits again."""
+    M, K, N = 96, 2048, 256
+    rng = np.random.default_rng(53 + bits)
+    lo, hi = (-8, 7) if bits == 4 else (-128, 127)
+    q = rng.integers(lo, hi + 1, size=(K, N)).astype(np.int8)
+    s = oracle.f32_to_bf16_bits(
+        (2.0 ** rng.integers(-8, -2, size=(K // 128, N))).astype(np.float32))
+    X = oracle.f32_to_bf16_bits(rng.integers(-4, 5, size=(M, K)).astype(np.float32))
+    Wp = wq.pack_codes(i8_to_dev(q), bits)
+    Xt, st = bf16_to_dev(X), bf16_to_dev(s)
+    Yref = oracle.gemm(X, oracle.pack(q, bits), s, K, N, bits)
+    want = oracle.f32_to_bf16_bits(Yref.astype(np.float32))
+    nchunks = (K // 128) // (4 if bits == 4 else 2)
+    try:
+        for ks in range(1, min(8, nchunks) + 1):
+            wq.wq_debug_set_split(ks)
+            Y1 = _gemm(wq, bits, Xt, Wp, st)
+            Y2 = _gemm(wq, bits, Xt, Wp, st)
+            torch.cuda.synchronize()
+            assert np.array_equal(bf16_to_host_bits(Y1), want), f"split {ks}"
+            assert torch.equal(Y1, Y2), f"split {ks}"
+    finally:
+        wq.wq_debug_set_split(0)
+
+
+def test_wt_k_split_beyond_chunks_is_refused(wq, wt_regime):
+    """A forced split above the tile's chunk count is reported, not run."""
+    M, K, N = 64, 512, 128  # one INT4 chunk
+    X, q, s = synth.small_case(M, K, N, 4, seed=3)
+    Wp = wq.pack_codes(i8_to_dev(q), 4)
+    try:
+        wq.wq_debug_set_split(2)
+        with pytest.raises(wq.WQError) as ei:
+            wq.gemm_w4a16(bf16_to_dev(X), Wp, bf16_to_dev(s))
+        assert ei.value.status == wq.WQ_ERR_UNSUPPORTED
+    finally:
+        wq.wq_debug_set_split(0)
+    torch.cuda.synchronize()
+
+
 @pytest.mark.parametrize("case", synth.C5, ids=_case_ids(synth.C5))
 def test_wt_workload_prefill_sampled_rows(wq, wt_regime, case):
     d = case.draw()

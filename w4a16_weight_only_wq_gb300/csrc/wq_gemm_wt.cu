@@ -47,6 +47,7 @@ namespace {
 
 constexpr int kTM = 128;          // tokens per tile (MMA N)
 constexpr int kNB = 8;            // X stages (64 deep) in shared memory
+constexpr int kXG = kNB / 2;      // ... filled a group (two stages) per copy
 constexpr int kNQ = 2;            // packed chunks in flight
 constexpr int kDequantWarps = 16;
 constexpr int kFirstDequantWarp = 2;
@@ -90,6 +91,7 @@ struct WtParams {
   __nv_bfloat16* Y;
   int M, N, K, G;
   int mt, nt;  // tile counts along M and N
+  int ks;      // CTAs of a cluster that split one tile's K range (1: none)
   KernelDiag diag;
 };
 
@@ -105,8 +107,8 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* b_full = bars;                 // [kNB] X stage landed
-  uint64_t* b_empty = b_full + kNB;        // [kNB] MMAs done with it
+  uint64_t* b_full = bars;                 // [kXG] X stages of a group landed
+  uint64_t* b_empty = b_full + kNB;        // [kXG] MMAs done with them
   uint64_t* q_full = b_empty + kNB;        // [kNQ] packed chunk + scales landed
   uint64_t* q_empty = q_full + kNQ;        // [kNQ] chunk dequantised
   uint64_t* a_full = q_empty + kNQ;        // [kGA] group of A written
@@ -121,14 +123,19 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nch = p.G / kChunk;            // chunks per tile
-  // Tiles: this CTA takes tiles t = blockIdx.x + k gridDim.x: token tile
-  // t % mt, column tile t / mt.
-  const int cl = blockIdx.x, ncl = gridDim.x;
+  // Tiles: cluster cl (of ncl; one CTA unless the K range is split) takes
+  // tiles t = cl + k ncl: token tile t % mt, column tile t / mt.  With a
+  // split, CTA `rank` of the cluster takes chunks [kc0, kc0 + kch) of each
+  // of its tiles' K range.
+  const int ks = HALVES == 1 ? p.ks : 1;
+  const int rank = ks > 1 ? static_cast<int>(blockIdx.x) % ks : 0;
+  const int cl = blockIdx.x / ks, ncl = gridDim.x / ks;
+  const int kc0 = (nch * rank) / ks, kch = (nch * (rank + 1)) / ks - kc0;
   const int ptiles = p.mt * p.nt;
   const int my_tiles = ptiles > cl ? (ptiles - 1 - cl) / ncl + 1 : 0;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNB; ++i) {
+    for (int i = 0; i < kXG; ++i) {
       mbar_init(&b_full[i], 1);
       mbar_init(&b_empty[i], 1);
     }
@@ -159,7 +166,7 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
   const uint32_t tmem_base = *tmem_slot;
   if (p.diag.force_timeout == 1) mbar_wait_bounded(never_bar, 0, p.diag);
 
-  int issued_q = 0, issued_b = 0, mma_last_stage = -1;
+  int issued_q = 0, issued_b = 0;
   if (warp == 0) {
     // ------------------------------------------------------- producer ---
     if (lane == 0) {
@@ -167,24 +174,23 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
       prefetch_tensor_map(&tmw);
     }
     pdl_wait_primary();
-    const int total_q = my_tiles * nch;
+    const int total_q = my_tiles * kch;
     bool ok = true;
     // chunk qc (global over this CTA's tiles) -> tile and first group
     auto issue_q = [&](int qc) -> bool {
       const int slot = qc % kNQ;
-      const int t2 = cl + (qc / nch) * ncl;
-      const int g0 = (qc % nch) * kChunk;
+      const int t2 = cl + (qc / kch) * ncl;
+      const int g0 = (kc0 + qc % kch) * kChunk;
       const int nt = t2 / p.mt;
-      const int ncells = min(C::kCellCols, (p.N - nt * kTN) / 64);
       int okw = 1;
       if (lane == 0) {
         if (qc >= kNQ) okw = wt_wait(&q_empty[slot], ((qc / kNQ) - 1) & 1, p.diag, abort_flag);
         if (okw) {
-          uint8_t* dst = smem + C::kOffQ + slot * C::kQBytes;
-          mbar_arrive_expect_tx(&q_full[slot], ncells * C::kColBytes);
-          for (int ci = 0; ci < ncells; ++ci)
-            tma_load_2d(dst + ci * C::kColBytes, &tmw, 0,
-                        ((nt * C::kCellCols + ci) * p.G + g0) * C::kCellRows, &q_full[slot]);
+          // every cell column of the tile in one copy; a column past N reads
+          // as zeros and still counts in the transaction
+          mbar_arrive_expect_tx(&q_full[slot], C::kCellCols * C::kColBytes);
+          tma_load_3d(smem + C::kOffQ + slot * C::kQBytes, &tmw, 0, g0 * C::kCellRows,
+                      nt * C::kCellCols, &q_full[slot]);
         }
       }
       okw = __shfl_sync(0xffffffffu, okw, 0);
@@ -200,26 +206,26 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
       cp_async_mbar_arrive_noinc(&q_full[slot]);
       return true;
     };
-    // X stages of chunk qc: 2 per group
+    // X of chunk qc: one copy per group (two 64-deep stages)
     auto issue_x = [&](int qc) -> bool {
-      const int t2 = cl + (qc / nch) * ncl;
-      const int g0 = (qc % nch) * kChunk;
+      const int t2 = cl + (qc / kch) * ncl;
+      const int g0 = (kc0 + qc % kch) * kChunk;
       const int m0 = (t2 % p.mt) * kTM;
-      for (int s = 0; s < 2 * kChunk; ++s) {
-        const int si = qc * 2 * kChunk + s;
-        const int slot = si % kNB;
+      for (int s = 0; s < kChunk; ++s) {
+        const int gi = qc * kChunk + s;
+        const int slot = gi % kXG;
         int okx = 1;
         if (lane == 0) {
-          if (si >= kNB) okx = wt_wait(&b_empty[slot], ((si / kNB) - 1) & 1, p.diag, abort_flag);
+          if (gi >= kXG) okx = wt_wait(&b_empty[slot], ((gi / kXG) - 1) & 1, p.diag, abort_flag);
           if (okx) {
-            mbar_arrive_expect_tx(&b_full[slot], kXStage);
-            tma_load_2d(smem + C::kOffX + slot * kXStage, &tmx, g0 * 128 + s * 64, m0,
+            mbar_arrive_expect_tx(&b_full[slot], 2 * kXStage);
+            tma_load_3d(smem + C::kOffX + slot * 2 * kXStage, &tmx, 0, m0, (g0 + s) * 2,
                         &b_full[slot]);
           }
         }
         okx = __shfl_sync(0xffffffffu, okx, 0);
         if (!okx) return false;
-        issued_b = si + 1;
+        issued_b = gi + 1;
       }
       return true;
     };
@@ -248,23 +254,24 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
           break;
         }
         tc_fence_after();
-        for (int g = 0; g < p.G; ++g, ++u) {
+        for (int g = 0; g < kch * kChunk; ++g, ++u) {
           const int as = u % kGA;
-          const bool hook = p.diag.force_timeout == 2 && tl == 0 && g == p.G / 2;
+          const bool hook = p.diag.force_timeout == 2 && tl == 0 && g == kch * kChunk / 2;
           if (!wt_wait(hook ? never_bar : &a_full[as], hook ? 0u : (u / kGA) & 1, p.diag,
                        abort_flag)) {
             ok = false;
             break;
           }
+          const int xs = u % kXG;
+          if (!wt_wait(&b_full[xs], (u / kXG) & 1, p.diag, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int si = 2 * u + h;
-            const int bs = si % kNB;
-            if (!wt_wait(&b_full[bs], (si / kNB) & 1, p.diag, abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint64_t b_desc = smem_desc_sw128(smem_addr(smem + C::kOffX + bs * kXStage));
+            const uint64_t b_desc =
+                smem_desc_sw128(smem_addr(smem + C::kOffX + (2 * xs + h) * kXStage));
 #pragma unroll
             for (int hf = 0; hf < HALVES; ++hf) {
               // half hf of the weight columns: its own accumulator and A
@@ -274,10 +281,8 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
               for (int j = 0; j < 4; ++j)
                 umma_bf16_ts(d_tmem, a_tmem + 8 * j, b_desc + 2 * j, idesc, (g | h | j) != 0);
             }
-            umma_commit(&b_empty[bs]);
-            mma_last_stage = si;
           }
-          if (!ok) break;
+          umma_commit(&b_empty[xs]);
           umma_commit(&a_empty[as]);
         }
         if (ok) umma_commit(&d_full[buf]);
@@ -298,7 +303,7 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
     const int aslot = HALVES == 1 ? r : (r >> 1);
     const int n = hf * 128 + 32 * q + lane;  // weight column within the tile
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
-    const int total_q = my_tiles * nch;
+    const int total_q = my_tiles * kch;
     bool ok = true;
     for (int qc = 0; qc < total_q && ok; ++qc) {
       // groups u = qc * kChunk + pos, A slot u % kGA; this warp takes aslot
@@ -332,6 +337,7 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
       const int buf = tl % C::kDBufs, use = tl / C::kDBufs;
       if (!wt_wait(&d_full[buf], use & 1, p.diag, abort_flag, 20000)) break;
       tc_fence_after();
+      if (ks > 1) break;  // one tile per CTA: partials are reduced after the roles
       const int t2 = cl + tl * ncl;
       const int m0 = (t2 % p.mt) * kTM;
 #pragma unroll 1
@@ -382,14 +388,74 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
         const int last = s + ((issued_q - 1 - s) / kNQ) * kNQ;
         mbar_wait_bounded(&q_full[s], (last / kNQ) & 1, drain);
       }
-      for (int s = 0; s < kNB && s < issued_b; ++s) {
-        const int last = s + ((issued_b - 1 - s) / kNB) * kNB;
-        mbar_wait_bounded(&b_full[s], (last / kNB) & 1, drain);
+      for (int s = 0; s < kXG && s < issued_b; ++s) {
+        const int last = s + ((issued_b - 1 - s) / kXG) * kXG;
+        mbar_wait_bounded(&b_full[s], (last / kXG) & 1, drain);
       }
     }
-    (void)mma_last_stage;  // the MMA thread waited for mma_done
+    // the MMA thread waited for mma_done
     __syncwarp();
     __syncthreads();
+  }
+  if (HALVES == 1 && ks > 1) {
+    // ------------------------------------------- K-split reduction ---
+    // The tile's 128 weight columns are dealt to the cluster's CTAs in
+    // groups of 8: rank r owns groups [16 r / ks, 16 (r + 1) / ks).  Every
+    // CTA pushes its fp32 partial of each column to the column's owner, into
+    // the owner's X stages (idle once every CTA of the cluster has passed its
+    // roles), as part[source rank][owned column][token], the 16-byte token
+    // quads of a column rotated by the column's low three bits so that a
+    // warp's stores (32 columns) spread over the banks.  The owner adds the
+    // partials in rank order and writes Y.
+    const int slice = 8 * ((16 + ks - 1) / ks);  // columns of the widest share
+    auto part_off = [&](int src, int local, int tok) -> uint32_t {
+      return static_cast<uint32_t>((((src * slice + local) * 32 + ((tok >> 2) ^ (local & 7))) << 4) +
+                                   ((tok & 3) << 2));
+    };
+    const int m0 = (cl % p.mt) * kTM;
+    cluster_sync();  // every owner's X stages are free
+    if (warp >= kFirstEpiWarp) {
+      tc_fence_after();
+      const int lane_base = 32 * (warp & 3);
+      const int col = lane_base + lane, owner = (((col >> 3) + 1) * ks - 1) / 16;
+      const int local = col - 8 * ((16 * owner) / ks);
+      const uint32_t dst = dsmem_map(smem + C::kOffX, static_cast<uint32_t>(owner));
+#pragma unroll 1
+      for (int c = 0; c < kTM / 32 && m0 + 32 * c < p.M; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(lane_base) << 16) + 32 * c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          dsmem_st_v4_f32(dst + part_off(rank, local, 32 * c + 4 * k), __uint_as_float(v[4 * k]),
+                          __uint_as_float(v[4 * k + 1]), __uint_as_float(v[4 * k + 2]),
+                          __uint_as_float(v[4 * k + 3]));
+      }
+    }
+    cluster_sync();  // every partial has arrived at its owner
+    pdl_wait_primary();  // every thread below may store Y
+    const int gs = (16 * rank) / ks, ng = (16 * (rank + 1)) / ks - gs;
+    const int rows = min(kTM, p.M - m0);
+    const int ncol0 = (cl / p.mt) * kTN + 8 * gs;
+    const uint32_t base = smem_addr(smem + C::kOffX);
+    // consecutive threads take consecutive tokens of one 8-column group: a
+    // warp's loads of one column are 32 consecutive words
+    for (int it = threadIdx.x; it < rows * ng; it += kThreads) {
+      const int tok = it % rows, cg = it / rows;
+      const int nc = ncol0 + 8 * cg;
+      if (nc >= p.N) continue;  // N is a multiple of 64: a group is all in or all out
+      float acc[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+      for (int src = 0; src < ks; ++src) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          acc[j] += __uint_as_float(ld_shared_u32(base + part_off(src, 8 * cg + j, tok)));
+      }
+      st_global_v4(p.Y + static_cast<size_t>(m0 + tok) * p.N + nc, pack_bf16x2(acc[0], acc[1]),
+                   pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                   pack_bf16x2(acc[6], acc[7]));
+    }
   }
   pdl_launch_dependents();
   __syncthreads();
@@ -419,20 +485,45 @@ WtEncodeFn wt_encode_fn() {
   return fn;
 }
 
+// Per device: the kernel's shared-memory attribute and, for every cluster
+// size 1..8, how many clusters can be resident at once (tiles of 128 columns
+// only: the K split is used there alone).
 template <int BITS, int HALVES>
 struct WtInit {
   std::atomic<uint64_t> done{0};
   std::mutex mu;
-  cudaError_t ensure(int device) {
+  int max_clusters[64][9] = {};
+  cudaError_t ensure(int device, int (&out)[9]) {
     const uint64_t bit = 1ull << (device & 63);
-    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
-    std::lock_guard<std::mutex> lk(mu);
-    if (done.load() & bit) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(gemm_wt_kernel<BITS, HALVES>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         WtCfg<BITS, HALVES>::kSmem);
-    if (e != cudaSuccess) return e;
-    done.fetch_or(bit, std::memory_order_release);
+    if (!(done.load(std::memory_order_acquire) & bit)) {
+      std::lock_guard<std::mutex> lk(mu);
+      if (!(done.load() & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_wt_kernel<BITS, HALVES>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             WtCfg<BITS, HALVES>::kSmem);
+        if (e != cudaSuccess) return e;
+        for (int c = 1; HALVES == 1 && c <= 8; ++c) {
+          cudaLaunchConfig_t cfg = {};
+          cfg.gridDim = dim3(c);
+          cfg.blockDim = dim3(kThreads);
+          cfg.dynamicSmemBytes = WtCfg<BITS, HALVES>::kSmem;
+          cudaLaunchAttribute at;
+          at.id = cudaLaunchAttributeClusterDimension;
+          at.val.clusterDim.x = c;
+          at.val.clusterDim.y = 1;
+          at.val.clusterDim.z = 1;
+          cfg.attrs = &at;
+          cfg.numAttrs = 1;
+          int n = 0;
+          if (cudaOccupancyMaxActiveClusters(&n, gemm_wt_kernel<BITS, HALVES>, &cfg) != cudaSuccess)
+            n = 0;
+          max_clusters[device & 63][c] = n;
+        }
+        cudaGetLastError();  // a refused size above is not an error of this call
+        done.fetch_or(bit, std::memory_order_release);
+      }
+    }
+    for (int c = 0; c <= 8; ++c) out[c] = max_clusters[device & 63][c];
     return cudaSuccess;
   }
 };
@@ -441,34 +532,55 @@ WtInit<8, 1> g_wt8;
 WtInit<4, 2> g_wt4w;
 WtInit<8, 2> g_wt8w;
 
+// K split of a tile over a cluster when the tiles alone leave at least half
+// the SMs idle: the largest split (in whole chunks, at most 8) whose CTAs fit
+// one per SM and whose clusters are all resident at once.  A positive hint
+// forces the split (any split up to 8 and the chunk count is correct).
+int wt_split(int64_t tiles, int nchunks, int num_sms, int hint, const int (&max_cl)[9]) {
+  if (hint > 0) return (hint <= 8 && hint <= nchunks && max_cl[hint] > 0) ? hint : -1;
+  int best = 1;
+  if (tiles * 2 > num_sms) return best;
+  for (int cs = 2; cs <= 8 && cs <= nchunks; ++cs)
+    if (tiles * cs <= num_sms && tiles <= max_cl[cs]) best = cs;
+  return best;
+}
+
 template <int BITS, int HALVES>
 cudaError_t launch_wt(const GemmArgs& a, cudaStream_t stream, WtEncodeFn enc) {
   using C = WtCfg<BITS, HALVES>;
   constexpr int kTN = C::kTN;
-  cudaError_t e = BITS == 4 ? (HALVES == 2 ? g_wt4w.ensure(a.device) : g_wt4.ensure(a.device))
-                            : (HALVES == 2 ? g_wt8w.ensure(a.device) : g_wt8.ensure(a.device));
+  int max_cl[9];
+  cudaError_t e = BITS == 4 ? (HALVES == 2 ? g_wt4w.ensure(a.device, max_cl)
+                                           : g_wt4.ensure(a.device, max_cl))
+                            : (HALVES == 2 ? g_wt8w.ensure(a.device, max_cl)
+                                           : g_wt8.ensure(a.device, max_cl));
   if (e != cudaSuccess) return e;
 
-  // X as a 2-D bf16 tensor [M rows, K cols]; box 64 x 128, 128-byte swizzle;
-  // rows past M read as zeros.
+  // X as a 3-D bf16 tensor [K/64 blocks][M rows][64]: one box is the two
+  // 64-deep stages of a group for 128 rows (128-byte swizzle); rows past M
+  // read as zeros.  A copy costs the copy engine about the same whatever its
+  // size, so each group's X is one copy.
   CUtensorMap tmx;
-  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(a.M)};
-  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(a.K) * 2};
-  const cuuint32_t box[2] = {64, kTM};
-  const cuuint32_t estride[2] = {1, 1};
-  CUresult r = enc(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.X), gdim,
+  const cuuint64_t gdim[3] = {64, static_cast<cuuint64_t>(a.M), static_cast<cuuint64_t>(a.K / 64)};
+  const cuuint64_t gstride[2] = {static_cast<cuuint64_t>(a.K) * 2, 128};
+  const cuuint32_t box[3] = {64, kTM, 2};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = enc(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.X), gdim,
                    gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  // The packed weights as a 2-D u32 tensor of 128-byte rows; one box is the
-  // kChunk consecutive cells of one cell column.
+  // The packed weights as a 3-D u32 tensor [N/64 cell columns][G cells x
+  // 128-byte rows][32 words]; one box is kChunk consecutive cells of every
+  // cell column of a tile.
   CUtensorMap tmw;
-  const int64_t words = BITS == 4 ? a.K * a.N / 8 : a.K * a.N / 4;
-  const cuuint64_t wdim[2] = {32, static_cast<cuuint64_t>(words / 32)};
-  const cuuint64_t wstride[1] = {128};
-  const cuuint32_t wbox[2] = {32, static_cast<cuuint32_t>(C::kChunk * C::kCellRows)};
-  r = enc(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(a.Wp), wdim, wstride,
+  const cuuint64_t groups = static_cast<cuuint64_t>(a.K / 128);
+  const cuuint64_t wdim[3] = {32, groups * C::kCellRows,
+                              static_cast<cuuint64_t>(a.N / 64)};
+  const cuuint64_t wstride[2] = {128, groups * C::kCellBytes};
+  const cuuint32_t wbox[3] = {32, static_cast<cuuint32_t>(C::kChunk * C::kCellRows),
+                              static_cast<cuuint32_t>(C::kCellCols)};
+  r = enc(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(a.Wp), wdim, wstride,
           wbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
@@ -486,17 +598,32 @@ cudaError_t launch_wt(const GemmArgs& a, cudaStream_t stream, WtEncodeFn enc) {
   p.diag.wait_limit_ns = a.diag.wait_limit_ns;
   p.diag.force_timeout = a.diag.force_timeout;
   const int64_t tiles = static_cast<int64_t>(p.mt) * p.nt;
+  const int ks = HALVES == 1 ? wt_split(tiles, p.G / C::kChunk, a.num_sms, a.split_hint, max_cl) : 1;
+  if (ks < 1) return cudaErrorNotSupported;
+  p.ks = ks;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(tiles < a.num_sms ? tiles : a.num_sms));
+  // K split: one cluster of ks CTAs per tile; else persistent, one CTA per SM
+  cfg.gridDim = dim3(static_cast<unsigned>(ks > 1 ? tiles * ks : (tiles < a.num_sms ? tiles : a.num_sms)));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr.val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = a.pdl ? 1 : 0;
+  cudaLaunchAttribute attrs[2];
+  int na = 0;
+  if (ks > 1) {
+    attrs[na].id = cudaLaunchAttributeClusterDimension;
+    attrs[na].val.clusterDim.x = ks;
+    attrs[na].val.clusterDim.y = 1;
+    attrs[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (a.pdl) {
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, gemm_wt_kernel<BITS, HALVES>, tmx, tmw, p);
 }
 
