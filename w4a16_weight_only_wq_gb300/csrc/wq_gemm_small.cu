@@ -42,9 +42,9 @@ constexpr int kConsumerWarps = 16;
 constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kChunk = 4;                  // groups per weight chunk
-constexpr int kRedStride = 33;             // floats per row of a half-tile partial
+constexpr int kRedStride = 36;             // floats per row of a half-tile partial (16-byte rows)
 constexpr int kRedBytes = kConsumerWarps * 16 * kRedStride * 4;
-constexpr int kPartFloats = 1024 + 8;      // cs slices of ceil(1024 / cs) floats
+constexpr int kPartFloats = 1024 + 64;     // cs slices of ceil(256 / cs) quads of floats
 
 template <int BITS>
 struct Cell {
@@ -312,50 +312,63 @@ gemm_small_kernel(const SmallParams p) {
   }
 
   // CTA reduction in a fixed order: every consumer warp stores its partial
-  // half tile ([16 rows][32 cols], rows padded to 33 floats), then each
-  // thread sums one element over the eight warps of that half, in order.
+  // half tile ([16 rows][32 cols], rows padded to 36 floats), then each
+  // thread sums a quad of 4 consecutive columns over the eight warps of that
+  // half, in order, with 16-byte loads.
   const int gl = lane >> 2, t4 = lane & 3;
   if (warp < kConsumerWarps) {
-    float* dst = red + warp * 16 * kRedStride;
+    const uint32_t dst = smem_addr(red + warp * 16 * kRedStride);
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const int col = t * 8 + 2 * t4;
-      dst[gl * kRedStride + col] = acc[t][0];
-      dst[gl * kRedStride + col + 1] = acc[t][1];
-      dst[(gl + 8) * kRedStride + col] = acc[t][2];
-      dst[(gl + 8) * kRedStride + col + 1] = acc[t][3];
+      st_shared_v2_f32(dst + (gl * kRedStride + col) * 4, acc[t][0], acc[t][1]);
+      st_shared_v2_f32(dst + ((gl + 8) * kRedStride + col) * 4, acc[t][2], acc[t][3]);
     }
   }
   __syncthreads();
-  // Element e = row * 64 + col of the tile.  With a cluster, rank r owns
-  // elements [r E / cs, (r + 1) E / cs) and receives every rank's partial
-  // of them in its `part` (slice q at q * slice), by remote stores.
-  const int E = rows * 64;
+  // Quad e = row * 16 + col / 4 of the tile.  With a cluster, rank r owns
+  // quads [r E / cs, (r + 1) E / cs) and receives every rank's partial of
+  // them in its `part` (slice q at q * slice quads), by 16-byte remote stores.
+  const int E = rows * 16;
   const int slice = (E + cs - 1) / cs;
   if (cs > 1) cluster_wait();
   for (int e = threadIdx.x; e < E; e += kThreads) {
-    const int r = e >> 6, c = e & 63, h = c >> 5, cc = c & 31;
-    float v = 0.f;
+    const int r = e >> 4, c = (e & 15) * 4, h = c >> 5, cc = c & 31;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < kConsumerWarps / 2; ++k)
-      v += red[(2 * k + h) * 16 * kRedStride + r * kRedStride + cc];
+    for (int k = 0; k < kConsumerWarps / 2; ++k) {
+      const float4 w =
+          ld_shared_v4_f32(smem_addr(red + (2 * k + h) * 16 * kRedStride + r * kRedStride + cc));
+      v.x += w.x;
+      v.y += w.y;
+      v.z += w.z;
+      v.w += w.w;
+    }
     if (cs == 1) {
-      p.Y[static_cast<size_t>(r) * p.N + tile * 64 + c] = __float2bfloat16_rn(v);
+      st_global_v2(p.Y + static_cast<size_t>(r) * p.N + tile * 64 + c,
+                   pack_bf16x2_rn(v.x, v.y), pack_bf16x2_rn(v.z, v.w));
     } else {
       int owner = (e * cs) / E;  // first rank whose range holds e
       while (owner + 1 < cs && e >= ((owner + 1) * E) / cs) ++owner;
       while (e < (owner * E) / cs) --owner;
       const int off = e - (owner * E) / cs;
-      dsmem_st_f32(dsmem_map(part + rank * slice + off, owner), v);
+      dsmem_st_v4_f32(dsmem_map(part + (rank * slice + off) * 4, owner), v.x, v.y, v.z, v.w);
     }
   }
   if (cs == 1) return;
   cluster_sync();  // every partial has arrived in its owner's `part`
   const int e0 = (rank * E) / cs, e1 = ((rank + 1) * E) / cs;
   for (int e = e0 + threadIdx.x; e < e1; e += kThreads) {
-    float v = 0.f;
-    for (int q = 0; q < cs; ++q) v += part[q * slice + (e - e0)];
-    p.Y[static_cast<size_t>(e >> 6) * p.N + tile * 64 + (e & 63)] = __float2bfloat16_rn(v);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < cs; ++q) {
+      const float4 w = ld_shared_v4_f32(smem_addr(part + (q * slice + (e - e0)) * 4));
+      v.x += w.x;
+      v.y += w.y;
+      v.z += w.z;
+      v.w += w.w;
+    }
+    st_global_v2(p.Y + static_cast<size_t>(e >> 4) * p.N + tile * 64 + (e & 15) * 4,
+                 pack_bf16x2_rn(v.x, v.y), pack_bf16x2_rn(v.z, v.w));
   }
 }
 
