@@ -186,6 +186,18 @@ __device__ __forceinline__ void dsmem_st_v4_f32(uint32_t cluster_addr, float a, 
                : "memory");
 }
 
+// 16-byte asynchronous store to shared memory of a CTA of the cluster that
+// counts its 16 bytes on that CTA's mbarrier `cluster_bar` (both addresses
+// from dsmem_map; the store address 16-byte aligned).
+__device__ __forceinline__ void dsmem_st_async_v4_f32(uint32_t cluster_addr, uint32_t cluster_bar,
+                                                      float a, float b, float c, float d) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          cluster_addr),
+      "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void dsmem_st_f32(uint32_t cluster_addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
 }

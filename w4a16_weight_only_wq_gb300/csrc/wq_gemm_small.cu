@@ -69,7 +69,7 @@ __host__ __device__ constexpr int wregion_bytes(int wslots, int slot) {
   return wslots * slot > kRedBytes ? wslots * slot : kRedBytes;
 }
 __host__ __device__ constexpr int smem_bytes_for(int wslots, int slot, int xstride) {
-  return wregion_bytes(wslots, slot) + 16 * xstride + kPartFloats * 4 + (2 * wslots + 2) * 8 + 16;
+  return wregion_bytes(wslots, slot) + 16 * xstride + kPartFloats * 4 + (2 * wslots + 3) * 8 + 16;
 }
 // X row stride for ng groups: 256 bytes per group, plus 64 so that rows g
 // and g + 1 sit 64 bytes apart modulo 128 (conflict-free fragment loads).
@@ -191,7 +191,8 @@ gemm_small_kernel(const SmallParams p) {
   uint64_t* wempty = wfull + DW;
   uint64_t* xfull = wempty + DW;
   uint64_t* never_bar = xfull + 1;
-  int& s_err = *reinterpret_cast<int*>(never_bar + 1);
+  uint64_t* part_full = never_bar + 1;  // every rank's partials of my quads landed
+  int& s_err = *reinterpret_cast<int*>(part_full + 1);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < DW; ++i) {
@@ -200,6 +201,7 @@ gemm_small_kernel(const SmallParams p) {
     }
     mbar_init(xfull, 1);
     mbar_init(never_bar, 1);
+    mbar_init(part_full, 1);
     fence_mbar_init();
     s_err = 0;
   }
@@ -328,10 +330,16 @@ gemm_small_kernel(const SmallParams p) {
   __syncthreads();
   // Quad e = row * 16 + col / 4 of the tile.  With a cluster, rank r owns
   // quads [r E / cs, (r + 1) E / cs) and receives every rank's partial of
-  // them in its `part` (slice q at q * slice quads), by 16-byte remote stores.
+  // them in its `part` (slice q at q * slice quads) by 16-byte asynchronous
+  // remote stores that count their bytes on its `part_full` barrier, so the
+  // owner waits for exactly its bytes instead of a second cluster barrier.
   const int E = rows * 16;
   const int slice = (E + cs - 1) / cs;
-  if (cs > 1) cluster_wait();
+  const int e0 = (rank * E) / cs, e1 = ((rank + 1) * E) / cs;
+  if (cs > 1) {
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(part_full, cs * (e1 - e0) * 16);
+    cluster_wait();  // every CTA of the cluster has initialised its barriers
+  }
   for (int e = threadIdx.x; e < E; e += kThreads) {
     const int r = e >> 4, c = (e & 15) * 4, h = c >> 5, cc = c & 31;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -352,12 +360,12 @@ gemm_small_kernel(const SmallParams p) {
       while (owner + 1 < cs && e >= ((owner + 1) * E) / cs) ++owner;
       while (e < (owner * E) / cs) --owner;
       const int off = e - (owner * E) / cs;
-      dsmem_st_v4_f32(dsmem_map(part + (rank * slice + off) * 4, owner), v.x, v.y, v.z, v.w);
+      dsmem_st_async_v4_f32(dsmem_map(part + (rank * slice + off) * 4, owner),
+                            dsmem_map(part_full, owner), v.x, v.y, v.z, v.w);
     }
   }
-  if (cs == 1) return;
-  cluster_sync();  // every partial has arrived in its owner's `part`
-  const int e0 = (rank * E) / cs, e1 = ((rank + 1) * E) / cs;
+  if (cs == 1 || e0 + static_cast<int>(threadIdx.x) >= e1) return;
+  if (!mbar_wait_bounded(part_full, 0, p.diag)) return;
   for (int e = e0 + threadIdx.x; e < e1; e += kThreads) {
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int q = 0; q < cs; ++q) {
