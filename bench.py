@@ -573,9 +573,74 @@ def run_sweep(args):
             "bytes": nbytes, "rotation": reps}), flush=True)
         del bufs, g
         torch.cuda.empty_cache()
+    if not args.shape and args.only in "c2_mlp_fused":
+        sweep_mlp_pair(wq, synth, stream, sh, l2, peak, peak_kind)
     if wq.wq_last_device_error() != wq.WQ_OK:
         raise RuntimeError("a bounded in-kernel wait ran out during the sweep")
     return 0
+
+
+def sweep_mlp_pair(wq, synth, stream, sh, l2, peak, peak_kind):
+    """The MLP-shaped pair at M=16 through the fused call (one API call for
+    both projections, the activation in the up-projection's store), for each
+    activation; bytes are both projections' algorithmic bytes."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    up_case, dn_case = synth.C2[0], synth.C2[1]
+    du, dd = up_case.draw(), dn_case.draw()
+    m, k, n1, n2 = up_case.M, up_case.K, up_case.N, dn_case.N
+    nbytes = algorithmic_bytes(m, k, n1) + algorithmic_bytes(m, n1, n2)
+    reps = max(2, math.ceil(2.0 * l2 / nbytes) + 1)
+
+    def dev_bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    wu = wq.pack_codes(torch.from_numpy(du["q"]).to(dev), 4)
+    wd = wq.pack_codes(torch.from_numpy(dd["q"]).to(dev), 4)
+    su, sd, x = dev_bf16(du["s"]), dev_bf16(dd["s"]), dev_bf16(du["X"])
+    bufs = [(x.clone(), wu.clone(), su.clone(), wd.clone(), sd.clone(),
+             torch.empty((m, n1), dtype=torch.bfloat16, device=dev),
+             torch.empty((m, n2), dtype=torch.bfloat16, device=dev)) for _ in range(reps)]
+    for act_name, act in (("none", wq.WQ_ACT_NONE), ("silu", wq.WQ_ACT_SILU)):
+        def call(i):
+            xb, wub, sub, wdb, sdb, hb, yb = bufs[i % reps]
+            st = wq.wq_mlp_w4a16(xb.data_ptr(), wub.data_ptr(), sub.data_ptr(), wdb.data_ptr(),
+                                 sdb.data_ptr(), hb.data_ptr(), yb.data_ptr(), m, k, n1, n2,
+                                 GROUP, act, sh)
+            if st != 0:
+                raise RuntimeError(wq.status_string(st))
+
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                call(i)
+        stream.synchronize()
+        per_graph = reps * max(1, 100 // reps)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(per_graph):
+                call(i)
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(5):
+                g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / (5 * per_graph)
+        gbs = nbytes / us / 1e3
+        print(json.dumps({
+            "case": f"c2_mlp_fused_{act_name}_w4_m16_{k}x{n1}x{n2}", "bits": 4, "M": m,
+            "K": k, "N1": n1, "N2": n2, "act": act_name, "us_per_pair": us, "GB/s": gbs,
+            "hbm_frac": gbs / peak, "peak_source": peak_kind, "bytes": nbytes,
+            "rotation": reps}), flush=True)
+        del g
+    del bufs
+    torch.cuda.empty_cache()
 
 
 def main():

@@ -76,6 +76,9 @@ typedef enum {
 
 typedef enum { WQ_F32 = 0, WQ_BF16 = 1 } wq_dtype;
 
+/* Activation between the two projections of wq_mlp_w4a16 / wq_mlp_w8a16. */
+typedef enum { WQ_ACT_NONE = 0, WQ_ACT_SILU = 1 } wq_act;
+
 /* Number of uint32 words in a packed [K,N] weight with `bits` (4 or 8)
    bits per code: K*N/8 or K*N/4.  Returns 0 for unsupported arguments. */
 WQ_API size_t wq_packed_words(int bits, int64_t K, int64_t N);
@@ -161,6 +164,33 @@ WQ_API wq_status wq_gemm_w4a16(const void* X, const uint32_t* Wp, const void* sc
 WQ_API wq_status wq_gemm_w8a16(const void* X, const uint32_t* Wp, const void* scales,
                         void* Y, int64_t M, int64_t N, int64_t K, int group,
                         cudaStream_t stream);
+
+/*
+ * The two quantized projections of one MLP block in one call (the INT4
+ * target's verifier forward, "Quantize the Target, Quantize the Drafter"):
+ *   H = act(bf16(X . dequant(Wu, Su)))   X bf16 [M,K], Wu [K,N1], H bf16 [M,N1]
+ *   Y = bf16(H . dequant(Wd, Sd))        Wd [N1,N2], Y bf16 [M,N2]
+ * act: WQ_ACT_NONE, or WQ_ACT_SILU = the up-projection's bf16 result h
+ * mapped to h / (1 + e^-h) in fp32 and rounded to bf16 (the pages name no
+ * activation; SiLU is the one the target family uses).  H is caller-owned
+ * device memory and holds the activated intermediate on return.  Each
+ * projection runs the kernel wq_gemm_w4a16 would pick (the activation is
+ * applied in the store of the warp-MMA and tensor-memory tiled kernels, in a
+ * separate pass otherwise); with the warp-MMA kernel the up-projection also
+ * pulls Wd into L2 once its own weights have landed.  Shapes and errors as
+ * for the GEMMs (K, N1 multiples of 128; N1, N2 multiples of 64; 16-byte
+ * aligned pointers), plus WQ_ERR_UNSUPPORTED for an unknown act.  H and Y
+ * must not overlap each other or the inputs.  Stream-ordered; allocates
+ * nothing.  wq_mlp_w8a16: the same with packed INT8 weights.
+ */
+WQ_API wq_status wq_mlp_w4a16(const void* X, const uint32_t* Wu, const void* Su,
+                              const uint32_t* Wd, const void* Sd, void* H, void* Y,
+                              int64_t M, int64_t K, int64_t N1, int64_t N2, int group,
+                              int act, cudaStream_t stream);
+WQ_API wq_status wq_mlp_w8a16(const void* X, const uint32_t* Wu, const void* Su,
+                              const uint32_t* Wd, const void* Sd, void* H, void* Y,
+                              int64_t M, int64_t K, int64_t N1, int64_t N2, int group,
+                              int act, cudaStream_t stream);
 
 /* The per-device error word of the current device: WQ_OK or
    WQ_ERR_DEVICE_TIMEOUT.  Synchronous (reads device memory); call after

@@ -66,6 +66,8 @@ def _bind(lib):
     lib.wqo_quantize.argtypes = [P, P, I64, I64, I, I, P]
     lib.wqo_widen_bf16.argtypes = [P, I64, P]
     lib.wqo_round_bf16.argtypes = [P, I64, P]
+    lib.wqo_round_bf16_f64.argtypes = [P, I64, P]
+    lib.wqo_silu_bf16.argtypes = [P, I64, P]
     lib.wqo_packed_words.argtypes = [I, I64, I64]
     lib.wqo_packed_words.restype = I64
     lib.wqo_pack.argtypes = [P, I64, I64, I, P]
@@ -249,6 +251,35 @@ def gemm(X_bf16: np.ndarray, packed: np.ndarray, s: np.ndarray, K: int, N: int,
     if rc != 0:
         raise MemoryError("oracle GEMM could not allocate its dequant buffer")
     return Y
+
+
+def round_bf16_f64(x: np.ndarray) -> np.ndarray:
+    """fp64 -> bf16 bit patterns (uint16), round to nearest even, directly."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().wqo_round_bf16_f64(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def silu_bf16(h_bits: np.ndarray) -> np.ndarray:
+    """bf16 bits -> bf16 bits of silu(h) = h / (1 + e^-h) (fp64, then RNE)."""
+    h = np.ascontiguousarray(h_bits, dtype=np.uint16)
+    out = np.empty(h.shape, dtype=np.uint16)
+    _load().wqo_silu_bf16(_ptr(h), h.size, _ptr(out))
+    return out
+
+
+def mlp(X_bf16: np.ndarray, packed_up: np.ndarray, s_up: np.ndarray, packed_down: np.ndarray,
+        s_down: np.ndarray, K: int, N1: int, N2: int, bits: int, act: str = "none",
+        rows=None, nthreads=None):
+    """The MLP pair: H = act(bf16(X . Wu)) as bf16 bits [M, N1] and
+    Y_ref = H . Wd in fp64 ([len(rows), N2]).  act is "none" or "silu"."""
+    if act not in ("none", "silu"):
+        raise ValueError("act must be 'none' or 'silu'")
+    H = round_bf16_f64(gemm(X_bf16, packed_up, s_up, K, N1, bits, nthreads=nthreads))
+    if act == "silu":
+        H = silu_bf16(H)
+    return H, gemm(H, packed_down, s_down, N1, N2, bits, rows=rows, nthreads=nthreads)
 
 
 def tolerance(Y_ref: np.ndarray) -> float:

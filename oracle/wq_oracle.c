@@ -27,6 +27,10 @@
  *  - bf16 weights are widened to fp32 exactly before the divide.
  *  - dequant w^ = fp32(s) * fp32(q) is exact in fp32 (<= 8 + 8 significant
  *    bits); the GEMM accumulates in fp64.
+ *  - the MLP pair's intermediate (the pages name no activation): the
+ *    up-projection rounded to bf16 (RNE, straight from fp64), then either
+ *    kept or mapped through silu(h) = h / (1 + e^-h) in fp64 and rounded to
+ *    bf16 again; the down-projection reads those bf16 values.
  *
  * Build: gcc -O2 -ffp-contract=off -fno-fast-math -shared -fPIC -pthread.
  * Everything here is single-threaded and element-by-element, except
@@ -60,6 +64,34 @@ static uint16_t f32_to_bf16_rne(float f) {
 }
 
 uint16_t wqo_f32_to_bf16(float f) { return f32_to_bf16_rne(f); }
+
+/* Round a binary64 to bf16 directly (8 significant bits, ties to even, bf16
+   subnormal spacing 2^-133), without passing through binary32. */
+static uint16_t f64_to_bf16_rne(double x) {
+  if (x == 0.0 || !isfinite(x)) return f32_to_bf16_rne((float)x);
+  int e;
+  frexp(x, &e);           /* |x| = m 2^e, m in [0.5, 1) */
+  int q = e - 8;          /* exponent of the last kept bit */
+  if (q < -133) q = -133;
+  const double r = nearbyint(ldexp(x, -q));  /* default mode: ties to even */
+  const float f = (float)ldexp(r, q);        /* exact: <= 8 significant bits */
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return (uint16_t)(u >> 16);
+}
+
+void wqo_round_bf16_f64(const double* x, int64_t count, uint16_t* out) {
+  for (int64_t i = 0; i < count; ++i) out[i] = f64_to_bf16_rne(x[i]);
+}
+
+/* The MLP activation on bf16 values: silu(h) = h / (1 + e^-h) in fp64,
+   rounded to bf16. */
+void wqo_silu_bf16(const uint16_t* h, int64_t count, uint16_t* out) {
+  for (int64_t i = 0; i < count; ++i) {
+    const double v = (double)bf16_to_f32(h[i]);
+    out[i] = f64_to_bf16_rne(v / (1.0 + exp(-v)));
+  }
+}
 float wqo_bf16_to_f32(uint16_t h) { return bf16_to_f32(h); }
 
 /* --------------------------------------------------------- code ranges -- */

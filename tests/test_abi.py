@@ -70,6 +70,17 @@ def test_argument_errors_without_gpu(wq):
     assert wq.wq_dequantize(A, A, 5, 128, 64, 128, A, s) == wq.WQ_ERR_UNSUPPORTED
     assert wq.wq_dequantize(A, A, 4, 128, 64, 64, A, s) == wq.WQ_ERR_SHAPE
     assert wq.wq_dequantize(A, A, 8, 256, 64, 128, A + 2, s) == wq.WQ_ERR_ALIGN
+    # fused MLP pair: X, Wu, Su, Wd, Sd, H, Y, M, K, N1, N2, group, act, stream
+    mlp = wq.wq_mlp_w4a16
+    assert mlp(None, A, A, A, A, A, A, 16, 128, 128, 64, 128, 0, s) == wq.WQ_ERR_NULL
+    assert mlp(A, A, A, A, A, None, A, 16, 128, 128, 64, 128, 0, s) == wq.WQ_ERR_NULL
+    assert mlp(A, A, A, A, A, A, A, 16, 128, 128, 64, 128, 2, s) == wq.WQ_ERR_UNSUPPORTED
+    assert mlp(A, A, A, A, A, A, A, 16, 100, 128, 64, 128, 1, s) == wq.WQ_ERR_SHAPE
+    assert mlp(A, A, A, A, A, A, A, 16, 128, 192, 64, 128, 1, s) == wq.WQ_ERR_SHAPE
+    assert mlp(A, A, A, A, A, A, A, 16, 128, 128, 96, 128, 0, s) == wq.WQ_ERR_SHAPE
+    assert mlp(A, A, A, A, A, A + 8, A, 16, 128, 128, 64, 128, 0, s) == wq.WQ_ERR_ALIGN
+    assert wq.wq_mlp_w8a16(A, A, A, A, A, A, A, 16, 128, 128, 64, 64, 0, s) == wq.WQ_ERR_SHAPE
+    assert mlp(A, A, A, A, A, A, A, 0, 128, 128, 64, 128, 1, s) == wq.WQ_OK
 
 
 def test_status_strings(wq):

@@ -335,3 +335,83 @@ def test_import_nk_round_trip(bits):
                                            bits)
     assert np.array_equal(got_q, q)
     assert np.array_equal(got_s, s)
+
+
+# ------------------------------------------------------------- MLP pair ---
+def _bits(x: float) -> int:
+    return int(np.array([x], dtype=np.float32).view(np.uint32)[0] >> 16)
+
+
+def test_round_bf16_f64_ties_and_ranges():
+    """Direct fp64 -> bf16 rounding: ties go to the even neighbour, a value
+    just past a tie rounds away (an fp32 step would make it a tie), the
+    subnormal grid is 2^-133, and past the largest bf16 lies infinity."""
+    cases = [
+        (1.0 + 2.0 ** -8, 0x3F80),                  # tie -> even (1.0)
+        (1.0 + 3 * 2.0 ** -8, 0x3F82),              # tie -> even (1 + 2^-6)
+        (1.0 + 2.0 ** -8 + 2.0 ** -40, 0x3F81),     # just past the tie
+        (-(1.0 + 2.0 ** -8 + 2.0 ** -40), 0xBF81),
+        (0.0, 0x0000),
+        (-0.0, 0x8000),
+        (2.0 ** -140, 0x0000),                      # below half the subnormal step
+        (1.5 * 2.0 ** -133, 0x0002),                # subnormal tie -> even
+        (2.0 ** 130, 0x7F80),                       # overflow
+        (3.0, 0x4040),
+    ]
+    x = np.array([c[0] for c in cases], dtype=np.float64)
+    got = oracle.round_bf16_f64(x)
+    assert [int(v) for v in got] == [c[1] for c in cases]
+
+
+def test_silu_closed_form_values():
+    """silu(h) = h * sigma(h): silu(0) = 0, silu(1) = e / (1 + e),
+    silu(-1) = -1 / (1 + e), silu(h) -> h for large h and -> -0 for very
+    negative h."""
+    e = 2.718281828459045
+    h = np.array([_bits(v) for v in (0.0, 1.0, -1.0, 30.0, -200.0, 2.0)], dtype=np.uint16)
+    got = oracle.silu_bf16(h)
+    want = oracle.round_bf16_f64(np.array([0.0, e / (1 + e), -1 / (1 + e), 30.0, -0.0,
+                                           2 * e * e / (1 + e * e)]))
+    assert [int(v) for v in got] == [int(v) for v in want]
+    assert int(got[1]) == 0x3F3B and int(got[2]) == 0xBE8A  # 0.73046875, -0.26953125
+
+
+def test_silu_minimum_and_odd_part():
+    """Over every bf16 value in [-16, 16]: silu never goes below its global
+    minimum (-0.2784645...), and silu(h) - silu(-h) = h up to the two
+    roundings."""
+    grid = np.arange(0x0000, 0x4180, dtype=np.uint32)        # 0 .. 16
+    pos = grid.astype(np.uint16)
+    neg = (grid | 0x8000).astype(np.uint16)
+    sp = oracle.bf16_bits_to_f32(oracle.silu_bf16(pos)).astype(np.float64)
+    sn = oracle.bf16_bits_to_f32(oracle.silu_bf16(neg)).astype(np.float64)
+    h = oracle.bf16_bits_to_f32(pos).astype(np.float64)
+    assert sn.min() >= -0.2784645428 * (1 + 2.0 ** -7)
+    ulp = np.maximum(np.abs(sp), np.abs(h)) * 2.0 ** -7 + 2.0 ** -133
+    assert np.all(np.abs((sp - sn) - h) <= ulp)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("act", ["none", "silu"])
+def test_mlp_one_hot_rows_bruteforce(bits, act):
+    """One-hot rows of X pick rows of the up-projection's weight: H row k =
+    act(bf16(s q)[k, :]), and Y = H . dequant(Wd) by a plain fp64 matmul."""
+    K, N1, N2 = 256, 128, 64
+    rng = np.random.default_rng(70 + bits)
+    lo, hi = (-8, 7) if bits == 4 else (-128, 127)
+    qu = rng.integers(lo, hi + 1, size=(K, N1)).astype(np.int8)
+    qd = rng.integers(lo, hi + 1, size=(N1, N2)).astype(np.int8)
+    su = oracle.f32_to_bf16_bits(rng.uniform(0.01, 0.05, size=(K // 128, N1)).astype(np.float32))
+    sd = oracle.f32_to_bf16_bits(rng.uniform(0.01, 0.05, size=(N1 // 128, N2)).astype(np.float32))
+    ks = np.array([0, 5, 127, 128, 255])
+    X = np.zeros((ks.size, K), dtype=np.float32)
+    X[np.arange(ks.size), ks] = 1.0
+    H, Y = oracle.mlp(oracle.f32_to_bf16_bits(X), oracle.pack(qu, bits), su,
+                      oracle.pack(qd, bits), sd, K, N1, N2, bits, act=act)
+    wu = oracle.dequant(qu, su)            # exact fp32 s * q
+    Hk = oracle.f32_to_bf16_bits(wu[ks])   # one rounding of the exact s * q
+    if act == "silu":
+        Hk = oracle.silu_bf16(Hk)
+    assert np.array_equal(H, Hk)
+    Yk = oracle.bf16_bits_to_f32(Hk).astype(np.float64) @ oracle.dequant(qd, sd).astype(np.float64)
+    assert np.allclose(Y, Yk, rtol=1e-12, atol=1e-12)

@@ -31,12 +31,14 @@ WQ_ERR_CUDA = 5
 WQ_ERR_DEVICE_TIMEOUT = 6
 WQ_F32 = 0
 WQ_BF16 = 1
+WQ_ACT_NONE = 0
+WQ_ACT_SILU = 1
 GROUP = 128
 
 EXPORTED = (
     "wq_packed_words", "wq_pack_symmetric", "wq_pack_codes", "wq_unpack", "wq_dequantize",
     "wq_import_packed_nk",
-    "wq_gemm_w4a16", "wq_gemm_w8a16", "wq_last_device_error",
+    "wq_gemm_w4a16", "wq_gemm_w8a16", "wq_mlp_w4a16", "wq_mlp_w8a16", "wq_last_device_error",
     "wq_clear_device_error", "wq_status_string", "wq_debug_set_wait_limit_ns",
     "wq_debug_force_timeout", "wq_gemm_regime", "wq_debug_set_split",
     "wq_set_programmatic_launch", "wq_last_cuda_error", "wq_debug_force_regime",
@@ -68,6 +70,8 @@ def _load() -> ctypes.CDLL:
         "wq_import_packed_nk": ([P, P, I, I64, I64, I, P, P, P], I),
         "wq_gemm_w4a16": ([P, P, P, P, I64, I64, I64, I, P], I),
         "wq_gemm_w8a16": ([P, P, P, P, I64, I64, I64, I, P], I),
+        "wq_mlp_w4a16": ([P, P, P, P, P, P, P, I64, I64, I64, I64, I, I, P], I),
+        "wq_mlp_w8a16": ([P, P, P, P, P, P, P, I64, I64, I64, I64, I, I, P], I),
         "wq_last_device_error": ([], I),
         "wq_clear_device_error": ([], I),
         "wq_status_string": ([I], ctypes.c_char_p),
@@ -282,3 +286,35 @@ def gemm_w8a16(X: torch.Tensor, Wp: torch.Tensor, scales: torch.Tensor,
     """Y[M,N] = X[M,K] . dequant(Wp INT8, scales)."""
     N = scales.shape[1] if N is None else N
     return _gemm(wq_gemm_w8a16, "wq_gemm_w8a16", X, Wp, scales, N, Y, stream)
+
+
+def wq_mlp_w4a16(X, Wu, Su, Wd, Sd, H, Y, M, K, N1, N2, group, act, stream) -> int:
+    return _lib.wq_mlp_w4a16(X, Wu, Su, Wd, Sd, H, Y, M, K, N1, N2, group, act, stream)
+
+
+def wq_mlp_w8a16(X, Wu, Su, Wd, Sd, H, Y, M, K, N1, N2, group, act, stream) -> int:
+    return _lib.wq_mlp_w8a16(X, Wu, Su, Wd, Sd, H, Y, M, K, N1, N2, group, act, stream)
+
+
+_ACTS = {"none": WQ_ACT_NONE, "silu": WQ_ACT_SILU}
+
+
+def mlp(X: torch.Tensor, Wu: torch.Tensor, Su: torch.Tensor, Wd: torch.Tensor,
+        Sd: torch.Tensor, bits: int, act: str = "none", H: torch.Tensor | None = None,
+        Y: torch.Tensor | None = None, stream=None):
+    """The two projections of an MLP block: H = act(bf16(X . Wu)),
+    Y = bf16(H . Wd).  Returns (H, Y)."""
+    M, K = X.shape
+    N1, N2 = Su.shape[1], Sd.shape[1]
+    if X.dtype != torch.bfloat16 or Su.dtype != torch.bfloat16 or Sd.dtype != torch.bfloat16:
+        raise ValueError("X and scales must be bfloat16")
+    if act not in _ACTS:
+        raise ValueError(f"act must be one of {sorted(_ACTS)}")
+    if H is None:
+        H = torch.empty((M, N1), dtype=torch.bfloat16, device=X.device)
+    if Y is None:
+        Y = torch.empty((M, N2), dtype=torch.bfloat16, device=X.device)
+    fn, name = (wq_mlp_w4a16, "wq_mlp_w4a16") if bits == 4 else (wq_mlp_w8a16, "wq_mlp_w8a16")
+    _check(fn(_ptr(X), _ptr(Wu), _ptr(Su), _ptr(Wd), _ptr(Sd), _ptr(H), _ptr(Y), M, K, N1, N2,
+              GROUP, _ACTS[act], _stream(stream)), name)
+    return H, Y

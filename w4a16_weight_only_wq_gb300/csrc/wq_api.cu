@@ -97,9 +97,8 @@ wq::DiagHost diag_for(const DeviceInfo& d) {
   return h;
 }
 
-wq_status gemm_common(int bits, const void* X, const uint32_t* Wp,
-                      const void* scales, void* Y, int64_t M, int64_t N,
-                      int64_t K, int group, cudaStream_t stream) {
+wq_status check_gemm(const void* X, const uint32_t* Wp, const void* scales, const void* Y,
+                     int64_t M, int64_t N, int64_t K, int group) {
   if (!X || !Wp || !scales || !Y) return M == 0 ? WQ_OK : WQ_ERR_NULL;
   if (group != 128) return WQ_ERR_SHAPE;
   if (M < 0 || M > (int64_t(1) << 30)) return WQ_ERR_SHAPE;
@@ -108,10 +107,22 @@ wq_status gemm_common(int bits, const void* X, const uint32_t* Wp,
   if (M * K >= (int64_t(1) << 40) || M * N >= (int64_t(1) << 40)) return WQ_ERR_SHAPE;
   if (!aligned16(X) || !aligned16(Wp) || !aligned16(scales) || !aligned16(Y))
     return WQ_ERR_ALIGN;
+  return WQ_OK;
+}
+
+// One GEMM on the chosen kernel family, arguments already checked.  act: the
+// activation of the fused MLP's up-projection; *act_done tells whether the
+// kernel applied it (the warp-MMA and tensor-memory tiled kernels do).
+// pf / pf_bytes: weights of the GEMM that follows, pulled into L2 by the
+// warp-MMA kernel after its own weights have landed.
+wq_status gemm_run(int bits, const void* X, const uint32_t* Wp, const void* scales, void* Y,
+                   int64_t M, int64_t N, int64_t K, cudaStream_t stream, int act,
+                   const void* pf, int64_t pf_bytes, bool* act_done) {
+  *act_done = act == 0;
   if (M == 0) return WQ_OK;
   int dev;
   DeviceInfo d;
-  st = device_info(&dev, &d);
+  wq_status st = device_info(&dev, &d);
   if (st != WQ_OK) return st;
   wq::GemmArgs a;
   a.X = X;
@@ -126,13 +137,18 @@ wq_status gemm_common(int bits, const void* X, const uint32_t* Wp,
   a.device = dev;
   a.pdl = g_pdl.load();
   a.split_hint = g_split_hint.load();
+  a.act = 0;
+  a.l2_prefetch = nullptr;
+  a.l2_prefetch_bytes = 0;
   a.diag = diag_for(d);
   int regime = pick_regime(M);
   if (regime == 0 && !wq::gemm_small_fits(bits, K, N, a.split_hint)) regime = 1;
   if (regime == 3 && !wq::gemm_wt_fits(bits, M, K, N)) regime = 1;
   if (regime == 3) {
+    a.act = act;
     cudaError_t e = wq::launch_gemm_wt(a, stream);
     if (e == cudaErrorNotSupported) return WQ_ERR_UNSUPPORTED;
+    *act_done = true;
     return cuda_status(e);
   }
   if (regime == 1) {
@@ -143,10 +159,14 @@ wq_status gemm_common(int bits, const void* X, const uint32_t* Wp,
   // The small-M kernels take up to 16 rows per launch; taller inputs are
   // processed in 16-row slices.
   const size_t xrow = static_cast<size_t>(K) * 2, yrow = static_cast<size_t>(N) * 2;
+  if (regime == 0) a.act = act;  // the tensor-memory small-M kernel has no activation
   for (int64_t m0 = 0; m0 < M; m0 += 16) {
     a.X = static_cast<const char*>(X) + m0 * xrow;
     a.Y = static_cast<char*>(Y) + m0 * yrow;
     a.M = (M - m0) < 16 ? (M - m0) : 16;
+    const bool last = m0 + 16 >= M;
+    a.l2_prefetch = last && pf != nullptr && regime == 0 ? pf : nullptr;
+    a.l2_prefetch_bytes = a.l2_prefetch != nullptr ? pf_bytes : 0;
     cudaError_t e = cudaErrorNotSupported;
     if (regime == 2) e = wq::launch_gemm_skinny(a, stream);
     // shapes the tensor-memory kernel cannot index go to the warp-MMA kernel
@@ -154,7 +174,36 @@ wq_status gemm_common(int bits, const void* X, const uint32_t* Wp,
     if (e == cudaErrorNotSupported) return WQ_ERR_SHAPE;
     if (e != cudaSuccess) return cuda_status(e);
   }
+  *act_done = act == 0 || regime == 0;
   return WQ_OK;
+}
+
+wq_status gemm_common(int bits, const void* X, const uint32_t* Wp, const void* scales, void* Y,
+                      int64_t M, int64_t N, int64_t K, int group, cudaStream_t stream) {
+  wq_status st = check_gemm(X, Wp, scales, Y, M, N, K, group);
+  if (st != WQ_OK || M == 0) return st;
+  bool act_done;
+  return gemm_run(bits, X, Wp, scales, Y, M, N, K, stream, 0, nullptr, 0, &act_done);
+}
+
+// The fused MLP pair: H = act(bf16(X . Wu)), Y = bf16(H . Wd).
+wq_status mlp_common(int bits, const void* X, const uint32_t* Wu, const void* Su,
+                     const uint32_t* Wd, const void* Sd, void* H, void* Y, int64_t M, int64_t K,
+                     int64_t N1, int64_t N2, int group, int act, cudaStream_t stream) {
+  if (act != WQ_ACT_NONE && act != WQ_ACT_SILU) return WQ_ERR_UNSUPPORTED;
+  wq_status st = check_gemm(X, Wu, Su, H, M, N1, K, group);
+  if (st != WQ_OK) return st;
+  st = check_gemm(H, Wd, Sd, Y, M, N2, N1, group);
+  if (st != WQ_OK || M == 0) return st;
+  const int64_t wd_bytes = bits == 4 ? N1 * N2 / 2 : N1 * N2;
+  bool act_done = false;
+  st = gemm_run(bits, X, Wu, Su, H, M, N1, K, stream, act, Wd, wd_bytes, &act_done);
+  if (st != WQ_OK) return st;
+  if (!act_done) {
+    st = cuda_status(wq::launch_silu_inplace(static_cast<uint16_t*>(H), M * N1, stream));
+    if (st != WQ_OK) return st;
+  }
+  return gemm_run(bits, H, Wd, Sd, Y, M, N2, N1, stream, 0, nullptr, 0, &act_done);
 }
 
 }  // namespace
@@ -262,6 +311,18 @@ wq_status wq_gemm_w8a16(const void* X, const uint32_t* Wp, const void* scales,
                         void* Y, int64_t M, int64_t N, int64_t K, int group,
                         cudaStream_t stream) {
   return gemm_common(8, X, Wp, scales, Y, M, N, K, group, stream);
+}
+
+wq_status wq_mlp_w4a16(const void* X, const uint32_t* Wu, const void* Su, const uint32_t* Wd,
+                       const void* Sd, void* H, void* Y, int64_t M, int64_t K, int64_t N1,
+                       int64_t N2, int group, int act, cudaStream_t stream) {
+  return mlp_common(4, X, Wu, Su, Wd, Sd, H, Y, M, K, N1, N2, group, act, stream);
+}
+
+wq_status wq_mlp_w8a16(const void* X, const uint32_t* Wu, const void* Su, const uint32_t* Wd,
+                       const void* Sd, void* H, void* Y, int64_t M, int64_t K, int64_t N1,
+                       int64_t N2, int group, int act, cudaStream_t stream) {
+  return mlp_common(8, X, Wu, Su, Wd, Sd, H, Y, M, K, N1, N2, group, act, stream);
 }
 
 wq_status wq_last_device_error(void) {

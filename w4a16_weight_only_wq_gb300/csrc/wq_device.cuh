@@ -290,6 +290,20 @@ __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
   return d;
 }
 
+// The activation applied by the fused MLP's up-projection epilogue: the
+// GEMM's bf16 result h, then silu(h) = h / (1 + e^-h) in fp32 (rounded to
+// bf16 by the caller's store).  act == 0 leaves v as it is.
+__device__ __forceinline__ float apply_act(float v, int act) {
+  if (act == 0) return v;
+  const float h = __bfloat162float(__float2bfloat16_rn(v));
+  return h / (1.0f + expf(-h));
+}
+
+// Pull `bytes` (a multiple of 16, 16-byte aligned) into L2, no destination.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Programmatic dependent launch controls (no-ops without the attribute).
 __device__ __forceinline__ void pdl_wait_primary() {
   asm volatile("griddepcontrol.wait;" ::: "memory");

@@ -61,6 +61,9 @@ struct SmallParams {
   const uint16_t* S;
   __nv_bfloat16* Y;
   int M, N, K, G, cs, wslots, xstride;
+  int act;                  // apply_act on the stored result
+  const uint8_t* pf;        // L2 prefetch range (the next GEMM's weights), or null
+  int64_t pf_bytes;
   KernelDiag diag;
 };
 
@@ -266,6 +269,19 @@ gemm_small_kernel(const SmallParams p) {
       issued = c + 1;
     }
     cp_async_wait_all();
+    if (p.pf != nullptr && issued == nch && lane == 0) {
+      // Once this CTA's last chunk has landed (HBM is then left to the other
+      // CTAs' tails), pull this CTA's share of the next GEMM's weights into L2.
+      const int last = nch - 1;
+      if (mbar_wait_bounded(&wfull[last % DW], (last / DW) & 1, p.diag)) {
+        const int64_t share = ((p.pf_bytes / gridDim.x + 15) / 16) * 16;
+        const int64_t b0 = share * blockIdx.x;
+        const int64_t nb = min(share, p.pf_bytes - b0);
+        if (nb > 0) prefetch_l2_bulk(p.pf + b0, static_cast<uint32_t>(nb));
+      } else {
+        s_err = 1;
+      }
+    }
   } else {
     pdl_launch_dependents();
     pdl_wait_primary();  // consumers store Y, which the preceding kernel may use
@@ -354,7 +370,8 @@ gemm_small_kernel(const SmallParams p) {
     }
     if (cs == 1) {
       st_global_v2(p.Y + static_cast<size_t>(r) * p.N + tile * 64 + c,
-                   pack_bf16x2_rn(v.x, v.y), pack_bf16x2_rn(v.z, v.w));
+                   pack_bf16x2_rn(apply_act(v.x, p.act), apply_act(v.y, p.act)),
+                   pack_bf16x2_rn(apply_act(v.z, p.act), apply_act(v.w, p.act)));
     } else {
       int owner = (e * cs) / E;  // first rank whose range holds e
       while (owner + 1 < cs && e >= ((owner + 1) * E) / cs) ++owner;
@@ -376,7 +393,8 @@ gemm_small_kernel(const SmallParams p) {
       v.w += w.w;
     }
     st_global_v2(p.Y + static_cast<size_t>(e >> 4) * p.N + tile * 64 + (e & 15) * 4,
-                 pack_bf16x2_rn(v.x, v.y), pack_bf16x2_rn(v.z, v.w));
+                 pack_bf16x2_rn(apply_act(v.x, p.act), apply_act(v.y, p.act)),
+                 pack_bf16x2_rn(apply_act(v.z, p.act), apply_act(v.w, p.act)));
   }
 }
 
@@ -466,6 +484,9 @@ cudaError_t launch_gemm_small(const GemmArgs& a, cudaStream_t stream) {
   while (dw > 0 && smem_bytes_for(dw, sb, p.xstride) > max_dyn) --dw;
   if (dw < 1) return cudaErrorNotSupported;
   p.wslots = dw;
+  p.act = a.act;
+  p.pf = static_cast<const uint8_t*>(a.l2_prefetch);
+  p.pf_bytes = a.l2_prefetch != nullptr ? a.l2_prefetch_bytes : 0;
   p.diag.err = a.diag.err;
   p.diag.wait_limit_ns = a.diag.wait_limit_ns;
   p.diag.force_timeout = a.diag.force_timeout;

@@ -95,7 +95,7 @@ struct WtParams {
   KernelDiag diag;
 };
 
-template <int BITS, int HALVES>
+template <int BITS, int HALVES, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                const WtParams p) {
@@ -355,7 +355,8 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
 #pragma unroll
         for (int i = 0; i < 32; ++i)
           st_shared_u16(tb + i * 64 + lane * 2,
-                        __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i]))));
+                        __bfloat16_as_ushort(
+                            __float2bfloat16_rn(apply_act(__uint_as_float(v[i]), ACT))));
         __syncwarp();
         const int ncol0 = (t2 / p.mt) * kTN + hf * 128 + lane_base;  // first column of the block
 #pragma unroll
@@ -452,6 +453,8 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
         for (int j = 0; j < 8; ++j)
           acc[j] += __uint_as_float(ld_shared_u32(base + part_off(src, 8 * cg + j, tok)));
       }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = apply_act(acc[j], ACT);
       st_global_v4(p.Y + static_cast<size_t>(m0 + tok) * p.N + nc, pack_bf16x2(acc[0], acc[1]),
                    pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
                    pack_bf16x2(acc[6], acc[7]));
@@ -488,7 +491,7 @@ WtEncodeFn wt_encode_fn() {
 // Per device: the kernel's shared-memory attribute and, for every cluster
 // size 1..8, how many clusters can be resident at once (tiles of 128 columns
 // only: the K split is used there alone).
-template <int BITS, int HALVES>
+template <int BITS, int HALVES, int ACT>
 struct WtInit {
   std::atomic<uint64_t> done{0};
   std::mutex mu;
@@ -498,7 +501,7 @@ struct WtInit {
     if (!(done.load(std::memory_order_acquire) & bit)) {
       std::lock_guard<std::mutex> lk(mu);
       if (!(done.load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_wt_kernel<BITS, HALVES>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_wt_kernel<BITS, HALVES, ACT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              WtCfg<BITS, HALVES>::kSmem);
         if (e != cudaSuccess) return e;
@@ -515,7 +518,7 @@ struct WtInit {
           cfg.attrs = &at;
           cfg.numAttrs = 1;
           int n = 0;
-          if (cudaOccupancyMaxActiveClusters(&n, gemm_wt_kernel<BITS, HALVES>, &cfg) != cudaSuccess)
+          if (cudaOccupancyMaxActiveClusters(&n, gemm_wt_kernel<BITS, HALVES, ACT>, &cfg) != cudaSuccess)
             n = 0;
           max_clusters[device & 63][c] = n;
         }
@@ -527,10 +530,10 @@ struct WtInit {
     return cudaSuccess;
   }
 };
-WtInit<4, 1> g_wt4;
-WtInit<8, 1> g_wt8;
-WtInit<4, 2> g_wt4w;
-WtInit<8, 2> g_wt8w;
+// One per kernel variant: bits, tile halves, activation (the fused MLP's
+// up-projection).
+template <int BITS, int HALVES, int ACT>
+WtInit<BITS, HALVES, ACT> g_wt_init;
 
 // K split of a tile over a cluster when the tiles alone leave at least half
 // the SMs idle: the largest split (in whole chunks, at most 8) whose CTAs fit
@@ -545,15 +548,12 @@ int wt_split(int64_t tiles, int nchunks, int num_sms, int hint, const int (&max_
   return best;
 }
 
-template <int BITS, int HALVES>
+template <int BITS, int HALVES, int ACT>
 cudaError_t launch_wt(const GemmArgs& a, cudaStream_t stream, WtEncodeFn enc) {
   using C = WtCfg<BITS, HALVES>;
   constexpr int kTN = C::kTN;
   int max_cl[9];
-  cudaError_t e = BITS == 4 ? (HALVES == 2 ? g_wt4w.ensure(a.device, max_cl)
-                                           : g_wt4.ensure(a.device, max_cl))
-                            : (HALVES == 2 ? g_wt8w.ensure(a.device, max_cl)
-                                           : g_wt8.ensure(a.device, max_cl));
+  cudaError_t e = g_wt_init<BITS, HALVES, ACT>.ensure(a.device, max_cl);
   if (e != cudaSuccess) return e;
 
   // X as a 3-D bf16 tensor [K/64 blocks][M rows][64]: one box is the two
@@ -624,7 +624,7 @@ cudaError_t launch_wt(const GemmArgs& a, cudaStream_t stream, WtEncodeFn enc) {
   }
   cfg.attrs = attrs;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, gemm_wt_kernel<BITS, HALVES>, tmx, tmw, p);
+  return cudaLaunchKernelEx(&cfg, gemm_wt_kernel<BITS, HALVES, ACT>, tmx, tmw, p);
 }
 
 }  // namespace
@@ -646,8 +646,14 @@ cudaError_t launch_gemm_wt(const GemmArgs& a, cudaStream_t stream) {
   WtEncodeFn enc = wt_encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   const bool wide = a.M >= kWideMinM;
-  if (a.bits == 4) return wide ? launch_wt<4, 2>(a, stream, enc) : launch_wt<4, 1>(a, stream, enc);
-  return wide ? launch_wt<8, 2>(a, stream, enc) : launch_wt<8, 1>(a, stream, enc);
+  if (a.act != 0) {
+    if (a.bits == 4)
+      return wide ? launch_wt<4, 2, 1>(a, stream, enc) : launch_wt<4, 1, 1>(a, stream, enc);
+    return wide ? launch_wt<8, 2, 1>(a, stream, enc) : launch_wt<8, 1, 1>(a, stream, enc);
+  }
+  if (a.bits == 4)
+    return wide ? launch_wt<4, 2, 0>(a, stream, enc) : launch_wt<4, 1, 0>(a, stream, enc);
+  return wide ? launch_wt<8, 2, 0>(a, stream, enc) : launch_wt<8, 1, 0>(a, stream, enc);
 }
 
 }  // namespace wq

@@ -28,6 +28,8 @@ cudaError_t launch_import_nk(const uint32_t* qweight, const uint16_t* scales_nk,
                              cudaStream_t stream);
 cudaError_t launch_dequantize(const uint32_t* packed, const uint16_t* scales, int bits,
                               int64_t K, int64_t N, uint16_t* W, cudaStream_t stream);
+// H[i] = bf16(silu(H[i])) for n bf16 values (wq_pack.cu).
+cudaError_t launch_silu_inplace(uint16_t* H, int64_t n, cudaStream_t stream);
 
 // Small-M split-K GEMM (wq_gemm_small.cu).
 struct GemmArgs {
@@ -41,6 +43,9 @@ struct GemmArgs {
   int device;
   int pdl;          // launch with programmatic stream serialization
   int split_hint;   // 0 = automatic cluster split
+  int act;          // 0: none; 1: Y = bf16(silu(bf16(X . W))) (small and wt kernels only)
+  const void* l2_prefetch;    // small kernel: bytes to pull into L2 once its weights have
+  int64_t l2_prefetch_bytes;  // landed (the next GEMM's weights); 16-byte aligned and sized
   DiagHost diag;
 };
 // Returns cudaErrorNotSupported when the shape does not fit this kernel.

@@ -12,6 +12,7 @@
 // writes the cell's 4 KiB (INT4) / 8 KiB (INT8) of words contiguously.
 #include <cuda_bf16.h>
 
+#include "wq_device.cuh"
 #include "wq_internal.h"
 
 namespace wq {
@@ -308,6 +309,29 @@ cudaError_t launch_dequantize(const uint32_t* packed, const uint16_t* scales, in
     dequantize_kernel<4><<<grid, kPackThreads, 0, stream>>>(packed, scales, K, N, out);
   else
     dequantize_kernel<8><<<grid, kPackThreads, 0, stream>>>(packed, scales, K, N, out);
+  return cudaGetLastError();
+}
+
+namespace {
+// One bf16 pair per thread iteration (n is even for every caller: N % 64 == 0).
+__global__ void silu_inplace_kernel(uint32_t* h2, int64_t npairs) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < npairs;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint32_t w = h2[i];
+    const float lo = apply_act(__uint_as_float(w << 16), 1);
+    const float hi = apply_act(__uint_as_float(w & 0xFFFF0000u), 1);
+    h2[i] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+            (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+  }
+}
+}  // namespace
+
+cudaError_t launch_silu_inplace(uint16_t* H, int64_t n, cudaStream_t stream) {
+  const int64_t npairs = n / 2;
+  if (npairs == 0) return cudaSuccess;
+  const int64_t blocks = (npairs + 255) / 256;
+  silu_inplace_kernel<<<static_cast<unsigned>(blocks < 1184 ? blocks : 1184), 256, 0, stream>>>(
+      reinterpret_cast<uint32_t*>(H), npairs);
   return cudaGetLastError();
 }
 
