@@ -68,6 +68,7 @@ def _bind(lib):
     lib.wqo_round_bf16.argtypes = [P, I64, P]
     lib.wqo_round_bf16_f64.argtypes = [P, I64, P]
     lib.wqo_silu_bf16.argtypes = [P, I64, P]
+    lib.wqo_swa_attention.argtypes = [P, P, P, I, I, I, I, I64, I64, P]
     lib.wqo_packed_words.argtypes = [I, I64, I64]
     lib.wqo_packed_words.restype = I64
     lib.wqo_pack.argtypes = [P, I64, I64, I, P]
@@ -280,6 +281,24 @@ def mlp(X_bf16: np.ndarray, packed_up: np.ndarray, s_up: np.ndarray, packed_down
     if act == "silu":
         H = silu_bf16(H)
     return H, gemm(H, packed_down, s_down, N1, N2, bits, rows=rows, nthreads=nthreads)
+
+
+def swa_attention(Q: np.ndarray, K: np.ndarray, V: np.ndarray, T: int, window: int) -> np.ndarray:
+    """The drafter's symmetric sliding-window attention, fp64 [B, Hq, D].
+
+    Q bf16 bits [B, Hq, D]; K, V bf16 bits [Hkv, T, D].  Query b sits at
+    position T - B + b and sees keys j with |j - (T - B + b)| <= window / 2;
+    window 0 or T <= window is full attention."""
+    Q = np.ascontiguousarray(Q, dtype=np.uint16)
+    K = np.ascontiguousarray(K, dtype=np.uint16)
+    V = np.ascontiguousarray(V, dtype=np.uint16)
+    B, Hq, D = Q.shape
+    Hkv = K.shape[0]
+    if K.shape != (Hkv, T, D) or V.shape != (Hkv, T, D) or Hq % Hkv != 0 or B > T:
+        raise ValueError("shape mismatch")
+    O = np.zeros((B, Hq, D), dtype=np.float64)
+    _load().wqo_swa_attention(_ptr(Q), _ptr(K), _ptr(V), B, Hq, Hkv, D, T, window, _ptr(O))
+    return O
 
 
 def tolerance(Y_ref: np.ndarray) -> float:

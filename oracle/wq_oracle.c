@@ -325,3 +325,54 @@ int wqo_gemm_rows(const uint16_t* X, const uint32_t* packed, const uint16_t* s,
   free(What);
   return 0;
 }
+
+/* ------------------------------------------ drafter attention (SWA) -- */
+
+/* The drafter's attention ("Quantize the Target, Quantize the Drafter",
+   drafter-SWA paragraph): a block of B query tokens, the last B positions
+   p_b = T - B + b of a sequence of T tokens whose keys and values are all
+   cached (the cache is kept whole), attends bidirectionally with a window
+   symmetric around each query: query b sees key j iff |j - p_b| <= W / 2.
+   W == 0, or a sequence no longer than the window (T <= W), is full
+   attention.  Q [B][Hq][D], K and V [Hkv][T][D], all bf16; query head h
+   reads key/value head h / (Hq / Hkv).  Scores q.k / sqrt(D), a softmax
+   over the visible keys and the weighted sum of values, all in fp64.
+   O [B][Hq][D] fp64. */
+void wqo_swa_attention(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int B, int Hq,
+                       int Hkv, int D, int64_t T, int64_t W, double* O) {
+  const int group = Hq / Hkv;
+  const int full = (W == 0 || T <= W);
+  double* score = (double*)malloc((size_t)T * sizeof(double));
+  if (!score) return;
+  for (int b = 0; b < B; ++b) {
+    const int64_t p = T - B + b;
+    const int64_t lo = full ? 0 : (p - W / 2 < 0 ? 0 : p - W / 2);
+    const int64_t hi = full ? T - 1 : (p + W / 2 > T - 1 ? T - 1 : p + W / 2);
+    for (int h = 0; h < Hq; ++h) {
+      const int kv = h / group;
+      const uint16_t* q = Q + ((int64_t)b * Hq + h) * D;
+      double mx = -INFINITY;
+      for (int64_t j = lo; j <= hi; ++j) {
+        const uint16_t* k = K + ((int64_t)kv * T + j) * D;
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d) acc += (double)bf16_to_f32(q[d]) * (double)bf16_to_f32(k[d]);
+        score[j] = acc / sqrt((double)D);
+        if (score[j] > mx) mx = score[j];
+      }
+      double den = 0.0;
+      for (int64_t j = lo; j <= hi; ++j) {
+        score[j] = exp(score[j] - mx);
+        den += score[j];
+      }
+      double* o = O + ((int64_t)b * Hq + h) * D;
+      for (int d = 0; d < D; ++d) o[d] = 0.0;
+      for (int64_t j = lo; j <= hi; ++j) {
+        const uint16_t* v = V + ((int64_t)kv * T + j) * D;
+        for (int d = 0; d < D; ++d) o[d] += score[j] * (double)bf16_to_f32(v[d]);
+      }
+      for (int d = 0; d < D; ++d) o[d] /= den;
+    }
+  }
+  free(score);
+}
+

@@ -415,3 +415,87 @@ def test_mlp_one_hot_rows_bruteforce(bits, act):
     assert np.array_equal(H, Hk)
     Yk = oracle.bf16_bits_to_f32(Hk).astype(np.float64) @ oracle.dequant(qd, sd).astype(np.float64)
     assert np.allclose(Y, Yk, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------ drafter attention (SWA) ---
+def _bf16(a) -> np.ndarray:
+    return oracle.f32_to_bf16_bits(np.asarray(a, dtype=np.float32))
+
+
+@pytest.mark.parametrize("T,W,B", [(200, 64, 16), (200, 2, 4), (100, 128, 16), (200, 0, 16),
+                                   (40, 38, 16), (17, 16, 16)])
+def test_swa_window_bounds_by_uniform_scores(T, W, B):
+    """Equal keys make every visible score equal, so the output is the mean
+    of the visible values; with value j at key j that mean is
+    (lo + hi) / 2, lo = max(0, p - W/2), hi = min(T - 1, p + W/2), p = T - B
+    + b, and the whole sequence when W = 0 or T <= W."""
+    Hq, Hkv, D = 2, 1, 128
+    rng = np.random.default_rng(T + W)
+    Q = _bf16(rng.normal(size=(B, Hq, D)))
+    K = _bf16(np.broadcast_to(rng.normal(size=(1, 1, D)), (Hkv, T, D)))
+    V = _bf16(np.broadcast_to(np.arange(T, dtype=np.float32)[None, :, None], (Hkv, T, D)))
+    O = oracle.swa_attention(Q, K, V, T, W)
+    for b in range(B):
+        p = T - B + b
+        if W == 0 or T <= W:
+            lo, hi = 0, T - 1
+        else:
+            lo, hi = max(0, p - W // 2), min(T - 1, p + W // 2)
+        assert np.allclose(O[b], (lo + hi) / 2, rtol=0, atol=1e-9), (b, lo, hi)
+
+
+def test_swa_grouped_heads_read_their_kv_head():
+    """Query head h reads key/value head h / (Hq / Hkv): with a constant
+    value per key/value head the output names the head."""
+    B, Hq, Hkv, D, T = 16, 8, 2, 128, 64
+    rng = np.random.default_rng(3)
+    Q = _bf16(rng.normal(size=(B, Hq, D)))
+    K = _bf16(rng.normal(size=(Hkv, T, D)))
+    V = _bf16(np.broadcast_to((np.arange(Hkv, dtype=np.float32) + 1)[:, None, None], (Hkv, T, D)))
+    O = oracle.swa_attention(Q, K, V, T, 32)
+    for h in range(Hq):
+        assert np.allclose(O[:, h, :], h // (Hq // Hkv) + 1, rtol=0, atol=1e-12)
+
+
+def test_swa_single_peak_closed_form():
+    """One key aligned with the query: its weight is e^s / (e^s + n - 1)
+    with s = |q|^2 / sqrt(D) and every other visible key scoring 0 (keys
+    orthogonal to q); a key outside the window gets no weight at all."""
+    B, Hq, Hkv, D, T, W = 16, 1, 1, 128, 300, 100
+    Q = np.zeros((B, Hq, D), dtype=np.float32)
+    Q[:, :, 0] = 2.0
+    K = np.zeros((Hkv, T, D), dtype=np.float32)
+    K[:, :, 1] = 1.0                                   # orthogonal to q: score 0
+    jstar = T - B - 10                                 # visible to queries b with p - 50 <= jstar
+    K[0, jstar, 0] = 3.0
+    K[0, 0, 0] = 3.0                                   # outside every window
+    V = np.zeros((Hkv, T, D), dtype=np.float32)
+    V[0, jstar, :] = 1.0
+    V[0, 0, :] = -7.0
+    O = oracle.swa_attention(_bf16(Q), _bf16(K), _bf16(V), T, W)
+    s = 6.0 / np.sqrt(D)
+    for b in range(B):
+        p = T - B + b
+        lo, hi = max(0, p - W // 2), min(T - 1, p + W // 2)
+        n = hi - lo + 1
+        want = np.exp(s) / (np.exp(s) + n - 1) if lo <= jstar <= hi else 0.0
+        assert np.allclose(O[b, 0, :], want, rtol=1e-12, atol=1e-15), b
+
+
+def test_swa_output_is_a_convex_combination_and_permutation_invariant():
+    """The output lies between the smallest and largest visible value, and
+    does not change when the visible keys and values are permuted together."""
+    B, Hq, Hkv, D, T, W = 16, 4, 2, 128, 96, 0
+    rng = np.random.default_rng(9)
+    Q = _bf16(rng.normal(size=(B, Hq, D)))
+    K = _bf16(rng.normal(size=(Hkv, T, D)))
+    V = _bf16(rng.normal(size=(Hkv, T, D)))
+    O = oracle.swa_attention(Q, K, V, T, W)
+    Vf = oracle.bf16_bits_to_f32(V).astype(np.float64)
+    for h in range(Hq):
+        kv = h // (Hq // Hkv)
+        assert np.all(O[:, h, :] <= Vf[kv].max(axis=0) + 1e-12)
+        assert np.all(O[:, h, :] >= Vf[kv].min(axis=0) - 1e-12)
+    perm = rng.permutation(T)
+    O2 = oracle.swa_attention(Q, K[:, perm], V[:, perm], T, W)
+    assert np.allclose(O, O2, rtol=1e-12, atol=1e-12)
