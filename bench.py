@@ -575,9 +575,68 @@ def run_sweep(args):
         torch.cuda.empty_cache()
     if not args.shape and args.only in "c2_mlp_fused":
         sweep_mlp_pair(wq, synth, stream, sh, l2, peak, peak_kind)
+    if not args.shape and args.only in "swa_drafter_attention":
+        for T, W in ((8192, 2048), (8192, 1024), (2048, 4096)):
+            sweep_swa(wq, stream, sh, l2, peak, peak_kind, T, W)
     if wq.wq_last_device_error() != wq.WQ_OK:
         raise RuntimeError("a bounded in-kernel wait ran out during the sweep")
     return 0
+
+
+def sweep_swa(wq, stream, sh, l2, peak, peak_kind, T, W, B=16, Hq=32, Hkv=8, D=128):
+    """The drafter's sliding-window attention: a 16-token block at the end of
+    a T-token cached sequence, 32 query heads over 8 key/value heads of 128;
+    bytes are Q, the visible keys and values of every head, and O."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    full = W == 0 or T <= W
+    klo = 0 if full else max(0, T - B - W // 2)
+    nk = T - klo
+    nbytes = 2 * B * Hq * D * 2 + 2 * Hkv * nk * D * 2
+    reps = max(2, math.ceil(2.0 * l2 / (2 * Hkv * nk * D * 2)) + 1)
+    g = torch.Generator(device="cpu").manual_seed(T + W)
+    q = torch.randn((B, Hq, D), generator=g).to(torch.bfloat16).to(dev)
+    k = torch.randn((Hkv, T, D), generator=g).to(torch.bfloat16).to(dev)
+    v = torch.randn((Hkv, T, D), generator=g).to(torch.bfloat16).to(dev)
+    bufs = [(q.clone(), k.clone(), v.clone(), torch.empty_like(q)) for _ in range(reps)]
+
+    def call(i):
+        qb, kb, vb, ob = bufs[i % reps]
+        st = wq.wq_swa_attention(qb.data_ptr(), kb.data_ptr(), vb.data_ptr(), ob.data_ptr(), B, Hq,
+                                 Hkv, D, T, W, sh)
+        if st != 0:
+            raise RuntimeError(wq.status_string(st))
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            call(i)
+    stream.synchronize()
+    per_graph = reps * max(1, 200 // reps)
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        for i in range(per_graph):
+            call(i)
+    with torch.cuda.stream(stream):
+        gr.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(5):
+            gr.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / (5 * per_graph)
+    gbs = nbytes / us / 1e3
+    print(json.dumps({
+        "case": f"swa_drafter_attention_b{B}_hq{Hq}_hkv{Hkv}_d{D}_t{T}_w{W}", "B": B, "Hq": Hq,
+        "Hkv": Hkv, "D": D, "T": T, "window": W, "visible_keys": nk, "us": us, "GB/s": gbs,
+        "hbm_frac": gbs / peak, "peak_source": peak_kind, "bytes": nbytes,
+        "rotation": reps}), flush=True)
+    del gr, bufs
+    torch.cuda.empty_cache()
 
 
 def sweep_mlp_pair(wq, synth, stream, sh, l2, peak, peak_kind):

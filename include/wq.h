@@ -187,6 +187,28 @@ WQ_API wq_status wq_mlp_w4a16(const void* X, const uint32_t* Wu, const void* Su,
                               const uint32_t* Wd, const void* Sd, void* H, void* Y,
                               int64_t M, int64_t K, int64_t N1, int64_t N2, int group,
                               int act, cudaStream_t stream);
+/*
+ * The drafter's attention with a symmetric sliding window ("Quantize the
+ * Target, Quantize the Drafter", drafter-SWA paragraph): a block of B
+ * query tokens (1..16: the anchor and the drafted tokens) at positions
+ * p_b = T - B + b, the last B of a sequence of T tokens whose keys and values
+ * are all cached, attends bidirectionally; query b sees key j iff
+ * |j - p_b| <= window / 2.  window == 0, or T <= window (a sequence the
+ * window covers), is full attention.  Scores q.k / sqrt(128), softmax over
+ * the visible keys, weighted sum of the values (fp32 accumulation, output
+ * rounded to bf16).
+ *   Q [B][Hq][128], K and V [Hkv][T][128], O [B][Hq][128], all bf16,
+ *   row-major and contiguous, 16-byte aligned, caller-owned device memory;
+ *   query head h reads key/value head h / (Hq / Hkv).
+ * Errors: WQ_ERR_NULL, WQ_ERR_UNSUPPORTED (head dim other than 128),
+ * WQ_ERR_SHAPE (B outside 1..16, Hq not a multiple of Hkv, T < B,
+ * window < 0), WQ_ERR_ALIGN, WQ_ERR_CUDA, and WQ_ERR_DEVICE_TIMEOUT through
+ * wq_last_device_error().  Stream-ordered; allocates nothing.
+ */
+WQ_API wq_status wq_swa_attention(const void* Q, const void* K, const void* V, void* O,
+                                  int64_t B, int64_t Hq, int64_t Hkv, int64_t D, int64_t T,
+                                  int64_t window, cudaStream_t stream);
+
 WQ_API wq_status wq_mlp_w8a16(const void* X, const uint32_t* Wu, const void* Su,
                               const uint32_t* Wd, const void* Sd, void* H, void* Y,
                               int64_t M, int64_t K, int64_t N1, int64_t N2, int group,

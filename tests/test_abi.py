@@ -81,6 +81,16 @@ def test_argument_errors_without_gpu(wq):
     assert mlp(A, A, A, A, A, A + 8, A, 16, 128, 128, 64, 128, 0, s) == wq.WQ_ERR_ALIGN
     assert wq.wq_mlp_w8a16(A, A, A, A, A, A, A, 16, 128, 128, 64, 64, 0, s) == wq.WQ_ERR_SHAPE
     assert mlp(A, A, A, A, A, A, A, 0, 128, 128, 64, 128, 1, s) == wq.WQ_OK
+    # sliding-window attention: Q, K, V, O, B, Hq, Hkv, D, T, window, stream
+    swa = wq.wq_swa_attention
+    assert swa(None, A, A, A, 16, 32, 8, 128, 4096, 2048, s) == wq.WQ_ERR_NULL
+    assert swa(A, A, A, A, 16, 32, 8, 64, 4096, 2048, s) == wq.WQ_ERR_UNSUPPORTED
+    assert swa(A, A, A, A, 17, 32, 8, 128, 4096, 2048, s) == wq.WQ_ERR_SHAPE
+    assert swa(A, A, A, A, 16, 30, 8, 128, 4096, 2048, s) == wq.WQ_ERR_SHAPE
+    assert swa(A, A, A, A, 16, 32, 8, 128, 8, 2048, s) == wq.WQ_ERR_SHAPE
+    assert swa(A, A, A, A, 16, 32, 8, 128, 4096, -2, s) == wq.WQ_ERR_SHAPE
+    assert swa(A, A, A + 4, A, 16, 32, 8, 128, 4096, 2048, s) == wq.WQ_ERR_ALIGN
+    assert swa(A, A, A, A, 0, 32, 8, 128, 4096, 2048, s) == wq.WQ_OK
 
 
 def test_status_strings(wq):

@@ -38,7 +38,8 @@ GROUP = 128
 EXPORTED = (
     "wq_packed_words", "wq_pack_symmetric", "wq_pack_codes", "wq_unpack", "wq_dequantize",
     "wq_import_packed_nk",
-    "wq_gemm_w4a16", "wq_gemm_w8a16", "wq_mlp_w4a16", "wq_mlp_w8a16", "wq_last_device_error",
+    "wq_gemm_w4a16", "wq_gemm_w8a16", "wq_mlp_w4a16", "wq_mlp_w8a16", "wq_swa_attention",
+    "wq_last_device_error",
     "wq_clear_device_error", "wq_status_string", "wq_debug_set_wait_limit_ns",
     "wq_debug_force_timeout", "wq_gemm_regime", "wq_debug_set_split",
     "wq_set_programmatic_launch", "wq_last_cuda_error", "wq_debug_force_regime",
@@ -72,6 +73,7 @@ def _load() -> ctypes.CDLL:
         "wq_gemm_w8a16": ([P, P, P, P, I64, I64, I64, I, P], I),
         "wq_mlp_w4a16": ([P, P, P, P, P, P, P, I64, I64, I64, I64, I, I, P], I),
         "wq_mlp_w8a16": ([P, P, P, P, P, P, P, I64, I64, I64, I64, I, I, P], I),
+        "wq_swa_attention": ([P, P, P, P, I64, I64, I64, I64, I64, I64, P], I),
         "wq_last_device_error": ([], I),
         "wq_clear_device_error": ([], I),
         "wq_status_string": ([I], ctypes.c_char_p),
@@ -318,3 +320,24 @@ def mlp(X: torch.Tensor, Wu: torch.Tensor, Su: torch.Tensor, Wd: torch.Tensor,
     _check(fn(_ptr(X), _ptr(Wu), _ptr(Su), _ptr(Wd), _ptr(Sd), _ptr(H), _ptr(Y), M, K, N1, N2,
               GROUP, _ACTS[act], _stream(stream)), name)
     return H, Y
+
+
+def wq_swa_attention(Q, K, V, O, B, Hq, Hkv, D, T, window, stream) -> int:
+    return _lib.wq_swa_attention(Q, K, V, O, B, Hq, Hkv, D, T, window, stream)
+
+
+def swa_attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, window: int,
+                  O: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The drafter's symmetric sliding-window attention.  Q [B, Hq, 128],
+    K and V [Hkv, T, 128] (bf16); query b sits at position T - B + b and
+    sees keys within window // 2 of it (window 0: all keys).  Returns
+    O [B, Hq, 128]."""
+    if Q.dtype != torch.bfloat16 or K.dtype != torch.bfloat16 or V.dtype != torch.bfloat16:
+        raise ValueError("Q, K and V must be bfloat16")
+    B, Hq, D = Q.shape
+    Hkv, T, _ = K.shape
+    if O is None:
+        O = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=Q.device)
+    _check(wq_swa_attention(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), B, Hq, Hkv, D, T, window,
+                            _stream(stream)), "wq_swa_attention")
+    return O

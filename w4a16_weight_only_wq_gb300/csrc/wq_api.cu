@@ -313,6 +313,37 @@ wq_status wq_gemm_w8a16(const void* X, const uint32_t* Wp, const void* scales,
   return gemm_common(8, X, Wp, scales, Y, M, N, K, group, stream);
 }
 
+wq_status wq_swa_attention(const void* Q, const void* K, const void* V, void* O, int64_t B,
+                           int64_t Hq, int64_t Hkv, int64_t D, int64_t T, int64_t window,
+                           cudaStream_t stream) {
+  if (B == 0) return WQ_OK;
+  if (!Q || !K || !V || !O) return WQ_ERR_NULL;
+  if (D != 128) return WQ_ERR_UNSUPPORTED;
+  if (B < 1 || B > 16 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Hq > 4096 || T < B ||
+      T > (int64_t(1) << 31) || window < 0 || Hkv * T * D >= (int64_t(1) << 40))
+    return WQ_ERR_SHAPE;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return WQ_ERR_ALIGN;
+  int dev;
+  DeviceInfo d;
+  wq_status st = device_info(&dev, &d);
+  if (st != WQ_OK) return st;
+  wq::SwaArgs a;
+  a.Q = Q;
+  a.K = K;
+  a.V = V;
+  a.O = O;
+  a.B = static_cast<int>(B);
+  a.Hq = static_cast<int>(Hq);
+  a.Hkv = static_cast<int>(Hkv);
+  a.T = T;
+  a.window = window;
+  a.num_sms = d.num_sms;
+  a.device = dev;
+  a.split_hint = g_split_hint.load();
+  a.diag = diag_for(d);
+  return cuda_status(wq::launch_swa_attention(a, stream));
+}
+
 wq_status wq_mlp_w4a16(const void* X, const uint32_t* Wu, const void* Su, const uint32_t* Wd,
                        const void* Sd, void* H, void* Y, int64_t M, int64_t K, int64_t N1,
                        int64_t N2, int group, int act, cudaStream_t stream) {

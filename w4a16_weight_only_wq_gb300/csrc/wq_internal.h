@@ -66,4 +66,20 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t stream);
 cudaError_t launch_gemm_wt(const GemmArgs& a, cudaStream_t stream);
 bool gemm_wt_fits(int bits, int64_t M, int64_t K, int64_t N);
 
+// The drafter's sliding-window attention (wq_swa.cu).  Q, O [B][Hq][128],
+// K, V [Hkv][T][128], bf16; arguments checked by the caller.
+struct SwaArgs {
+  const void* Q;
+  const void* K;
+  const void* V;
+  void* O;
+  int B, Hq, Hkv;
+  int64_t T, window;
+  int num_sms;
+  int device;
+  int split_hint;   // 0 = automatic number of key slices per head
+  DiagHost diag;
+};
+cudaError_t launch_swa_attention(const SwaArgs& a, cudaStream_t stream);
+
 }  // namespace wq
