@@ -575,9 +575,10 @@ def run_sweep(args):
         torch.cuda.empty_cache()
     if not args.shape and args.only in "c2_mlp_fused":
         sweep_mlp_pair(wq, synth, stream, sh, l2, peak, peak_kind)
-    if not args.shape and args.only in "swa_drafter_attention":
+    if not args.shape:
         for T, W in ((8192, 2048), (8192, 1024), (2048, 4096)):
-            sweep_swa(wq, stream, sh, l2, peak, peak_kind, T, W)
+            if args.only in f"swa_drafter_attention_b16_hq32_hkv8_d128_t{T}_w{W}":
+                sweep_swa(wq, stream, sh, l2, peak, peak_kind, T, W)
     if wq.wq_last_device_error() != wq.WQ_OK:
         raise RuntimeError("a bounded in-kernel wait ran out during the sweep")
     return 0
