@@ -83,3 +83,31 @@ def test_abandoned_data_wait_drains_and_recovers(wq, small, bits):
     assert wq.wq_last_device_error() == wq.WQ_OK
     Yref = oracle.gemm(X, oracle.pack(q, bits), s, K, N, bits)
     assert_close_to_oracle(Y, Yref, "after an abandoned wait")
+
+
+def test_attention_abandoned_wait_reports_and_recovers(wq):
+    """The merge wait of the sliding-window attention looks at a barrier that
+    never completes: the kernel gives up, lets the partials land, reports
+    the timeout, and a normal call afterwards is correct."""
+    B, Hq, Hkv, T, W = 16, 8, 2, 700, 256
+    rng = np.random.default_rng(21)
+    Q = oracle.f32_to_bf16_bits(rng.normal(size=(B, Hq, 128)).astype(np.float32))
+    K = oracle.f32_to_bf16_bits(rng.normal(size=(Hkv, T, 128)).astype(np.float32))
+    V = oracle.f32_to_bf16_bits(rng.normal(size=(Hkv, T, 128)).astype(np.float32))
+    Qt, Kt, Vt = bf16_to_dev(Q), bf16_to_dev(K), bf16_to_dev(V)
+    torch.cuda.synchronize()
+    assert wq.wq_clear_device_error() == wq.WQ_OK
+    try:
+        wq.wq_debug_set_wait_limit_ns(1_000_000)  # 1 ms
+        wq.wq_debug_force_timeout(2)
+        wq.swa_attention(Qt, Kt, Vt, W)
+        torch.cuda.synchronize()
+    finally:
+        wq.wq_debug_force_timeout(0)
+        wq.wq_debug_set_wait_limit_ns(0)
+    assert wq.wq_last_device_error() == wq.WQ_ERR_DEVICE_TIMEOUT
+    assert wq.wq_clear_device_error() == wq.WQ_OK
+    O = wq.swa_attention(Qt, Kt, Vt, W)
+    torch.cuda.synchronize()
+    assert wq.wq_last_device_error() == wq.WQ_OK
+    assert_close_to_oracle(O, oracle.swa_attention(Q, K, V, T, W), "after an abandoned wait")

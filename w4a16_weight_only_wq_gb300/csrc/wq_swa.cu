@@ -49,7 +49,7 @@ constexpr int kORow = kD + 4;                        // fp32 rows of 132: confli
 constexpr int kOffO = kOffW + kWarps * 2 * kRows * 4;  // the CTA's values [16][132] fp32
 constexpr int kOffRecv = kOffO + kRows * kORow * 4;  // rank 0: [S][kPartFloats]
 constexpr int kOffBar = kOffRecv + kMaxCluster * kPartFloats * 4;
-constexpr int kSmem = kOffBar + 16;  // the barrier, then rank 0's "bytes arrived" flag
+constexpr int kSmem = kOffBar + 24;  // two barriers, then rank 0's "bytes arrived" flag
 constexpr float kScale = 0.0883883476483184405f;     // 1 / sqrt(128)
 
 struct SwaParams {
@@ -86,10 +86,12 @@ __global__ void __launch_bounds__(kThreads, 1) swa_attention_kernel(const SwaPar
   const int64_t c0 = klo + nk * rank / S, c1 = klo + nk * (rank + 1) / S;
   const int nchunks = static_cast<int>((c1 - c0 + kChunk - 1) / kChunk);
   uint64_t* recv_bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* never_bar = recv_bar + 1;  // test hook: a barrier nothing completes
   const uint32_t sbase = smem_addr(smem);
 
   if (threadIdx.x == 0) {
     mbar_init(recv_bar, 1);
+    mbar_init(never_bar, 1);
     fence_mbar_init();
     if (rank == 0) mbar_arrive_expect_tx(recv_bar, S * kPartFloats * 4);
   }
@@ -297,8 +299,16 @@ __global__ void __launch_bounds__(kThreads, 1) swa_attention_kernel(const SwaPar
   if (rank != 0) return;
 
   // ---- rank 0: merge the S partials in rank order and write O
-  int* okflag = reinterpret_cast<int*>(smem + kOffBar + 8);
-  if (threadIdx.x == 0) *okflag = mbar_wait_bounded(recv_bar, 0, p.diag) ? 1 : 0;
+  int* okflag = reinterpret_cast<int*>(smem + kOffBar + 16);
+  if (threadIdx.x == 0) {
+    // Test hook 2: wait on a barrier nothing completes; the wait gives up,
+    // reports the timeout, and the partials are still drained below before
+    // the CTA (whose shared memory they land in) exits, without an output.
+    const bool hooked = p.diag.force_timeout == 2 && !mbar_wait_bounded(never_bar, 0, p.diag);
+    KernelDiag drain = p.diag;
+    if (hooked && drain.wait_limit_ns < 1000000000ull) drain.wait_limit_ns = 1000000000ull;
+    *okflag = mbar_wait_bounded(recv_bar, 0, drain) && !hooked ? 1 : 0;
+  }
   __syncthreads();
   if (*okflag == 0) return;
   const float* rp = reinterpret_cast<const float*>(smem + kOffRecv);
