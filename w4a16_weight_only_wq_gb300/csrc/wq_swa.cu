@@ -50,7 +50,9 @@ constexpr int kOffO = kOffW + kWarps * 2 * kRows * 4;  // the CTA's values [16][
 constexpr int kOffRecv = kOffO + kRows * kORow * 4;  // rank 0: [S][kPartFloats]
 constexpr int kOffBar = kOffRecv + kMaxCluster * kPartFloats * 4;
 constexpr int kSmem = kOffBar + 24;  // two barriers, then rank 0's "bytes arrived" flag
-constexpr float kScale = 0.0883883476483184405f;     // 1 / sqrt(128)
+// scores are kept in base 2: q.k / sqrt(128) * log2(e), so the softmax
+// weights are exp2f of differences (the same weights, a cheaper function)
+constexpr float kScale2 = 0.0883883476483184405f * 1.44269504088896341f;
 
 struct SwaParams {
   const __nv_bfloat16* Q;  // [B][Hq][128]
@@ -168,18 +170,32 @@ __global__ void __launch_bounds__(kThreads, 1) swa_attention_kernel(const SwaPar
         mma_bf16_16816(s[nb], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1, s[nb]);
       }
     }
-    // mask (slice end, window) and scale; running max / sum per row
+    // mask (slice end, window) and scale; running max / sum per row.  A step
+    // whose 16 keys lie in every query's window and before the slice end
+    // needs no mask.
     float mx[2] = {-INFINITY, -INFINITY};
+    const bool interior =
+        kb + 16 <= c1 && (full || (kb >= p0 + p.B - 1 - half && kb + 15 <= p0 + half));
+    if (interior) {
 #pragma unroll
-    for (int nb = 0; nb < 2; ++nb) {
+      for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = g + 8 * (e >> 1);
-        const int jr = static_cast<int>(kb - p0) + 8 * nb + 2 * t4 + (e & 1) - r;  // j - p_r
-        const bool vis = jr + r < static_cast<int>(c1 - p0) &&
-                         (full || r >= p.B || (jr >= -ihalf && jr <= ihalf));
-        s[nb][e] = vis ? s[nb][e] * kScale : -INFINITY;
-        mx[e >> 1] = fmaxf(mx[e >> 1], s[nb][e]);
+        for (int e = 0; e < 4; ++e) {
+          s[nb][e] *= kScale2;
+          mx[e >> 1] = fmaxf(mx[e >> 1], s[nb][e]);
+        }
+    } else {
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = g + 8 * (e >> 1);
+          const int jr = static_cast<int>(kb - p0) + 8 * nb + 2 * t4 + (e & 1) - r;  // j - p_r
+          const bool vis = jr + r < static_cast<int>(c1 - p0) &&
+                           (full || r >= p.B || (jr >= -ihalf && jr <= ihalf));
+          s[nb][e] = vis ? s[nb][e] * kScale2 : -INFINITY;
+          mx[e >> 1] = fmaxf(mx[e >> 1], s[nb][e]);
+        }
       }
     }
     float alpha[2], psum[2] = {0.f, 0.f};
@@ -188,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_attention_kernel(const SwaPar
       mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
       mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
       const float mnew = fmaxf(m_run[i], mx[i]);
-      alpha[i] = mnew == -INFINITY ? 1.f : expf(m_run[i] - mnew);
+      alpha[i] = mnew == -INFINITY ? 1.f : exp2f(m_run[i] - mnew);
       m_run[i] = mnew;
     }
 #pragma unroll
@@ -196,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_attention_kernel(const SwaPar
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = e >> 1;
-        s[nb][e] = m_run[i] == -INFINITY ? 0.f : expf(s[nb][e] - m_run[i]);
+        s[nb][e] = m_run[i] == -INFINITY ? 0.f : exp2f(s[nb][e] - m_run[i]);
         psum[i] += s[nb][e];
       }
     }
@@ -206,12 +222,14 @@ __global__ void __launch_bounds__(kThreads, 1) swa_attention_kernel(const SwaPar
       psum[i] += __shfl_xor_sync(0xffffffffu, psum[i], 2);
       l_run[i] = l_run[i] * alpha[i] + psum[i];
     }
+    if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {  // a row's max moved
 #pragma unroll
-    for (int db = 0; db < 16; ++db) {
-      o[db][0] *= alpha[0];
-      o[db][1] *= alpha[0];
-      o[db][2] *= alpha[1];
-      o[db][3] *= alpha[1];
+      for (int db = 0; db < 16; ++db) {
+        o[db][0] *= alpha[0];
+        o[db][1] *= alpha[0];
+        o[db][2] *= alpha[1];
+        o[db][3] *= alpha[1];
+      }
     }
     // probabilities as the A operand (16 rows x 16 keys)
     const uint32_t pa0 = pack_bf16x2_rn(s[0][0], s[0][1]);
@@ -254,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_attention_kernel(const SwaPar
     const int r = g + 8 * i;
     float M = -INFINITY;
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wml[(w * 2) * kRows + r]);
-    f[i] = (M == -INFINITY || m_run[i] == -INFINITY) ? 0.f : expf(m_run[i] - M);
+    f[i] = (M == -INFINITY || m_run[i] == -INFINITY) ? 0.f : exp2f(m_run[i] - M);
   }
   float* mine = wo + warp * kRows * kORow;
 #pragma unroll
@@ -279,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_attention_kernel(const SwaPar
     for (int w = 0; w < kWarps; ++w) rowmax = fmaxf(rowmax, wml[(w * 2) * kRows + r]);
     for (int w = 0; w < kWarps; ++w) {
       const float mw = wml[(w * 2) * kRows + r];
-      if (mw != -INFINITY) rowsum += wml[(w * 2 + 1) * kRows + r] * expf(mw - rowmax);
+      if (mw != -INFINITY) rowsum += wml[(w * 2 + 1) * kRows + r] * exp2f(mw - rowmax);
     }
   }
   __syncthreads();  // everyone has read wml and written co
@@ -320,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_attention_kernel(const SwaPar
     float L = 0.f;
     for (int q = 0; q < S; ++q) {
       const float mq = rp[q * kPartFloats + r];
-      const float w = mq == -INFINITY ? 0.f : expf(mq - M);
+      const float w = mq == -INFINITY ? 0.f : exp2f(mq - M);
       wts[q * kRows + r] = w;
       L += rp[q * kPartFloats + kRows + r] * w;
     }
