@@ -103,6 +103,7 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
   constexpr int kChunk = C::kChunk;
   constexpr int kGA = C::kGA;
   constexpr int kTN = C::kTN;
+  static_assert(HALVES == 2 || kGA == kXG, "one-accumulator tiles share the A and X slot ring");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
 
@@ -216,7 +217,11 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
         const int slot = gi % kXG;
         int okx = 1;
         if (lane == 0) {
-          if (gi >= kXG) okx = wt_wait(&b_empty[slot], ((gi / kXG) - 1) & 1, p.diag, abort_flag);
+          // with one accumulator half the A and X rings coincide (slot u % 4)
+          // and the MMAs release both with one commit on a_empty
+          if (gi >= kXG)
+            okx = wt_wait(HALVES == 1 ? &a_empty[slot] : &b_empty[slot], ((gi / kXG) - 1) & 1,
+                          p.diag, abort_flag);
           if (okx) {
             mbar_arrive_expect_tx(&b_full[slot], 2 * kXStage);
             tma_load_3d(smem + C::kOffX + slot * 2 * kXStage, &tmx, 0, m0, (g0 + s) * 2,
@@ -263,7 +268,9 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
             break;
           }
           const int xs = u % kXG;
-          if (!wt_wait(&b_full[xs], (u / kXG) & 1, p.diag, abort_flag)) {
+          // HALVES == 1: the dequant warps saw the group's X land before
+          // marking its A slot full, so one wait covers both
+          if (HALVES == 2 && !wt_wait(&b_full[xs], (u / kXG) & 1, p.diag, abort_flag)) {
             ok = false;
             break;
           }
@@ -282,7 +289,7 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
                 umma_bf16_ts(d_tmem, a_tmem + 8 * j, b_desc + 2 * j, idesc, (g | h | j) != 0);
             }
           }
-          umma_commit(&b_empty[xs]);
+          if (HALVES == 2) umma_commit(&b_empty[xs]);
           umma_commit(&a_empty[as]);
         }
         if (ok) umma_commit(&d_full[buf]);
@@ -325,9 +332,12 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
+        // HALVES == 1: the group's X (same slot) has landed too
+        if (HALVES == 1 && !wt_wait(&b_full[aslot], (u / kXG) & 1, p.diag, abort_flag)) ok = false;
         mbar_arrive(&a_full[aslot]);
         mbar_arrive(&q_empty[slot]);
       }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     }
   } else {
     // ------------------------------------------------ epilogue warps ---
