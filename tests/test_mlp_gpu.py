@@ -96,3 +96,20 @@ def test_mlp_empty_and_errors(wq):
     assert H.shape == (0, 128) and Y.shape == (0, 64)
     with pytest.raises(ValueError):
         wq.mlp(X, W, s, Wd, sd, 4, act="gelu")
+
+
+@pytest.mark.parametrize("M", [16, 40])
+def test_mlp_without_activation_equals_two_gemm_calls(wq, M):
+    """With no activation the pair is exactly the two GEMMs: the same kernels
+    run, so H and Y match two wq_gemm_w4a16 calls bit for bit."""
+    K, N1, N2, bits = 1024, 512, 256, 4
+    X, qu, su = synth.small_case(M, K, N1, bits, seed=40 + M)
+    _, qd, sd = synth.small_case(1, N1, N2, bits, seed=41 + M)
+    Xt, sut, sdt = bf16_to_dev(X), bf16_to_dev(su), bf16_to_dev(sd)
+    Wu, Wd = wq.pack_codes(i8_to_dev(qu), bits), wq.pack_codes(i8_to_dev(qd), bits)
+    H, Y = wq.mlp(Xt, Wu, sut, Wd, sdt, bits, act="none")
+    H2 = wq.gemm_w4a16(Xt, Wu, sut)
+    Y2 = wq.gemm_w4a16(H2, Wd, sdt)
+    torch.cuda.synchronize()
+    assert torch.equal(H, H2)
+    assert torch.equal(Y, Y2)
