@@ -86,9 +86,10 @@ def test_abandoned_data_wait_drains_and_recovers(wq, small, bits):
 
 
 def test_attention_abandoned_wait_reports_and_recovers(wq):
-    """The merge wait of the sliding-window attention looks at a barrier that
-    never completes: the kernel gives up, lets the partials land, reports
-    the timeout, and a normal call afterwards is correct."""
+    """The wait for the last key/value chunk and the merge wait of the
+    sliding-window attention look at a barrier that never completes: the
+    kernel gives up, lets its copies and the partials land, reports the
+    timeout, and a normal call afterwards is correct."""
     B, Hq, Hkv, T, W = 16, 8, 2, 700, 256
     rng = np.random.default_rng(21)
     Q = oracle.f32_to_bf16_bits(rng.normal(size=(B, Hq, 128)).astype(np.float32))

@@ -320,7 +320,7 @@ wq_status wq_swa_attention(const void* Q, const void* K, const void* V, void* O,
   if (!Q || !K || !V || !O) return WQ_ERR_NULL;
   if (D != 128) return WQ_ERR_UNSUPPORTED;
   if (B < 1 || B > 16 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Hq > 4096 || T < B ||
-      T > (int64_t(1) << 30) || window < 0 || Hkv * T * D >= (int64_t(1) << 40))
+      T > (int64_t(1) << 30) || window < 0 || Hkv * T > (int64_t(1) << 31) - 256)
     return WQ_ERR_SHAPE;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return WQ_ERR_ALIGN;
   int dev;

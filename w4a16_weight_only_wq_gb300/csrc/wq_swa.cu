@@ -10,12 +10,14 @@
 //  * Work unit: one query head x one contiguous slice of the keys its block
 //    can see.  A thread-block cluster of S CTAs covers the slices of one
 //    head; each CTA keeps a running (max, sum, weighted values) per query row
-//    and sends it to rank 0 of the cluster with 16-byte asynchronous remote
-//    stores counted on rank 0's mbarrier; rank 0 merges the S partial
-//    softmaxes in rank order and writes the output (deterministic).
-//  * Keys in chunks of 128 rows (16 per warp, eight warps), K and V staged
-//    by 16-byte cp.async into rows padded to 272 bytes (conflict-free
-//    fragment loads), double-buffered.  Scores and the weighted sum use mma.sync m16n8k16
+//    and sends each row's partial to the row's owner (rank row % S) with
+//    16-byte asynchronous remote stores counted on the owner's mbarrier;
+//    every owner merges the S partials of its rows in rank order and writes
+//    them (deterministic).
+//  * Keys in chunks of 128 rows (16 per warp, eight warps).  K and V come
+//    by TMA, four copies per chunk (each 64-dimension half of K and of V)
+//    with the 128-byte swizzle, so the fragment loads are conflict-free;
+//    three chunks in flight.  Keys past the slice are masked.  Scores and the weighted sum use mma.sync m16n8k16
 //    (bf16 in, fp32 accumulate); the probabilities are re-packed from the
 //    score accumulators into the A operand of the second MMA, and V is read
 //    transposed with ldmatrix.
@@ -28,6 +30,8 @@
 
 #include "wq_device.cuh"
 #include "wq_internal.h"
+#include "wq_tcgen05.cuh"
+#include "wq_tensor_map.h"
 
 namespace wq {
 namespace {
@@ -37,19 +41,46 @@ constexpr int kRows = 16;               // query rows per CTA (the block, padded
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kChunk = 128;             // keys per chunk, 16 per warp
-constexpr int kNB = 2;                  // chunk buffers in flight
-constexpr int kRow = kD * 2 + 16;       // 272-byte shared-memory rows
+constexpr int kNB = 3;                  // chunk buffers in flight
+constexpr int kRow = kD * 2;            // 256-byte Q rows (pieces permuted)
 constexpr int kMaxCluster = 8;
-constexpr int kPartFloats = 2 * kRows + kRows * kD;  // max[16], sum[16], values[16][128]
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kRows * kRow;          // kNB K chunk buffers
-constexpr int kOffV = kOffK + kNB * kChunk * kRow;   // kNB V chunk buffers
-constexpr int kOffW = kOffV + kNB * kChunk * kRow;   // per-warp max / sum [warps][2][16]
-constexpr int kORow = kD + 4;                        // fp32 rows of 132: conflict-free
+// One row's partial: (max, sum, 0, 0) then the 128 weighted values.
+constexpr int kRowPart = 4 + kD;
+// A K or V chunk buffer: two 64-dimension halves of 128 rows x 128 bytes,
+// each as TMA writes it with the 128-byte swizzle (1024-byte aligned).
+constexpr int kHalfBytes = kChunk * 128;
+constexpr int kChunkBytes = 2 * kHalfBytes;
+constexpr int kOffK = 0;                             // kNB K chunk buffers
+constexpr int kOffV = kOffK + kNB * kChunkBytes;     // kNB V chunk buffers
+constexpr int kOffQ = kOffV + kNB * kChunkBytes;     // Q [16][256 bytes]
+constexpr int kOffW = kOffQ + kRows * kRow;          // per-warp max / sum [warps][2][16]
+constexpr int kORow = kD + 8;                        // fp32 rows of 136: conflict-free 8-byte stores
 constexpr int kOffO = kOffW + kWarps * 2 * kRows * 4;  // the CTA's values [16][132] fp32
-constexpr int kOffRecv = kOffO + kRows * kORow * 4;  // rank 0: [S][kPartFloats]
-constexpr int kOffBar = kOffRecv + kMaxCluster * kPartFloats * 4;
-constexpr int kSmem = kOffBar + 24;  // two barriers, then rank 0's "bytes arrived" flag
+// Owner's receive buffer: [source rank][owned row][kRowPart] for up to
+// ceil(16 / S) owned rows; the largest over S = 1..8 is 7 x 3 rows.
+constexpr int kRecvRows = 21;
+constexpr int kOffRecv = kOffO + kRows * kORow * 4;
+constexpr int kOffBar = kOffRecv + kRecvRows * kRowPart * 4;
+// barriers: receive, test hook, kNB chunks landed; then two int flags
+constexpr int kNumBars = 2 + kNB;
+constexpr int kSmem = kOffBar + kNumBars * 8 + 8 + 1024;  // + alignment slack
+static_assert(kSmem <= 232448, "shared memory of one CTA");
+static_assert(kWarps * kRows * kORow * 4 <= kNB * kChunkBytes, "warp merge fits the K buffers");
+
+// Byte offset of byte `b` (0..255) of row `r` in a K or V chunk buffer: the
+// half b / 128, then the 128-byte row with its 16-byte pieces permuted by
+// r % 8 (the TMA 128-byte swizzle).
+__host__ __device__ constexpr uint32_t kv_off(int r, int b) {
+  return static_cast<uint32_t>((b >> 7) * kHalfBytes + r * 128 +
+                               (((((b & 127) >> 4) ^ (r & 7))) << 4) + (b & 15));
+}
+
+// Byte offset of byte `b` of row `r` in a 256-byte-row buffer whose 16-byte
+// pieces are permuted by r % 8, so that the eight rows a quarter-warp reads
+// at one column fall on distinct banks.
+__host__ __device__ constexpr uint32_t swz(int r, int b) {
+  return static_cast<uint32_t>(r * kRow + ((((b >> 4) ^ (r & 7)) << 4) | (b & 15)));
+}
 // scores are kept in base 2: q.k / sqrt(128) * log2(e), so the softmax
 // weights are exp2f of differences (the same weights, a cheaper function)
 constexpr float kScale2 = 0.0883883476483184405f * 1.44269504088896341f;
@@ -71,8 +102,13 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, u
                : "r"(addr));
 }
 
-__global__ void __launch_bounds__(kThreads, 1) swa_attention_kernel(const SwaParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];
+__global__ void __launch_bounds__(kThreads, 1)
+swa_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                     const SwaParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  // the swizzled TMA buffers want 1024-byte alignment; every CTA of the
+  // cluster gets the same offset, so remote addresses match
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int S = p.S;
@@ -89,43 +125,51 @@ __global__ void __launch_bounds__(kThreads, 1) swa_attention_kernel(const SwaPar
   const int nchunks = static_cast<int>((c1 - c0 + kChunk - 1) / kChunk);
   uint64_t* recv_bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* never_bar = recv_bar + 1;  // test hook: a barrier nothing completes
+  uint64_t* chunk_full = never_bar + 1;  // [kNB] a chunk's K and V landed
+  int* okflag = reinterpret_cast<int*>(chunk_full + kNB);  // rank's partials arrived
+  int* loadok = okflag + 1;                                  // the current chunk landed
   const uint32_t sbase = smem_addr(smem);
 
   if (threadIdx.x == 0) {
+    prefetch_tensor_map(&tmk);
+    prefetch_tensor_map(&tmv);
     mbar_init(recv_bar, 1);
     mbar_init(never_bar, 1);
+    for (int i = 0; i < kNB; ++i) mbar_init(&chunk_full[i], 1);
     fence_mbar_init();
-    if (rank == 0) mbar_arrive_expect_tx(recv_bar, S * kPartFloats * 4);
+    // this CTA owns rows rank, rank + S, ...: S partials of each arrive here
+    const int owned = (kRows - rank + S - 1) / S;
+    mbar_arrive_expect_tx(recv_bar, S * owned * kRowPart * 4);
   }
   __syncthreads();
   cluster_arrive_relaxed();  // every CTA's barrier is initialised before any remote store
 
-  // ---- staging: Q once, then K / V chunks (rows past the slice read as 0)
+  // ---- staging: K / V chunks by TMA (thread 0), Q by cp.async.  A chunk
+  // covers key rows kv * T + j0 .. + 127 of the [Hkv * T][128] view; rows
+  // past the slice are real keys of the cache (or zeros past its end) and
+  // are masked below.
+  auto load_chunk = [&](int c) {
+    const int buf = c % kNB;
+    const int y = static_cast<int>(static_cast<int64_t>(kv) * T + c0 + static_cast<int64_t>(c) * kChunk);
+    uint8_t* kb = smem + kOffK + buf * kChunkBytes;
+    uint8_t* vb = smem + kOffV + buf * kChunkBytes;
+    mbar_arrive_expect_tx(&chunk_full[buf], 2 * kChunkBytes);
+    tma_load_2d(kb, &tmk, 0, y, &chunk_full[buf]);
+    tma_load_2d(kb + kHalfBytes, &tmk, 64, y, &chunk_full[buf]);
+    tma_load_2d(vb, &tmv, 0, y, &chunk_full[buf]);
+    tma_load_2d(vb + kHalfBytes, &tmv, 64, y, &chunk_full[buf]);
+  };
+  const int first = nchunks < kNB ? nchunks : kNB;
+  if (threadIdx.x == 0)
+    for (int c = 0; c < first; ++c) load_chunk(c);
+  int issued = first;  // thread 0's count of chunks whose copies were issued
   for (int i = threadIdx.x; i < kRows * 16; i += kThreads) {
     const int r = i >> 4, piece = i & 15;
     const bool live = r < p.B;
     const __nv_bfloat16* src = live ? p.Q + (static_cast<int64_t>(r) * p.Hq + h) * kD + piece * 8 : p.Q;
-    cp_async_16(sbase + kOffQ + r * kRow + piece * 16, src, live ? 16u : 0u);
+    cp_async_16(sbase + kOffQ + swz(r, piece * 16), src, live ? 16u : 0u);
   }
-  auto load_chunk = [&](int c) {
-    const int buf = c % kNB;
-    const int64_t j0 = c0 + static_cast<int64_t>(c) * kChunk;
-    for (int i = threadIdx.x; i < kChunk * 16; i += kThreads) {
-      const int r = i >> 4, piece = i & 15;
-      const int64_t j = j0 + r;
-      const bool live = j < c1;
-      const int64_t off = live ? (static_cast<int64_t>(kv) * T + j) * kD + piece * 8 : 0;
-      cp_async_16(sbase + kOffK + (buf * kChunk + r) * kRow + piece * 16, p.K + off, live ? 16u : 0u);
-      cp_async_16(sbase + kOffV + (buf * kChunk + r) * kRow + piece * 16, p.V + off, live ? 16u : 0u);
-    }
-  };
-  // chunk c is cp.async group c (Q travels with chunk 0); up to kNB ahead
-  const int first = nchunks < kNB ? nchunks : kNB;
-  for (int c = 0; c < first; ++c) {
-    load_chunk(c);
-    cp_async_commit();
-  }
-  if (first == 0) cp_async_commit();
+  cp_async_commit();
 
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
   float o[16][4];
@@ -135,130 +179,163 @@ __global__ void __launch_bounds__(kThreads, 1) swa_attention_kernel(const SwaPar
     for (int e = 0; e < 4; ++e) o[db][e] = 0.f;
   uint32_t qa[8][4];
 
+  cp_async_wait_group<0>();  // Q
+  bool loaded = true;
   for (int c = 0; c < nchunks; ++c) {
-    // groups committed after chunk c's: min(kNB - 1, nchunks - 1 - c)
-    const int later = nchunks - 1 - c < kNB - 1 ? nchunks - 1 - c : kNB - 1;
-    if (later >= 3) cp_async_wait_group<3>();
-    else if (later == 2) cp_async_wait_group<2>();
-    else if (later == 1) cp_async_wait_group<1>();
-    else cp_async_wait_group<0>();
+    const int buf = c % kNB;
+    // Thread 0 waits (bounded) and tells the others, so that all threads
+    // leave the loop together if the wait gives up.
+    if (threadIdx.x == 0) {
+      // test hook 2: the last chunk's wait looks for a phase that never completes
+      const bool hook = p.diag.force_timeout == 2 && c == nchunks - 1;
+      *loadok = mbar_wait_bounded(hook ? never_bar : &chunk_full[buf], hook ? 0u : (c / kNB) & 1,
+                                  p.diag)
+                    ? 1
+                    : 0;
+    }
     __syncthreads();
+    if (*loadok == 0) {
+      loaded = false;
+      break;
+    }
+    // completes at once: makes the landed bytes visible to this thread
+    mbar_wait_bounded(&chunk_full[buf], (c / kNB) & 1, p.diag);
     if (c == 0) {
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t a = sbase + kOffQ + g * kRow + (16 * ks + 2 * t4) * 2;
-        qa[ks][0] = ld_shared_u32(a);
-        qa[ks][1] = ld_shared_u32(a + 8 * kRow);
-        qa[ks][2] = ld_shared_u32(a + 16);
-        qa[ks][3] = ld_shared_u32(a + 8 * kRow + 16);
+        const int b = 32 * ks + 4 * t4;
+        qa[ks][0] = ld_shared_u32(sbase + kOffQ + swz(g, b));
+        qa[ks][1] = ld_shared_u32(sbase + kOffQ + swz(g + 8, b));
+        qa[ks][2] = ld_shared_u32(sbase + kOffQ + swz(g, b + 16));
+        qa[ks][3] = ld_shared_u32(sbase + kOffQ + swz(g + 8, b + 16));
       }
     }
-    const int buf = c % kNB;
-    const int rb = buf * kChunk + 16 * warp;  // this warp's first row in the buffers
+    const uint32_t kbase = sbase + kOffK + buf * kChunkBytes;
+    const uint32_t vbase = sbase + kOffV + buf * kChunkBytes;
+    const int rb = 16 * warp;  // this warp's first row in the chunk
     const int64_t kb = c0 + static_cast<int64_t>(c) * kChunk + 16 * warp;  // its first key
-    // scores s[nb]: rows g / g + 8, keys kb + 8 nb + 2 t4 + {0, 1}
-    float s[2][4];
+    // a warp whose 16 keys all lie past the slice end has nothing to add
+    if (kb < c1) {
+      // scores s[nb]: rows g / g + 8, keys kb + 8 nb + 2 t4 + {0, 1}
+      float s[2][4];
 #pragma unroll
-    for (int nb = 0; nb < 2; ++nb) {
+      for (int nb = 0; nb < 2; ++nb) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[nb][e] = 0.f;
-      const uint32_t kaddr = sbase + kOffK + (rb + 8 * nb + g) * kRow + 4 * t4;
+        for (int e = 0; e < 4; ++e) s[nb][e] = 0.f;
+        const int kr = rb + 8 * nb + g;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t b0 = ld_shared_u32(kaddr + 32 * ks);
-        const uint32_t b1 = ld_shared_u32(kaddr + 32 * ks + 16);
-        mma_bf16_16816(s[nb], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1, s[nb]);
-      }
-    }
-    // mask (slice end, window) and scale; running max / sum per row.  A step
-    // whose 16 keys lie in every query's window and before the slice end
-    // needs no mask.
-    float mx[2] = {-INFINITY, -INFINITY};
-    const bool interior =
-        kb + 16 <= c1 && (full || (kb >= p0 + p.B - 1 - half && kb + 15 <= p0 + half));
-    if (interior) {
-#pragma unroll
-      for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          s[nb][e] *= kScale2;
-          mx[e >> 1] = fmaxf(mx[e >> 1], s[nb][e]);
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t b0 = ld_shared_u32(kbase + kv_off(kr, 32 * ks + 4 * t4));
+          const uint32_t b1 = ld_shared_u32(kbase + kv_off(kr, 32 * ks + 16 + 4 * t4));
+          mma_bf16_16816(s[nb], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1, s[nb]);
         }
-    } else {
+      }
+      // mask (slice end, window) and scale; running max / sum per row.  A step
+      // whose 16 keys lie in every query's window and before the slice end
+      // needs no mask.
+      float mx[2] = {-INFINITY, -INFINITY};
+      const bool interior =
+          kb + 16 <= c1 && (full || (kb >= p0 + p.B - 1 - half && kb + 15 <= p0 + half));
+      if (interior) {
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            s[nb][e] *= kScale2;
+            mx[e >> 1] = fmaxf(mx[e >> 1], s[nb][e]);
+          }
+      } else {
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int r = g + 8 * (e >> 1);
+            const int jr = static_cast<int>(kb - p0) + 8 * nb + 2 * t4 + (e & 1) - r;  // j - p_r
+            const bool vis = jr + r < static_cast<int>(c1 - p0) &&
+                             (full || r >= p.B || (jr >= -ihalf && jr <= ihalf));
+            s[nb][e] = vis ? s[nb][e] * kScale2 : -INFINITY;
+            mx[e >> 1] = fmaxf(mx[e >> 1], s[nb][e]);
+          }
+        }
+      }
+      float alpha[2], psum[2] = {0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
+        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
+        const float mnew = fmaxf(m_run[i], mx[i]);
+        alpha[i] = mnew == -INFINITY ? 1.f : exp2f(m_run[i] - mnew);
+        m_run[i] = mnew;
+      }
 #pragma unroll
       for (int nb = 0; nb < 2; ++nb) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int r = g + 8 * (e >> 1);
-          const int jr = static_cast<int>(kb - p0) + 8 * nb + 2 * t4 + (e & 1) - r;  // j - p_r
-          const bool vis = jr + r < static_cast<int>(c1 - p0) &&
-                           (full || r >= p.B || (jr >= -ihalf && jr <= ihalf));
-          s[nb][e] = vis ? s[nb][e] * kScale2 : -INFINITY;
-          mx[e >> 1] = fmaxf(mx[e >> 1], s[nb][e]);
+          const int i = e >> 1;
+          s[nb][e] = m_run[i] == -INFINITY ? 0.f : exp2f(s[nb][e] - m_run[i]);
+          psum[i] += s[nb][e];
         }
       }
-    }
-    float alpha[2], psum[2] = {0.f, 0.f};
+      // l_run is this thread's share of the row sum (its four keys of each
+      // step); alpha is the same across the quad, so the shares are added
+      // once, after the loop
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
-      mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
-      const float mnew = fmaxf(m_run[i], mx[i]);
-      alpha[i] = mnew == -INFINITY ? 1.f : exp2f(m_run[i] - mnew);
-      m_run[i] = mnew;
-    }
+      for (int i = 0; i < 2; ++i) l_run[i] = l_run[i] * alpha[i] + psum[i];
+      if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {  // a row's max moved
 #pragma unroll
-    for (int nb = 0; nb < 2; ++nb) {
+        for (int db = 0; db < 16; ++db) {
+          o[db][0] *= alpha[0];
+          o[db][1] *= alpha[0];
+          o[db][2] *= alpha[1];
+          o[db][3] *= alpha[1];
+        }
+      }
+      // probabilities as the A operand (16 rows x 16 keys)
+      const uint32_t pa0 = pack_bf16x2_rn(s[0][0], s[0][1]);
+      const uint32_t pa1 = pack_bf16x2_rn(s[0][2], s[0][3]);
+      const uint32_t pa2 = pack_bf16x2_rn(s[1][0], s[1][1]);
+      const uint32_t pa3 = pack_bf16x2_rn(s[1][2], s[1][3]);
+      // values: V rows rb .. rb + 15 read transposed, 16 dims per ldmatrix
+      const int mi = lane >> 3;
+      const int vr = rb + 8 * (mi & 1) + (lane & 7);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = e >> 1;
-        s[nb][e] = m_run[i] == -INFINITY ? 0.f : exp2f(s[nb][e] - m_run[i]);
-        psum[i] += s[nb][e];
+      for (int dp = 0; dp < 8; ++dp) {
+        uint32_t r0, r1, r2, r3;
+        ldmatrix_x4_trans(vbase + kv_off(vr, 32 * dp + 16 * (mi >> 1)), r0, r1, r2, r3);
+        mma_bf16_16816(o[2 * dp], pa0, pa1, pa2, pa3, r0, r1, o[2 * dp]);
+        mma_bf16_16816(o[2 * dp + 1], pa0, pa1, pa2, pa3, r2, r3, o[2 * dp + 1]);
       }
     }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      psum[i] += __shfl_xor_sync(0xffffffffu, psum[i], 1);
-      psum[i] += __shfl_xor_sync(0xffffffffu, psum[i], 2);
-      l_run[i] = l_run[i] * alpha[i] + psum[i];
-    }
-    if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {  // a row's max moved
-#pragma unroll
-      for (int db = 0; db < 16; ++db) {
-        o[db][0] *= alpha[0];
-        o[db][1] *= alpha[0];
-        o[db][2] *= alpha[1];
-        o[db][3] *= alpha[1];
-      }
-    }
-    // probabilities as the A operand (16 rows x 16 keys)
-    const uint32_t pa0 = pack_bf16x2_rn(s[0][0], s[0][1]);
-    const uint32_t pa1 = pack_bf16x2_rn(s[0][2], s[0][3]);
-    const uint32_t pa2 = pack_bf16x2_rn(s[1][0], s[1][1]);
-    const uint32_t pa3 = pack_bf16x2_rn(s[1][2], s[1][3]);
-    // values: V rows rb .. rb + 15 read transposed, 16 dims per ldmatrix
-    const int mi = lane >> 3;
-    const uint32_t vaddr =
-        sbase + kOffV + (rb + 8 * (mi & 1) + (lane & 7)) * kRow + 8 * (mi >> 1) * 2;
-#pragma unroll
-    for (int dp = 0; dp < 8; ++dp) {
-      uint32_t r0, r1, r2, r3;
-      ldmatrix_x4_trans(vaddr + 32 * dp, r0, r1, r2, r3);
-      mma_bf16_16816(o[2 * dp], pa0, pa1, pa2, pa3, r0, r1, o[2 * dp]);
-      mma_bf16_16816(o[2 * dp + 1], pa0, pa1, pa2, pa3, r2, r3, o[2 * dp + 1]);
-    }
-    __syncthreads();  // every warp is done with the buffer: refill it
-    if (c + kNB < nchunks) {
+    // every warp is done with the buffer: refill it (the async-proxy writes
+    // of the copy are ordered after this CTA's reads of the buffer)
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0 && c + kNB < nchunks) {
       load_chunk(c + kNB);
-      cp_async_commit();
+      issued = c + kNB + 1;
     }
   }
-  cp_async_wait_group<0>();  // a CTA with no chunk still waits for its Q copies
+  if (!loaded && threadIdx.x == 0) {
+    // A wait gave up: let every issued copy land (bounded, at least 1 s)
+    // before the buffers are reused below or the CTA exits.
+    KernelDiag drain = p.diag;
+    if (drain.wait_limit_ns < 1000000000ull) drain.wait_limit_ns = 1000000000ull;
+    for (int b = 0; b < kNB && b < issued; ++b) {
+      const int last = b + ((issued - 1 - b) / kNB) * kNB;
+      mbar_wait_bounded(&chunk_full[b], (last / kNB) & 1, drain);
+    }
+  }
+  __syncthreads();
 
   // ---- the CTA's partial: merge the warps in order
   float* wml = reinterpret_cast<float*>(smem + kOffW);  // [warp][0: max, 1: sum][row]
-  float* co = reinterpret_cast<float*>(smem + kOffO);   // [row][132]
-  float* wo = reinterpret_cast<float*>(smem + kOffK);   // [warp][row][132], K/V are done
+  float* co = reinterpret_cast<float*>(smem + kOffO);   // [row][136]
+  float* wo = reinterpret_cast<float*>(smem + kOffK);   // [warp][row][136], K/V are done
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    l_run[i] += __shfl_xor_sync(0xffffffffu, l_run[i], 1);
+    l_run[i] += __shfl_xor_sync(0xffffffffu, l_run[i], 2);
+  }
   if (t4 == 0) {
     wml[(warp * 2 + 0) * kRows + g] = m_run[0];
     wml[(warp * 2 + 0) * kRows + g + 8] = m_run[1];
@@ -274,23 +351,28 @@ __global__ void __launch_bounds__(kThreads, 1) swa_attention_kernel(const SwaPar
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wml[(w * 2) * kRows + r]);
     f[i] = (M == -INFINITY || m_run[i] == -INFINITY) ? 0.f : exp2f(m_run[i] - M);
   }
-  float* mine = wo + warp * kRows * kORow;
+  const uint32_t mine = smem_addr(wo + warp * kRows * kORow);
 #pragma unroll
   for (int db = 0; db < 16; ++db) {
     const int col = 8 * db + 2 * t4;
-    mine[g * kORow + col] = o[db][0] * f[0];
-    mine[g * kORow + col + 1] = o[db][1] * f[0];
-    mine[(g + 8) * kORow + col] = o[db][2] * f[1];
-    mine[(g + 8) * kORow + col + 1] = o[db][3] * f[1];
+    st_shared_v2_f32(mine + (g * kORow + col) * 4, o[db][0] * f[0], o[db][1] * f[0]);
+    st_shared_v2_f32(mine + ((g + 8) * kORow + col) * 4, o[db][2] * f[1], o[db][3] * f[1]);
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < kRows * kD; i += kThreads) {
-    const int r = i / kD, col = i % kD;
-    float v = 0.f;
-    for (int w = 0; w < kWarps; ++w) v += wo[(w * kRows + r) * kORow + col];
-    co[r * kORow + col] = v;
+  // quads of four values: the warps' partials added in warp order
+  for (int i = threadIdx.x; i < kRows * kD / 4; i += kThreads) {
+    const int r = i / (kD / 4), col = 4 * (i % (kD / 4));
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int w = 0; w < kWarps; ++w) {
+      const float4 x = ld_shared_v4_f32(smem_addr(wo + (w * kRows + r) * kORow + col));
+      v.x += x.x;
+      v.y += x.y;
+      v.z += x.z;
+      v.w += x.w;
+    }
+    *reinterpret_cast<float4*>(co + r * kORow + col) = v;
   }
-  // max and sum of the CTA's rows go in front of the values: part = wml[0 .. 31]
+  // max and sum of the CTA's rows go in front of each row's values
   float rowmax = -INFINITY, rowsum = 0.f;
   if (threadIdx.x < kRows) {
     const int r = threadIdx.x;
@@ -308,16 +390,23 @@ __global__ void __launch_bounds__(kThreads, 1) swa_attention_kernel(const SwaPar
   }
   __syncthreads();
   cluster_wait();
-  const uint32_t recv = dsmem_map(smem + kOffRecv, 0) + rank * kPartFloats * 4;
-  const uint32_t rbar = dsmem_map(recv_bar, 0);
-  for (int q = threadIdx.x; q < kPartFloats / 4; q += kThreads) {
-    const float* src = q < 8 ? part + 4 * q : co + ((q - 8) / 32) * kORow + 4 * ((q - 8) % 32);
-    dsmem_st_async_v4_f32(recv + 16 * q, rbar, src[0], src[1], src[2], src[3]);
+  // Row r's partial goes to rank r % S, slot (this rank, r / S) of its
+  // receive buffer: piece 0 is (max, sum, 0, 0), pieces 1..32 the values.
+  const int max_owned = (kRows + S - 1) / S;
+  for (int q = threadIdx.x; q < kRows * (kRowPart / 4); q += kThreads) {
+    const int r = q / (kRowPart / 4), piece = q % (kRowPart / 4);
+    const int owner = r % S;
+    const uint32_t dst = dsmem_map(smem + kOffRecv, owner) +
+                         ((rank * max_owned + r / S) * kRowPart + 4 * piece) * 4;
+    if (piece == 0) {
+      dsmem_st_async_v4_f32(dst, dsmem_map(recv_bar, owner), part[r], part[kRows + r], 0.f, 0.f);
+    } else {
+      const float* src = co + r * kORow + 4 * (piece - 1);
+      dsmem_st_async_v4_f32(dst, dsmem_map(recv_bar, owner), src[0], src[1], src[2], src[3]);
+    }
   }
-  if (rank != 0) return;
 
-  // ---- rank 0: merge the S partials in rank order and write O
-  int* okflag = reinterpret_cast<int*>(smem + kOffBar + 16);
+  // ---- every rank: merge the S partials of its rows in rank order, write O
   if (threadIdx.x == 0) {
     // Test hook 2: wait on a barrier nothing completes; the wait gives up,
     // reports the timeout, and the partials are still drained below before
@@ -330,29 +419,33 @@ __global__ void __launch_bounds__(kThreads, 1) swa_attention_kernel(const SwaPar
   __syncthreads();
   if (*okflag == 0) return;
   const float* rp = reinterpret_cast<const float*>(smem + kOffRecv);
-  float* wts = reinterpret_cast<float*>(smem + kOffW + 2 * kRows * 4);  // [S][16] after part
-  if (threadIdx.x < kRows) {
-    const int r = threadIdx.x;
+  float* wts = reinterpret_cast<float*>(smem + kOffW + 2 * kRows * 4);  // [S][owned] after part
+  const int owned = (kRows - rank + S - 1) / S;
+  if (threadIdx.x < owned) {
+    const int i = threadIdx.x;
     float M = -INFINITY;
-    for (int q = 0; q < S; ++q) M = fmaxf(M, rp[q * kPartFloats + r]);
+    for (int q = 0; q < S; ++q) M = fmaxf(M, rp[(q * max_owned + i) * kRowPart]);
     float L = 0.f;
     for (int q = 0; q < S; ++q) {
-      const float mq = rp[q * kPartFloats + r];
+      const float mq = rp[(q * max_owned + i) * kRowPart];
       const float w = mq == -INFINITY ? 0.f : exp2f(mq - M);
-      wts[q * kRows + r] = w;
-      L += rp[q * kPartFloats + kRows + r] * w;
+      wts[q * max_owned + i] = w;
+      L += rp[(q * max_owned + i) * kRowPart + 1] * w;
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    for (int q = 0; q < S; ++q) wts[q * kRows + r] *= inv;
+    for (int q = 0; q < S; ++q) wts[q * max_owned + i] *= inv;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < p.B * (kD / 2); i += kThreads) {
-    const int r = i / (kD / 2), d = 2 * (i % (kD / 2));
+  for (int e = threadIdx.x; e < owned * (kD / 2); e += kThreads) {
+    const int i = e / (kD / 2), d = 2 * (e % (kD / 2));
+    const int r = rank + i * S;
+    if (r >= p.B) continue;
     float v0 = 0.f, v1 = 0.f;
     for (int q = 0; q < S; ++q) {
-      const float w = wts[q * kRows + r];
-      v0 += rp[q * kPartFloats + 2 * kRows + r * kD + d] * w;
-      v1 += rp[q * kPartFloats + 2 * kRows + r * kD + d + 1] * w;
+      const float w = wts[q * max_owned + i];
+      const float* src = rp + (q * max_owned + i) * kRowPart + 4 + d;
+      v0 += src[0] * w;
+      v1 += src[1] * w;
     }
     *reinterpret_cast<uint32_t*>(p.O + (static_cast<int64_t>(r) * p.Hq + h) * kD + d) =
         pack_bf16x2_rn(v0, v1);
@@ -426,6 +519,24 @@ cudaError_t launch_swa_attention(const SwaArgs& a, cudaStream_t stream) {
   p.diag.err = a.diag.err;
   p.diag.wait_limit_ns = a.diag.wait_limit_ns;
   p.diag.force_timeout = a.diag.force_timeout;
+  // K and V as 2-D bf16 tensors [Hkv * T rows][128]; a box is 64
+  // dimensions x one chunk of rows, written with the 128-byte swizzle;
+  // rows past the end read as zeros.
+  TensorMapEncodeFn enc = tensor_map_encoder();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  CUtensorMap tmk, tmv;
+  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(kD),
+                              static_cast<cuuint64_t>(a.Hkv) * static_cast<cuuint64_t>(a.T)};
+  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(kD) * 2};
+  const cuuint32_t box[2] = {64, kChunk};
+  const cuuint32_t estride[2] = {1, 1};
+  for (int i = 0; i < 2; ++i) {
+    const CUresult r = enc(i == 0 ? &tmk : &tmv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                           const_cast<void*>(i == 0 ? a.K : a.V), gdim, gstride, box, estride,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.Hq * S));
   cfg.blockDim = dim3(kThreads);
@@ -438,7 +549,7 @@ cudaError_t launch_swa_attention(const SwaArgs& a, cudaStream_t stream) {
   attrs[0].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, swa_attention_kernel, p);
+  return cudaLaunchKernelEx(&cfg, swa_attention_kernel, tmk, tmv, p);
 }
 
 }  // namespace wq
