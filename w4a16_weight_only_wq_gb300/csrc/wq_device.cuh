@@ -167,6 +167,12 @@ __device__ __forceinline__ uint32_t dsmem_map(const void* p, uint32_t rank) {
                : "r"(smem_addr(p)), "r"(rank));
   return out;
 }
+// The same for a shared-memory address already in the 32-bit window.
+__device__ __forceinline__ uint32_t dsmem_map_addr(uint32_t saddr, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(saddr), "r"(rank));
+  return out;
+}
 
 __device__ __forceinline__ float dsmem_ld_f32(uint32_t cluster_addr) {
   float v;

@@ -55,11 +55,10 @@ constexpr int kOffV = kOffK + kNB * kChunkBytes;     // kNB V chunk buffers
 constexpr int kOffQ = kOffV + kNB * kChunkBytes;     // Q [16][256 bytes]
 constexpr int kOffW = kOffQ + kRows * kRow;          // per-warp max / sum [warps][2][16]
 constexpr int kORow = kD + 8;                        // fp32 rows of 136: conflict-free 8-byte stores
-constexpr int kOffO = kOffW + kWarps * 2 * kRows * 4;  // the CTA's values [16][132] fp32
 // Owner's receive buffer: [source rank][owned row][kRowPart] for up to
 // ceil(16 / S) owned rows; the largest over S = 1..8 is 7 x 3 rows.
 constexpr int kRecvRows = 21;
-constexpr int kOffRecv = kOffO + kRows * kORow * 4;
+constexpr int kOffRecv = kOffW + kWarps * 2 * kRows * 4;
 constexpr int kOffBar = kOffRecv + kRecvRows * kRowPart * 4;
 // barriers: receive, test hook, kNB chunks landed; then two int flags
 constexpr int kNumBars = 2 + kNB;
@@ -327,9 +326,12 @@ swa_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_const
   }
   __syncthreads();
 
-  // ---- the CTA's partial: merge the warps in order
+  // ---- the CTA's partial: merge the warps in order and send every row's
+  // share to its owner (rank row % S), slot (this rank, row / S) of the
+  // owner's receive buffer: piece 0 is (max, sum, 0, 0), pieces 1..32 the
+  // values, as 16-byte asynchronous remote stores counted on the owner's
+  // barrier.
   float* wml = reinterpret_cast<float*>(smem + kOffW);  // [warp][0: max, 1: sum][row]
-  float* co = reinterpret_cast<float*>(smem + kOffO);   // [row][136]
   float* wo = reinterpret_cast<float*>(smem + kOffK);   // [warp][row][136], K/V are done
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
@@ -359,9 +361,11 @@ swa_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_const
     st_shared_v2_f32(mine + ((g + 8) * kORow + col) * 4, o[db][2] * f[1], o[db][3] * f[1]);
   }
   __syncthreads();
-  // quads of four values: the warps' partials added in warp order
-  for (int i = threadIdx.x; i < kRows * kD / 4; i += kThreads) {
-    const int r = i / (kD / 4), col = 4 * (i % (kD / 4));
+  cluster_wait();  // every CTA of the cluster has initialised its barriers
+  const int max_owned = (kRows + S - 1) / S;
+  const uint32_t recv_local = smem_addr(smem + kOffRecv);
+  for (int q = threadIdx.x; q < kRows * kD / 4; q += kThreads) {
+    const int r = q / (kD / 4), col = 4 * (q % (kD / 4));
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int w = 0; w < kWarps; ++w) {
       const float4 x = ld_shared_v4_f32(smem_addr(wo + (w * kRows + r) * kORow + col));
@@ -370,40 +374,23 @@ swa_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_const
       v.z += x.z;
       v.w += x.w;
     }
-    *reinterpret_cast<float4*>(co + r * kORow + col) = v;
+    const int owner = r % S;
+    const uint32_t dst = recv_local + ((rank * max_owned + r / S) * kRowPart + 4 + col) * 4;
+    dsmem_st_async_v4_f32(dsmem_map_addr(dst, owner), dsmem_map(recv_bar, owner), v.x, v.y, v.z,
+                          v.w);
   }
-  // max and sum of the CTA's rows go in front of each row's values
-  float rowmax = -INFINITY, rowsum = 0.f;
   if (threadIdx.x < kRows) {
     const int r = threadIdx.x;
+    float rowmax = -INFINITY, rowsum = 0.f;
     for (int w = 0; w < kWarps; ++w) rowmax = fmaxf(rowmax, wml[(w * 2) * kRows + r]);
     for (int w = 0; w < kWarps; ++w) {
       const float mw = wml[(w * 2) * kRows + r];
       if (mw != -INFINITY) rowsum += wml[(w * 2 + 1) * kRows + r] * exp2f(mw - rowmax);
     }
-  }
-  __syncthreads();  // everyone has read wml and written co
-  float* part = wml;
-  if (threadIdx.x < kRows) {
-    part[threadIdx.x] = rowmax;
-    part[kRows + threadIdx.x] = rowsum;
-  }
-  __syncthreads();
-  cluster_wait();
-  // Row r's partial goes to rank r % S, slot (this rank, r / S) of its
-  // receive buffer: piece 0 is (max, sum, 0, 0), pieces 1..32 the values.
-  const int max_owned = (kRows + S - 1) / S;
-  for (int q = threadIdx.x; q < kRows * (kRowPart / 4); q += kThreads) {
-    const int r = q / (kRowPart / 4), piece = q % (kRowPart / 4);
     const int owner = r % S;
-    const uint32_t dst = dsmem_map(smem + kOffRecv, owner) +
-                         ((rank * max_owned + r / S) * kRowPart + 4 * piece) * 4;
-    if (piece == 0) {
-      dsmem_st_async_v4_f32(dst, dsmem_map(recv_bar, owner), part[r], part[kRows + r], 0.f, 0.f);
-    } else {
-      const float* src = co + r * kORow + 4 * (piece - 1);
-      dsmem_st_async_v4_f32(dst, dsmem_map(recv_bar, owner), src[0], src[1], src[2], src[3]);
-    }
+    const uint32_t dst = recv_local + ((rank * max_owned + r / S) * kRowPart) * 4;
+    dsmem_st_async_v4_f32(dsmem_map_addr(dst, owner), dsmem_map(recv_bar, owner), rowmax, rowsum,
+                          0.f, 0.f);
   }
 
   // ---- every rank: merge the S partials of its rows in rank order, write O
@@ -418,37 +405,27 @@ swa_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_const
   }
   __syncthreads();
   if (*okflag == 0) return;
+  // Thread (row i, dimension pair d) weighs the S partials of its row
+  // itself: w_q = exp2(m_q - M) / sum_q' l_q' exp2(m_q' - M).
   const float* rp = reinterpret_cast<const float*>(smem + kOffRecv);
-  float* wts = reinterpret_cast<float*>(smem + kOffW + 2 * kRows * 4);  // [S][owned] after part
   const int owned = (kRows - rank + S - 1) / S;
-  if (threadIdx.x < owned) {
-    const int i = threadIdx.x;
-    float M = -INFINITY;
-    for (int q = 0; q < S; ++q) M = fmaxf(M, rp[(q * max_owned + i) * kRowPart]);
-    float L = 0.f;
-    for (int q = 0; q < S; ++q) {
-      const float mq = rp[(q * max_owned + i) * kRowPart];
-      const float w = mq == -INFINITY ? 0.f : exp2f(mq - M);
-      wts[q * max_owned + i] = w;
-      L += rp[(q * max_owned + i) * kRowPart + 1] * w;
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    for (int q = 0; q < S; ++q) wts[q * max_owned + i] *= inv;
-  }
-  __syncthreads();
   for (int e = threadIdx.x; e < owned * (kD / 2); e += kThreads) {
     const int i = e / (kD / 2), d = 2 * (e % (kD / 2));
     const int r = rank + i * S;
     if (r >= p.B) continue;
-    float v0 = 0.f, v1 = 0.f;
+    float M = -INFINITY;
+    for (int q = 0; q < S; ++q) M = fmaxf(M, rp[(q * max_owned + i) * kRowPart]);
+    float L = 0.f, v0 = 0.f, v1 = 0.f;
     for (int q = 0; q < S; ++q) {
-      const float w = wts[q * max_owned + i];
-      const float* src = rp + (q * max_owned + i) * kRowPart + 4 + d;
-      v0 += src[0] * w;
-      v1 += src[1] * w;
+      const float* src = rp + (q * max_owned + i) * kRowPart;
+      const float w = src[0] == -INFINITY ? 0.f : exp2f(src[0] - M);
+      L += src[1] * w;
+      v0 += src[4 + d] * w;
+      v1 += src[5 + d] * w;
     }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
     *reinterpret_cast<uint32_t*>(p.O + (static_cast<int64_t>(r) * p.Hq + h) * kD + d) =
-        pack_bf16x2_rn(v0, v1);
+        pack_bf16x2_rn(v0 * inv, v1 * inv);
   }
 }
 
