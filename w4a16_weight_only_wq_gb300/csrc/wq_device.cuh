@@ -100,6 +100,26 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar,
   }
 }
 
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, const KernelDiag& d,
+                                          volatile int* abort_flag, uint32_t hint_ns = 0) {
+  const uint32_t a = smem_addr(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (hint_ns ? mbar_try_wait_sleep(a, parity, hint_ns) : mbar_try_wait(a, parity))
+        return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > d.wait_limit_ns) {
+      atomicMax(d.err, kErrTimeout);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
 // ------------------------------------------------------- bulk copies ---
 // 1-D bulk copy global -> this CTA's shared memory, completing `bytes` of
 // transaction on `bar`.  Addresses 16-byte aligned, bytes % 16 == 0.

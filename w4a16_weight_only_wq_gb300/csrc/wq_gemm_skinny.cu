@@ -165,7 +165,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       const int g = g0 + qc * kChunk;
       int okw = 1;
       if (lane == 0) {
-        if (qc >= kNQ) okw = wt_wait(&q_empty[slot], ((qc / kNQ) - 1) & 1, p.diag, abort_flag);
+        if (qc >= kNQ) okw = role_wait(&q_empty[slot], ((qc / kNQ) - 1) & 1, p.diag, abort_flag);
         if (okw) {
           uint8_t* dst = smem + C::kOffQ + slot * C::kQBytes;
           mbar_arrive_expect_tx(&q_full[slot], ncells * C::kColBytes);
@@ -198,7 +198,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       const int slot = si % kNX;
       int okx = 1;
       if (lane == 0) {
-        if (si >= kNX) okx = wt_wait(&x_empty[slot], ((si / kNX) - 1) & 1, p.diag, abort_flag);
+        if (si >= kNX) okx = role_wait(&x_empty[slot], ((si / kNX) - 1) & 1, p.diag, abort_flag);
         if (okx) {
           mbar_arrive_expect_tx(&x_full[slot], kXStage);
           tma_load_2d(smem + C::kOffX + slot * kXStage, &tmx, (g0 * 2 + si) * 64, 0, &x_full[slot]);
@@ -240,15 +240,15 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       for (int u = 0; u < ng; ++u) {
         const int as = u % kGA;
         const bool hook = p.diag.force_timeout == 2 && u == ng / 2;
-        if (!wt_wait(hook ? never_bar : &a_full[as], hook ? 0u : (u / kGA) & 1, p.diag,
-                     abort_flag))
+        if (!role_wait(hook ? never_bar : &a_full[as], hook ? 0u : (u / kGA) & 1, p.diag,
+                       abort_flag))
           break;
         bool ok = true;
         for (int h = 0; h < 2; ++h) {
           const int si = 2 * u + h, xs = si % kNX;
           const bool xwait = p.xblocks > 0 ? si == 0 : true;
-          if (xwait && !wt_wait(&x_full[p.xblocks > 0 ? 0 : xs], p.xblocks > 0 ? 0u : (si / kNX) & 1,
-                                p.diag, abort_flag)) {
+          if (xwait && !role_wait(&x_full[p.xblocks > 0 ? 0 : xs], p.xblocks > 0 ? 0u : (si / kNX) & 1,
+                                  p.diag, abort_flag)) {
             ok = false;
             break;
           }
@@ -279,8 +279,8 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       if (pos < 0 || pos >= kChunk) continue;  // not this warp's chunk
       const int slot = qc % kNQ;
       const int u = qc * kChunk + pos;
-      if (!wt_wait(&q_full[slot], (qc / kNQ) & 1, p.diag, abort_flag) ||
-          (u >= kGA && !wt_wait(&a_empty[r], ((u / kGA) - 1) & 1, p.diag, abort_flag)))
+      if (!role_wait(&q_full[slot], (qc / kNQ) & 1, p.diag, abort_flag) ||
+          (u >= kGA && !role_wait(&a_empty[r], ((u / kGA) - 1) & 1, p.diag, abort_flag)))
         break;
       const uint32_t qbase = smem_addr(smem + C::kOffQ + slot * C::kQBytes);
       const uint32_t s1 = ld_shared_u16(qbase + C::kScaleOff + (pos * kCols + n) * 2);
@@ -307,7 +307,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
   if (warp >= kFirstEpiWarp) {
     pdl_wait_primary();  // these warps store Y
     const int lane_base = 32 * (warp & 3);
-    if (wt_wait(d_full, 0, p.diag, abort_flag, 2000)) {
+    if (role_wait(d_full, 0, p.diag, abort_flag, 2000)) {
       tc_fence_after();
 #pragma unroll
       for (int i = 0; i < kAcc; ++i) {

@@ -185,7 +185,7 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
       const int nt = t2 / p.mt;
       int okw = 1;
       if (lane == 0) {
-        if (qc >= kNQ) okw = wt_wait(&q_empty[slot], ((qc / kNQ) - 1) & 1, p.diag, abort_flag);
+        if (qc >= kNQ) okw = role_wait(&q_empty[slot], ((qc / kNQ) - 1) & 1, p.diag, abort_flag);
         if (okw) {
           // every cell column of the tile in one copy; a column past N reads
           // as zeros and still counts in the transaction
@@ -220,8 +220,8 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
           // with one accumulator half the A and X rings coincide (slot u % 4)
           // and the MMAs release both with one commit on a_empty
           if (gi >= kXG)
-            okx = wt_wait(HALVES == 1 ? &a_empty[slot] : &b_empty[slot], ((gi / kXG) - 1) & 1,
-                          p.diag, abort_flag);
+            okx = role_wait(HALVES == 1 ? &a_empty[slot] : &b_empty[slot], ((gi / kXG) - 1) & 1,
+                            p.diag, abort_flag);
           if (okx) {
             mbar_arrive_expect_tx(&b_full[slot], 2 * kXStage);
             tma_load_3d(smem + C::kOffX + slot * 2 * kXStage, &tmx, 0, m0, (g0 + s) * 2,
@@ -254,7 +254,7 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
       bool ok = true;
       for (int tl = 0; ok && tl < my_tiles; ++tl) {
         const int buf = tl % C::kDBufs, use = tl / C::kDBufs;
-        if (tl >= C::kDBufs && !wt_wait(&d_empty[buf], (use - 1) & 1, p.diag, abort_flag)) {
+        if (tl >= C::kDBufs && !role_wait(&d_empty[buf], (use - 1) & 1, p.diag, abort_flag)) {
           ok = false;
           break;
         }
@@ -262,15 +262,15 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
         for (int g = 0; g < kch * kChunk; ++g, ++u) {
           const int as = u % kGA;
           const bool hook = p.diag.force_timeout == 2 && tl == 0 && g == kch * kChunk / 2;
-          if (!wt_wait(hook ? never_bar : &a_full[as], hook ? 0u : (u / kGA) & 1, p.diag,
-                       abort_flag)) {
+          if (!role_wait(hook ? never_bar : &a_full[as], hook ? 0u : (u / kGA) & 1, p.diag,
+                         abort_flag)) {
             ok = false;
             break;
           }
           const int xs = u % kXG;
           // HALVES == 1: the dequant warps saw the group's X land before
           // marking its A slot full, so one wait covers both
-          if (HALVES == 2 && !wt_wait(&b_full[xs], (u / kXG) & 1, p.diag, abort_flag)) {
+          if (HALVES == 2 && !role_wait(&b_full[xs], (u / kXG) & 1, p.diag, abort_flag)) {
             ok = false;
             break;
           }
@@ -318,8 +318,8 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
       if (pos < 0 || pos >= kChunk) continue;  // not this warp's chunk
       const int slot = qc % kNQ;
       const int u = qc * kChunk + pos;
-      if (!wt_wait(&q_full[slot], (qc / kNQ) & 1, p.diag, abort_flag) ||
-          (u >= kGA && !wt_wait(&a_empty[aslot], ((u / kGA) - 1) & 1, p.diag, abort_flag))) {
+      if (!role_wait(&q_full[slot], (qc / kNQ) & 1, p.diag, abort_flag) ||
+          (u >= kGA && !role_wait(&a_empty[aslot], ((u / kGA) - 1) & 1, p.diag, abort_flag))) {
         ok = false;
         break;
       }
@@ -333,7 +333,7 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
       __syncwarp();
       if (lane == 0) {
         // HALVES == 1: the group's X (same slot) has landed too
-        if (HALVES == 1 && !wt_wait(&b_full[aslot], (u / kXG) & 1, p.diag, abort_flag)) ok = false;
+        if (HALVES == 1 && !role_wait(&b_full[aslot], (u / kXG) & 1, p.diag, abort_flag)) ok = false;
         mbar_arrive(&a_full[aslot]);
         mbar_arrive(&q_empty[slot]);
       }
@@ -345,7 +345,7 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
     const int lane_base = 32 * (warp & 3);
     for (int tl = 0; tl < my_tiles; ++tl) {
       const int buf = tl % C::kDBufs, use = tl / C::kDBufs;
-      if (!wt_wait(&d_full[buf], use & 1, p.diag, abort_flag, 20000)) break;
+      if (!role_wait(&d_full[buf], use & 1, p.diag, abort_flag, 20000)) break;
       tc_fence_after();
       if (ks > 1) break;  // one tile per CTA: partials are reduced after the roles
       const int t2 = cl + tl * ncl;

@@ -60,9 +60,11 @@ constexpr int kORow = kD + 8;                        // fp32 rows of 136: confli
 constexpr int kRecvRows = 21;
 constexpr int kOffRecv = kOffW + kWarps * 2 * kRows * 4;
 constexpr int kOffBar = kOffRecv + kRecvRows * kRowPart * 4;
-// barriers: receive, test hook, kNB chunks landed; then two int flags
+// barriers: receive, test hook, kNB chunks landed; then the int flags
+// (partials arrived, abort, chunks issued, kNB release counters)
 constexpr int kNumBars = 2 + kNB;
-constexpr int kSmem = kOffBar + kNumBars * 8 + 8 + 1024;  // + alignment slack
+constexpr int kNumFlags = 3 + kNB;
+constexpr int kSmem = kOffBar + kNumBars * 8 + kNumFlags * 4 + 1024;  // + alignment slack
 static_assert(kSmem <= 232448, "shared memory of one CTA");
 static_assert(kWarps * kRows * kORow * 4 <= kNB * kChunkBytes, "warp merge fits the K buffers");
 
@@ -126,7 +128,9 @@ swa_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_const
   uint64_t* never_bar = recv_bar + 1;  // test hook: a barrier nothing completes
   uint64_t* chunk_full = never_bar + 1;  // [kNB] a chunk's K and V landed
   int* okflag = reinterpret_cast<int*>(chunk_full + kNB);  // rank's partials arrived
-  int* loadok = okflag + 1;                                  // the current chunk landed
+  volatile int* abort_flag = okflag + 1;                     // some wait gave up
+  int* issued = okflag + 2;    // chunks whose copies were issued
+  int* released = okflag + 3;  // [kNB] warps done with each buffer, over all its uses
   const uint32_t sbase = smem_addr(smem);
 
   if (threadIdx.x == 0) {
@@ -134,7 +138,11 @@ swa_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_const
     prefetch_tensor_map(&tmv);
     mbar_init(recv_bar, 1);
     mbar_init(never_bar, 1);
-    for (int i = 0; i < kNB; ++i) mbar_init(&chunk_full[i], 1);
+    for (int i = 0; i < kNB; ++i) {
+      mbar_init(&chunk_full[i], 1);
+      released[i] = 0;
+    }
+    *abort_flag = 0;
     fence_mbar_init();
     // this CTA owns rows rank, rank + S, ...: S partials of each arrive here
     const int owned = (kRows - rank + S - 1) / S;
@@ -143,10 +151,11 @@ swa_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_const
   __syncthreads();
   cluster_arrive_relaxed();  // every CTA's barrier is initialised before any remote store
 
-  // ---- staging: K / V chunks by TMA (thread 0), Q by cp.async.  A chunk
-  // covers key rows kv * T + j0 .. + 127 of the [Hkv * T][128] view; rows
-  // past the slice are real keys of the cache (or zeros past its end) and
-  // are masked below.
+  // ---- staging: K / V chunks by TMA, Q by cp.async.  A chunk covers key
+  // rows kv * T + j0 .. + 127 of the [Hkv * T][128] view; rows past the
+  // slice are real keys of the cache (or zeros past its end) and are masked
+  // below.  The last warp to release a buffer refills it, so the warps walk
+  // the chunks at their own pace, with no block-wide barrier per chunk.
   auto load_chunk = [&](int c) {
     const int buf = c % kNB;
     const int y = static_cast<int>(static_cast<int64_t>(kv) * T + c0 + static_cast<int64_t>(c) * kChunk);
@@ -159,9 +168,10 @@ swa_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_const
     tma_load_2d(vb + kHalfBytes, &tmv, 64, y, &chunk_full[buf]);
   };
   const int first = nchunks < kNB ? nchunks : kNB;
-  if (threadIdx.x == 0)
+  if (threadIdx.x == 0) {
     for (int c = 0; c < first; ++c) load_chunk(c);
-  int issued = first;  // thread 0's count of chunks whose copies were issued
+    *issued = first;
+  }
   for (int i = threadIdx.x; i < kRows * 16; i += kThreads) {
     const int r = i >> 4, piece = i & 15;
     const bool live = r < p.B;
@@ -179,24 +189,19 @@ swa_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_const
   uint32_t qa[8][4];
 
   cp_async_wait_group<0>();  // Q
-  bool loaded = true;
+  __syncthreads();           // every thread's Q pieces have landed
   for (int c = 0; c < nchunks; ++c) {
     const int buf = c % kNB;
-    // Thread 0 waits (bounded) and tells the others, so that all threads
-    // leave the loop together if the wait gives up.
-    if (threadIdx.x == 0) {
+    // Lane 0 waits (bounded) and tells its warp, so that the warp leaves
+    // the loop as a whole if the wait gives up.
+    int ok = 1;
+    if (lane == 0) {
       // test hook 2: the last chunk's wait looks for a phase that never completes
       const bool hook = p.diag.force_timeout == 2 && c == nchunks - 1;
-      *loadok = mbar_wait_bounded(hook ? never_bar : &chunk_full[buf], hook ? 0u : (c / kNB) & 1,
-                                  p.diag)
-                    ? 1
-                    : 0;
+      ok = role_wait(hook ? never_bar : &chunk_full[buf], hook ? 0u : (c / kNB) & 1, p.diag,
+                     abort_flag);
     }
-    __syncthreads();
-    if (*loadok == 0) {
-      loaded = false;
-      break;
-    }
+    if (!__shfl_sync(0xffffffffu, ok, 0)) break;
     // completes at once: makes the landed bytes visible to this thread
     mbar_wait_bounded(&chunk_full[buf], (c / kNB) & 1, p.diag);
     if (c == 0) {
@@ -305,22 +310,34 @@ swa_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_const
         mma_bf16_16816(o[2 * dp + 1], pa0, pa1, pa2, pa3, r2, r3, o[2 * dp + 1]);
       }
     }
-    // every warp is done with the buffer: refill it (the async-proxy writes
-    // of the copy are ordered after this CTA's reads of the buffer)
+    // This warp is done with the buffer: when a later chunk goes into it,
+    // its reads are ordered before the async-proxy writes of the refill, and
+    // the warp whose release completes the buffer's use (the count reaches
+    // kWarps times its uses) refills it.
+    if (c + kNB >= nchunks) continue;
     fence_proxy_async_smem();
-    __syncthreads();
-    if (threadIdx.x == 0 && c + kNB < nchunks) {
-      load_chunk(c + kNB);
-      issued = c + kNB + 1;
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      const int prev = atomicAdd(&released[buf], 1);
+      if (prev == (c / kNB + 1) * kWarps - 1) {
+        __threadfence_block();
+        fence_proxy_async_smem();
+        load_chunk(c + kNB);
+        atomicMax(issued, c + kNB + 1);
+      }
     }
   }
-  if (!loaded && threadIdx.x == 0) {
+  __syncwarp();
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) {
     // A wait gave up: let every issued copy land (bounded, at least 1 s)
     // before the buffers are reused below or the CTA exits.
     KernelDiag drain = p.diag;
     if (drain.wait_limit_ns < 1000000000ull) drain.wait_limit_ns = 1000000000ull;
-    for (int b = 0; b < kNB && b < issued; ++b) {
-      const int last = b + ((issued - 1 - b) / kNB) * kNB;
+    const int n = *issued;
+    for (int b = 0; b < kNB && b < n; ++b) {
+      const int last = b + ((n - 1 - b) / kNB) * kNB;
       mbar_wait_bounded(&chunk_full[b], (last / kNB) & 1, drain);
     }
   }

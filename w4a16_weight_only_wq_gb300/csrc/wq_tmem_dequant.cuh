@@ -1,6 +1,6 @@
-// wq_tmem_dequant.cuh -- dequantisation of packed cells into tensor memory
-// and the bounded role wait shared by the tcgen05 kernels whose A operand
-// is the dequantised weights (wq_gemm_wt.cu, wq_gemm_skinny.cu).
+// wq_tmem_dequant.cuh -- dequantisation of packed cells into tensor memory,
+// shared by the tcgen05 kernels whose A operand is the dequantised weights
+// (wq_gemm_wt.cu, wq_gemm_skinny.cu).
 #pragma once
 
 #include <cstdint>
@@ -77,26 +77,6 @@ __device__ __forceinline__ void dequant_group_to_tmem(uint32_t cell, int n, uint
         }
       }
       tmem_st_32x32b_x32(taddr + 32 * h, r);
-    }
-  }
-}
-
-// Bounded wait that also gives up as soon as another role has aborted.
-__device__ __forceinline__ bool wt_wait(uint64_t* bar, uint32_t parity, const KernelDiag& d,
-                                        volatile int* abort_flag, uint32_t hint_ns = 0) {
-  const uint32_t a = smem_addr(bar);
-  if (mbar_try_wait(a, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 16; ++i)
-      if (hint_ns ? mbar_try_wait_sleep(a, parity, hint_ns) : mbar_try_wait(a, parity))
-        return true;
-    if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > d.wait_limit_ns) {
-      atomicMax(d.err, kErrTimeout);
-      *abort_flag = 1;
-      return false;
     }
   }
 }
