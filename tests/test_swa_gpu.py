@@ -97,3 +97,22 @@ def test_swa_grouped_heads_and_determinism(wq):
     got = O1.float().cpu().numpy()
     for h in range(Hq):
         assert np.allclose(got[:, h, :], h // (Hq // Hkv) + 1, rtol=2.0 ** -7, atol=0)
+
+
+@pytest.mark.parametrize("S", [1, 2])
+def test_swa_long_slices_refill_every_buffer(wq, S):
+    """Full attention over 4,096 keys in one or two slices per head: 32 or 16
+    chunks of 128 keys per CTA, so each of the three chunk buffers is
+    refilled many times by whichever warp releases it last; the result is
+    deterministic and matches the oracle."""
+    B, Hq, Hkv, T, W = 16, 2, 1, 4096, 0
+    Q, K, V = _case(B, Hq, Hkv, T, seed=60 + S)
+    ref = oracle.swa_attention(Q, K, V, T, W)
+    try:
+        wq.wq_debug_set_split(S)
+        O1 = _run(wq, Q, K, V, T, W)
+        O2 = _run(wq, Q, K, V, T, W)
+    finally:
+        wq.wq_debug_set_split(0)
+    assert torch.equal(O1, O2)
+    assert_close_to_oracle(O1, ref, f"split {S}")
