@@ -242,11 +242,13 @@ WQ_API void wq_debug_force_timeout(int mode);
    one tile's K range in the small-M kernels and in the tensor-memory kernel
    at M < 512 (1..8, at most the tile's packed chunks; 0 restores the
    automatic choice; a split the tensor-memory kernel cannot take makes the
-   call report WQ_ERR_UNSUPPORTED), and enable programmatic dependent launch, which lets a
+   call report WQ_ERR_UNSUPPORTED; for wq_swa_attention, the number of key
+   slices per head), and enable programmatic dependent launch, which lets a
    GEMM start streaming its weights while the preceding kernel on the stream
-   finishes.  With it on, the weights and scales of a GEMM must not be
-   written by the kernel immediately before it on the same stream (X and Y
-   may be).  Both settings are process-wide. */
+   finishes, and lets the attention kernel launch and set up meanwhile (it
+   reads nothing before that kernel completes).  With it on, the weights and
+   scales of a GEMM must not be written by the kernel immediately before it
+   on the same stream (X and Y may be).  Both settings are process-wide. */
 WQ_API void wq_debug_set_split(int cs);
 WQ_API void wq_set_programmatic_launch(int on);
 

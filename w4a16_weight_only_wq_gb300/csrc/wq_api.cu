@@ -339,6 +339,7 @@ wq_status wq_swa_attention(const void* Q, const void* K, const void* V, void* O,
   a.window = window;
   a.num_sms = d.num_sms;
   a.device = dev;
+  a.pdl = g_pdl.load();
   a.split_hint = g_split_hint.load();
   a.diag = diag_for(d);
   return cuda_status(wq::launch_swa_attention(a, stream));

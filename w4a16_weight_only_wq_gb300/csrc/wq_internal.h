@@ -77,6 +77,7 @@ struct SwaArgs {
   int64_t T, window;
   int num_sms;
   int device;
+  int pdl;          // launch with programmatic stream serialization
   int split_hint;   // 0 = automatic number of key slices per head
   DiagHost diag;
 };

@@ -17,7 +17,8 @@
 //  * Keys in chunks of 128 rows (16 per warp, eight warps).  K and V come
 //    by TMA, four copies per chunk (each 64-dimension half of K and of V)
 //    with the 128-byte swizzle, so the fragment loads are conflict-free;
-//    three chunks in flight.  Keys past the slice are masked.  Scores and the weighted sum use mma.sync m16n8k16
+//    three chunks in flight; a slice's last, partial chunk in 16-row boxes.
+//    Keys past the slice are masked.  Scores and the weighted sum use mma.sync m16n8k16
 //    (bf16 in, fp32 accumulate); the probabilities are re-packed from the
 //    score accumulators into the A operand of the second MMA, and V is read
 //    transposed with ldmatrix.
@@ -105,7 +106,8 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, u
 
 __global__ void __launch_bounds__(kThreads, 1)
 swa_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                     const SwaParams p) {
+                     const __grid_constant__ CUtensorMap tmk16,
+                     const __grid_constant__ CUtensorMap tmv16, const SwaParams p) {
   extern __shared__ uint8_t smem_raw[];
   // the swizzled TMA buffers want 1024-byte alignment; every CTA of the
   // cluster gets the same offset, so remote addresses match
@@ -136,6 +138,8 @@ swa_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_const
   if (threadIdx.x == 0) {
     prefetch_tensor_map(&tmk);
     prefetch_tensor_map(&tmv);
+    prefetch_tensor_map(&tmk16);
+    prefetch_tensor_map(&tmv16);
     mbar_init(recv_bar, 1);
     mbar_init(never_bar, 1);
     for (int i = 0; i < kNB; ++i) {
@@ -150,22 +154,43 @@ swa_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_const
   }
   __syncthreads();
   cluster_arrive_relaxed();  // every CTA's barrier is initialised before any remote store
+  // Q, K and V may come from the preceding kernel (programmatic launch):
+  // nothing global is read before it completes; the next kernel may start
+  // launching now.
+  pdl_wait_primary();
+  pdl_launch_dependents();
 
   // ---- staging: K / V chunks by TMA, Q by cp.async.  A chunk covers key
   // rows kv * T + j0 .. + 127 of the [Hkv * T][128] view; rows past the
   // slice are real keys of the cache (or zeros past its end) and are masked
   // below.  The last warp to release a buffer refills it, so the warps walk
   // the chunks at their own pace, with no block-wide barrier per chunk.
+  // A chunk with fewer than 128 keys left in the slice (its last) comes in
+  // boxes of 16 rows, as many as cover its keys.
   auto load_chunk = [&](int c) {
     const int buf = c % kNB;
-    const int y = static_cast<int>(static_cast<int64_t>(kv) * T + c0 + static_cast<int64_t>(c) * kChunk);
+    const int64_t j0 = c0 + static_cast<int64_t>(c) * kChunk;
+    const int y = static_cast<int>(static_cast<int64_t>(kv) * T + j0);
     uint8_t* kb = smem + kOffK + buf * kChunkBytes;
     uint8_t* vb = smem + kOffV + buf * kChunkBytes;
-    mbar_arrive_expect_tx(&chunk_full[buf], 2 * kChunkBytes);
-    tma_load_2d(kb, &tmk, 0, y, &chunk_full[buf]);
-    tma_load_2d(kb + kHalfBytes, &tmk, 64, y, &chunk_full[buf]);
-    tma_load_2d(vb, &tmv, 0, y, &chunk_full[buf]);
-    tma_load_2d(vb + kHalfBytes, &tmv, 64, y, &chunk_full[buf]);
+    const int64_t left = c1 - j0;
+    if (left >= kChunk) {
+      mbar_arrive_expect_tx(&chunk_full[buf], 2 * kChunkBytes);
+      tma_load_2d(kb, &tmk, 0, y, &chunk_full[buf]);
+      tma_load_2d(kb + kHalfBytes, &tmk, 64, y, &chunk_full[buf]);
+      tma_load_2d(vb, &tmv, 0, y, &chunk_full[buf]);
+      tma_load_2d(vb + kHalfBytes, &tmv, 64, y, &chunk_full[buf]);
+    } else {
+      const int nblk = static_cast<int>((left + 15) / 16);
+      mbar_arrive_expect_tx(&chunk_full[buf], static_cast<uint32_t>(4 * nblk * 16 * 128));
+      for (int b = 0; b < nblk; ++b) {
+        const int off = b * 16 * 128;
+        tma_load_2d(kb + off, &tmk16, 0, y + 16 * b, &chunk_full[buf]);
+        tma_load_2d(kb + kHalfBytes + off, &tmk16, 64, y + 16 * b, &chunk_full[buf]);
+        tma_load_2d(vb + off, &tmv16, 0, y + 16 * b, &chunk_full[buf]);
+        tma_load_2d(vb + kHalfBytes + off, &tmv16, 64, y + 16 * b, &chunk_full[buf]);
+      }
+    }
   };
   const int first = nchunks < kNB ? nchunks : kNB;
   if (threadIdx.x == 0) {
@@ -518,15 +543,16 @@ cudaError_t launch_swa_attention(const SwaArgs& a, cudaStream_t stream) {
   // rows past the end read as zeros.
   TensorMapEncodeFn enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
-  CUtensorMap tmk, tmv;
+  // A second pair of maps with 16-row boxes serves a slice's last chunk.
+  CUtensorMap maps[4];  // K, V (128-row boxes), K, V (16-row boxes)
   const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(kD),
                               static_cast<cuuint64_t>(a.Hkv) * static_cast<cuuint64_t>(a.T)};
   const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(kD) * 2};
-  const cuuint32_t box[2] = {64, kChunk};
   const cuuint32_t estride[2] = {1, 1};
-  for (int i = 0; i < 2; ++i) {
-    const CUresult r = enc(i == 0 ? &tmk : &tmv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                           const_cast<void*>(i == 0 ? a.K : a.V), gdim, gstride, box, estride,
+  for (int i = 0; i < 4; ++i) {
+    const cuuint32_t box[2] = {64, i < 2 ? static_cast<cuuint32_t>(kChunk) : 16u};
+    const CUresult r = enc(&maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                           const_cast<void*>(i % 2 == 0 ? a.K : a.V), gdim, gstride, box, estride,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
@@ -536,14 +562,21 @@ cudaError_t launch_swa_attention(const SwaArgs& a, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attrs[1];
-  attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = S;
-  attrs[0].val.clusterDim.y = 1;
-  attrs[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attrs[2];
+  int na = 0;
+  attrs[na].id = cudaLaunchAttributeClusterDimension;
+  attrs[na].val.clusterDim.x = S;
+  attrs[na].val.clusterDim.y = 1;
+  attrs[na].val.clusterDim.z = 1;
+  ++na;
+  if (a.pdl) {
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attrs;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, swa_attention_kernel, tmk, tmv, p);
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, swa_attention_kernel, maps[0], maps[1], maps[2], maps[3], p);
 }
 
 }  // namespace wq
