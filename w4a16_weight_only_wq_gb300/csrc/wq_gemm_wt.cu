@@ -165,6 +165,9 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The next kernel may launch now: its CTAs take SMs this grid leaves
+  // free, and it reads nothing this grid writes before it completes.
+  pdl_launch_dependents();
   if (p.diag.force_timeout == 1) mbar_wait_bounded(never_bar, 0, p.diag);
 
   int issued_q = 0, issued_b = 0;
@@ -174,7 +177,6 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
       prefetch_tensor_map(&tmx);
       prefetch_tensor_map(&tmw);
     }
-    pdl_wait_primary();
     const int total_q = my_tiles * kch;
     bool ok = true;
     // chunk qc (global over this CTA's tiles) -> tile and first group
@@ -234,10 +236,14 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
       }
       return true;
     };
+    // The packed weights and scales do not depend on the preceding kernel:
+    // the first chunks are requested before waiting for it (programmatic
+    // launch); X, which it may write, after.
     for (int qc = 0; qc < min(kNQ, total_q) && ok; ++qc) {
       ok = issue_q(qc);
       if (ok) issued_q = qc + 1;
     }
+    pdl_wait_primary();
     for (int qc = 0; qc < total_q && ok; ++qc) {
       ok = issue_x(qc);
       if (ok && qc + kNQ < total_q) {
@@ -470,7 +476,6 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
                    pack_bf16x2(acc[6], acc[7]));
     }
   }
-  pdl_launch_dependents();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
