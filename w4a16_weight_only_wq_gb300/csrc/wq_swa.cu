@@ -18,11 +18,18 @@
 //    by TMA, four copies per chunk (each 64-dimension half of K and of V)
 //    with the 128-byte swizzle, so the fragment loads are conflict-free;
 //    three chunks in flight; a slice's last, partial chunk in 16-row boxes.
-//    Keys past the slice are masked.  Scores and the weighted sum use mma.sync m16n8k16
-//    (bf16 in, fp32 accumulate); the probabilities are re-packed from the
-//    score accumulators into the A operand of the second MMA, and V is read
-//    transposed with ldmatrix.
-//  * The pass is bound by reading each head's visible K and V once.
+//    Keys past the slice are masked.  The warps walk the chunks at their own
+//    pace (no block-wide barrier per chunk); the last warp to release a
+//    buffer issues its refill.
+//  * Scores and the weighted sum use mma.sync m16n8k16 (bf16 in, fp32
+//    accumulate) with an online softmax in base 2; the probabilities are
+//    re-packed from the score accumulators into the A operand of the second
+//    MMA, and V is read transposed with ldmatrix.
+//  * With programmatic launch the kernel sets up while the preceding kernel
+//    drains and reads nothing global before it completes.
+//  * Its bytes are each head's visible K and V read once; at the drafter's
+//    sizes the pass is bound by latency (copy landing, the per-chunk
+//    dependent MMA and softmax steps, the merges), not by those bytes.
 #include <cuda_bf16.h>
 
 #include <atomic>
