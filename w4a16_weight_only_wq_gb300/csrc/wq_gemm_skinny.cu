@@ -39,6 +39,7 @@
 #include "wq_device.cuh"
 #include "wq_internal.h"
 #include "wq_tcgen05.cuh"
+#include "wq_tensor_map.h"
 #include "wq_tmem_dequant.cuh"
 
 namespace wq {
@@ -387,24 +388,6 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
 }
 
 // ------------------------------------------------------------ host side ---
-typedef CUresult (*SkEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                               const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                               const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                               CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-SkEncodeFn sk_encode_fn() {
-  static SkEncodeFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<SkEncodeFn>(f);
-  });
-  return fn;
-}
 
 // Per device: the kernel's shared-memory attribute, and for every cluster
 // size 1..8 how many clusters can be resident at once.
@@ -472,7 +455,7 @@ bool gemm_skinny_fits(int bits, int64_t K, int64_t N) {
 
 cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t stream) {
   if (a.M > kTok || !gemm_skinny_fits(a.bits, a.K, a.N)) return cudaErrorNotSupported;
-  SkEncodeFn enc = sk_encode_fn();
+  TensorMapEncodeFn enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
   int max_cl[9];
   cudaError_t e = a.bits == 4 ? g_sk4.ensure(a.device, max_cl) : g_sk8.ensure(a.device, max_cl);

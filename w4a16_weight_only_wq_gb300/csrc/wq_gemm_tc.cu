@@ -29,6 +29,7 @@
 #include "wq_device.cuh"
 #include "wq_internal.h"
 #include "wq_tcgen05.cuh"
+#include "wq_tensor_map.h"
 
 namespace wq {
 namespace {
@@ -415,24 +416,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const TcParams p) {
 }
 
 // ------------------------------------------------------------ host side ---
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  });
-  return fn;
-}
 
 template <int BITS>
 struct TcInit {
@@ -457,7 +440,7 @@ TcInit<8> g_tc8;
 }  // namespace
 
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t stream) {
-  EncodeTiledFn enc = encode_fn();
+  TensorMapEncodeFn enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
   cudaError_t e = a.bits == 4 ? g_tc4.ensure(a.device) : g_tc8.ensure(a.device);
   if (e != cudaSuccess) return e;

@@ -40,6 +40,7 @@
 #include "wq_device.cuh"
 #include "wq_internal.h"
 #include "wq_tcgen05.cuh"
+#include "wq_tensor_map.h"
 #include "wq_tmem_dequant.cuh"
 
 namespace wq {
@@ -484,24 +485,6 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
 }
 
 // ------------------------------------------------------------ host side ---
-typedef CUresult (*WtEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                               const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                               const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                               CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-WtEncodeFn wt_encode_fn() {
-  static WtEncodeFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<WtEncodeFn>(f);
-  });
-  return fn;
-}
 
 // Per device: the kernel's shared-memory attribute and, for every cluster
 // size 1..8, how many clusters can be resident at once (tiles of 128 columns
@@ -564,7 +547,7 @@ int wt_split(int64_t tiles, int nchunks, int num_sms, int hint, const int (&max_
 }
 
 template <int BITS, int HALVES, int ACT>
-cudaError_t launch_wt(const GemmArgs& a, cudaStream_t stream, WtEncodeFn enc) {
+cudaError_t launch_wt(const GemmArgs& a, cudaStream_t stream, TensorMapEncodeFn enc) {
   using C = WtCfg<BITS, HALVES>;
   constexpr int kTN = C::kTN;
   int max_cl[9];
@@ -658,7 +641,7 @@ bool gemm_wt_fits(int bits, int64_t M, int64_t K, int64_t N) {
 
 cudaError_t launch_gemm_wt(const GemmArgs& a, cudaStream_t stream) {
   if (!gemm_wt_fits(a.bits, a.M, a.K, a.N)) return cudaErrorNotSupported;
-  WtEncodeFn enc = wt_encode_fn();
+  TensorMapEncodeFn enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
   const bool wide = a.M >= kWideMinM;
   if (a.act != 0) {
