@@ -150,6 +150,9 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
   // every CTA of the cluster has started before any remote store (epilogue)
   if (cs > 1) cluster_arrive_relaxed();
   const uint32_t tmem_base = *tmem_slot;
+  // The next kernel may launch now: it reads nothing this grid writes
+  // before this grid completes.
+  pdl_launch_dependents();
   if (p.diag.force_timeout == 1) mbar_wait_bounded(never_bar, 0, p.diag);
 
   int issued_q = 0, issued_x = 0;
@@ -379,7 +382,6 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       p.Y[static_cast<size_t>(m) * p.N + n0 + cb0 + c] = __float2bfloat16_rn(acc);
     }
   }
-  pdl_launch_dependents();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();

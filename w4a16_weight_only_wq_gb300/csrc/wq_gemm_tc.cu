@@ -232,6 +232,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const TcParams p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The next kernel may launch now: it reads nothing this grid writes
+  // before this grid completes.
+  pdl_launch_dependents();
 
   // X and Y may belong to the preceding kernel on the stream.
   pdl_wait_primary();
@@ -408,7 +411,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const TcParams p) {
     __syncwarp();
     __syncthreads();
   }
-  pdl_launch_dependents();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
