@@ -47,6 +47,8 @@ def _run(wq, Q, K, V, T, W):
     (5, 4, 2, 700, 128),        # a short block
     (1, 2, 1, 90, 16),
     (16, 2, 2, 16, 8),          # the block alone
+    (16, 6, 2, 900, 512),       # three query heads per key/value head: one CTA per query head
+    (16, 16, 8, 2000, 600),     # two query heads per key/value head: one CTA per key/value head
 ])
 def test_swa_matches_oracle(wq, B, Hq, Hkv, T, W):
     Q, K, V = _case(B, Hq, Hkv, T, seed=B + T + W)
