@@ -118,3 +118,14 @@ def test_swa_long_slices_refill_every_buffer(wq, S):
         wq.wq_debug_set_split(0)
     assert torch.equal(O1, O2)
     assert_close_to_oracle(O1, ref, f"split {S}")
+
+
+@pytest.mark.parametrize("T,W", [(8192, 2048), (8192, 1024), (2048, 4096)])
+def test_swa_bench_workloads(wq, T, W):
+    """The three attention workloads bench.py times (16-token block, 32 query
+    heads over 8 key/value heads of 128), in the same launch configuration,
+    against the oracle over every output."""
+    B, Hq, Hkv = 16, 32, 8
+    Q, K, V = _case(B, Hq, Hkv, T, seed=T + W)
+    assert_close_to_oracle(_run(wq, Q, K, V, T, W), oracle.swa_attention(Q, K, V, T, W),
+                           f"T={T} W={W}")
