@@ -402,6 +402,12 @@ swa_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_const
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wml[(w * 2) * kRows + r]);
     f[i] = (M == -INFINITY || m_run[i] == -INFINITY) ? 0.f : exp2f(m_run[i] - M);
   }
+  // the warp's row sums rescaled to the CTA's row maxima replace its sums
+  // (only the maxima are read above)
+  if (t4 == 0) {
+    wml[(warp * 2 + 1) * kRows + g] = l_run[0] * f[0];
+    wml[(warp * 2 + 1) * kRows + g + 8] = l_run[1] * f[1];
+  }
   const uint32_t mine = smem_addr(wo + warp * kRows * kORow);
 #pragma unroll
   for (int db = 0; db < 16; ++db) {
@@ -431,10 +437,9 @@ swa_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_const
   if (threadIdx.x < kRows) {
     const int r = threadIdx.x;
     float rowmax = -INFINITY, rowsum = 0.f;
-    for (int w = 0; w < kWarps; ++w) rowmax = fmaxf(rowmax, wml[(w * 2) * kRows + r]);
     for (int w = 0; w < kWarps; ++w) {
-      const float mw = wml[(w * 2) * kRows + r];
-      if (mw != -INFINITY) rowsum += wml[(w * 2 + 1) * kRows + r] * exp2f(mw - rowmax);
+      rowmax = fmaxf(rowmax, wml[(w * 2) * kRows + r]);
+      rowsum += wml[(w * 2 + 1) * kRows + r];  // already rescaled to the row maximum
     }
     const int owner = r % S;
     const uint32_t dst = recv_local + ((rank * max_owned + r / S) * kRowPart) * 4;
