@@ -202,9 +202,9 @@ WQ_API wq_status wq_mlp_w4a16(const void* X, const uint32_t* Wu, const void* Su,
  *   query head h reads key/value head h / (Hq / Hkv).
  * Errors: WQ_ERR_NULL, WQ_ERR_UNSUPPORTED (head dim other than 128),
  * WQ_ERR_SHAPE (B outside 1..16, Hq not a multiple of Hkv, Hq > 4096, T < B,
- * T > 2^30, Hkv * T > 2^31 - 256, window < 0), WQ_ERR_ALIGN, WQ_ERR_CUDA, and
- * WQ_ERR_DEVICE_TIMEOUT through
- * wq_last_device_error().  Stream-ordered; allocates nothing.
+ * T > 2^30, Hkv * T > 2^31 - 256, window < 0), WQ_ERR_ALIGN, WQ_ERR_CUDA,
+ * and WQ_ERR_DEVICE_TIMEOUT through wq_last_device_error().  Stream-ordered;
+ * allocates nothing.
  */
 WQ_API wq_status wq_swa_attention(const void* Q, const void* K, const void* V, void* O,
                                   int64_t B, int64_t Hq, int64_t Hkv, int64_t D, int64_t T,
