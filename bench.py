@@ -454,7 +454,7 @@ def run_wq(args):
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak,
                 "traffic": recorded_traffic(WORKLOAD),
-                "kernel": "gemm_small_kernel<4>",
+                "kernel": "gemm_small_kernel<4, CH> (CH = 4 up, 2 down)",
                 "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
                 "bytes_per_launch": BYTES_STEP // 2}
 

@@ -15,10 +15,11 @@
 //  * Copies are few and large, because the copy engine of an SM issues one
 //    copy every ~30 ns whatever its size: the tile's packed cells over the
 //    CTA's K range are contiguous, so a chunk of four groups (16 KiB INT4 /
-//    32 KiB INT8) is one bulk copy, and X is one bulk copy per row for the
-//    whole K range.  The producer warp issues weight chunk 0, waits for the
-//    preceding kernel (programmatic launch), issues X, then the rest of the
-//    weight ring; scales travel with their chunk (16-byte cp.async).
+//    32 KiB INT8; two groups for a K split with long CTA ranges) is one
+//    bulk copy, and X is one bulk copy per row for the whole K range.  The
+//    producer warp issues weight chunk 0, waits for the preceding kernel
+//    (programmatic launch), issues X, then the rest of the weight ring;
+//    scales travel with their chunk (16-byte cp.async).
 //  * Sixteen consumer warps each take half a group (32 columns) at a time.
 //    Dequant happens in registers: one LOP3 turns two 4-bit fields into the
 //    bf16 values 128 + u (INT8: 128 + lo and 2048 + 16 hi), one exact
@@ -41,18 +42,18 @@ namespace {
 constexpr int kConsumerWarps = 16;
 constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kChunk = 4;                  // groups per weight chunk
 constexpr int kRedStride = 36;             // floats per row of a half-tile partial (16-byte rows)
 constexpr int kRedBytes = kConsumerWarps * 16 * kRedStride * 4;
 constexpr int kPartFloats = 1024 + 64;     // cs slices of ceil(256 / cs) quads of floats
 
-template <int BITS>
+// CH groups per weight chunk (one bulk copy): 4, or 2 (see launch_gemm_small).
+template <int BITS, int CH>
 struct Cell {
   static constexpr int kWords = BITS == 4 ? 1024 : 2048;
   static constexpr int kBytes = kWords * 4;
-  // weight chunk slot: kChunk cells, then kChunk x 64 scales
-  static constexpr int kSlot = kChunk * kBytes + kChunk * 128;
-  static constexpr int kScaleOff = kChunk * kBytes;
+  // weight chunk slot: CH cells, then CH x 64 scales
+  static constexpr int kSlot = CH * kBytes + CH * 128;
+  static constexpr int kScaleOff = CH * kBytes;
 };
 
 struct SmallParams {
@@ -84,7 +85,6 @@ template <int BITS>
 __device__ __forceinline__ void process_half(float (&acc)[4][4], uint32_t slot_addr,
                                              uint32_t s_addr, uint32_t x_addr, int xstride,
                                              int half, int lane) {
-  using C = Cell<BITS>;
   constexpr uint32_t kMask = 0x000F000Fu;
   constexpr uint32_t kLo = 0x43004300u;    // bf16 128.0 in both halves
   constexpr uint32_t kHi = 0x45004500u;    // bf16 2048.0 in both halves
@@ -169,10 +169,11 @@ __device__ __forceinline__ void process_half(float (&acc)[4][4], uint32_t slot_a
   }
 }
 
-template <int BITS>
+template <int BITS, int CH>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_small_kernel(const SmallParams p) {
-  using C = Cell<BITS>;
+  using C = Cell<BITS, CH>;
+  constexpr int kChunk = CH;
   extern __shared__ __align__(16) uint8_t smem[];
 
   const int cs = p.cs, DW = p.wslots, xs = p.xstride;
@@ -399,7 +400,7 @@ gemm_small_kernel(const SmallParams p) {
 }
 
 // ------------------------------------------------------------ host side ---
-template <int BITS>
+template <int BITS, int CH>
 struct KernelInit {
   std::atomic<uint64_t> done{0};  // one bit per device
   std::mutex mu;
@@ -414,10 +415,10 @@ struct KernelInit {
             &optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
         if (e != cudaSuccess) return e;
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, gemm_small_kernel<BITS>);
+        e = cudaFuncGetAttributes(&fa, gemm_small_kernel<BITS, CH>);
         if (e != cudaSuccess) return e;
         const int dyn = optin - static_cast<int>(fa.sharedSizeBytes);
-        e = cudaFuncSetAttribute(gemm_small_kernel<BITS>,
+        e = cudaFuncSetAttribute(gemm_small_kernel<BITS, CH>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
         if (e != cudaSuccess) return e;
         max_dyn[device & 63] = dyn;
@@ -428,10 +429,15 @@ struct KernelInit {
     return cudaSuccess;
   }
 };
-KernelInit<4> g_init4;
-KernelInit<8> g_init8;
+KernelInit<4, 4> g_init44;
+KernelInit<4, 2> g_init42;
+KernelInit<8, 4> g_init84;
+KernelInit<8, 2> g_init82;
 
-int slot_bytes(int bits) { return bits == 4 ? Cell<4>::kSlot : Cell<8>::kSlot; }
+int slot_bytes(int bits, int ch) {
+  if (bits == 4) return ch == 4 ? Cell<4, 4>::kSlot : Cell<4, 2>::kSlot;
+  return ch == 4 ? Cell<8, 4>::kSlot : Cell<8, 2>::kSlot;
+}
 
 // Cluster split along K: the largest cs in 1..8 (and <= groups) for which
 // tiles * cs CTAs still fit one per SM, so the whole grid is resident and
@@ -454,16 +460,16 @@ bool gemm_small_fits(int bits, int64_t K, int64_t N, int split_hint) {
   // 227 KiB a CTA may use on sm_103.
   const int64_t ng_max = (K / 128 + cs - 1) / cs;
   if (ng_max > 4096) return false;
-  return smem_bytes_for(1, slot_bytes(bits), x_stride(static_cast<int>(ng_max))) <= 232448;
+  return smem_bytes_for(1, slot_bytes(bits, 2), x_stride(static_cast<int>(ng_max))) <= 232448;
 }
 
 cudaError_t launch_gemm_small(const GemmArgs& a, cudaStream_t stream) {
   if (a.M > 16) return cudaErrorNotSupported;
   const int cs = choose_split(a.K, a.N, a.num_sms, a.split_hint);
   if (cs < 0) return cudaErrorNotSupported;
-  int max_dyn = 0;
-  cudaError_t e = a.bits == 4 ? g_init4.ensure(a.device, &max_dyn)
-                              : g_init8.ensure(a.device, &max_dyn);
+  int max_dyn = 0;  // the same for every variant (none uses static shared memory)
+  cudaError_t e = a.bits == 4 ? g_init44.ensure(a.device, &max_dyn)
+                              : g_init84.ensure(a.device, &max_dyn);
   if (e != cudaSuccess) return e;
 
   SmallParams p;
@@ -477,12 +483,22 @@ cudaError_t launch_gemm_small(const GemmArgs& a, cudaStream_t stream) {
   p.G = static_cast<int>(a.K / 128);
   p.cs = cs;
   const int ng_max = (p.G + cs - 1) / cs;
-  const int nch_max = (ng_max + kChunk - 1) / kChunk;
-  const int sb = slot_bytes(a.bits);
   p.xstride = x_stride(ng_max);
+  // Chunks of four groups; of two for a K split with long CTA ranges
+  // (measured at M = 16: 9728 x 2560, 26 groups per CTA, 8.23 -> 8.09 us;
+  // short ranges such as 2560 x 2560, 7 groups, and unsplit tiles are
+  // slower with them).
+  const int ch = cs > 1 && ng_max >= 16 ? 2 : 4;
+  const int nch_max = (ng_max + ch - 1) / ch;
+  const int sb = slot_bytes(a.bits, ch);
   int dw = nch_max;
   while (dw > 0 && smem_bytes_for(dw, sb, p.xstride) > max_dyn) --dw;
   if (dw < 1) return cudaErrorNotSupported;
+  if (a.bits == 4)
+    e = ch == 4 ? g_init44.ensure(a.device, &max_dyn) : g_init42.ensure(a.device, &max_dyn);
+  else
+    e = ch == 4 ? g_init84.ensure(a.device, &max_dyn) : g_init82.ensure(a.device, &max_dyn);
+  if (e != cudaSuccess) return e;
   p.wslots = dw;
   p.act = a.act;
   p.pf = static_cast<const uint8_t*>(a.l2_prefetch);
@@ -510,8 +526,11 @@ cudaError_t launch_gemm_small(const GemmArgs& a, cudaStream_t stream) {
   }
   cfg.attrs = attrs;
   cfg.numAttrs = na;
-  if (a.bits == 4) return cudaLaunchKernelEx(&cfg, gemm_small_kernel<4>, p);
-  return cudaLaunchKernelEx(&cfg, gemm_small_kernel<8>, p);
+  if (a.bits == 4)
+    return ch == 4 ? cudaLaunchKernelEx(&cfg, gemm_small_kernel<4, 4>, p)
+                   : cudaLaunchKernelEx(&cfg, gemm_small_kernel<4, 2>, p);
+  return ch == 4 ? cudaLaunchKernelEx(&cfg, gemm_small_kernel<8, 4>, p)
+                 : cudaLaunchKernelEx(&cfg, gemm_small_kernel<8, 2>, p);
 }
 
 }  // namespace wq
