@@ -93,6 +93,7 @@ struct WtParams {
   int M, N, K, G;
   int mt, nt;  // tile counts along M and N
   int ks;      // CTAs of a cluster that split one tile's K range (1: none)
+  int tn;      // tokens per MMA (N): 64 when M <= 64, else kTM
   KernelDiag diag;
 };
 
@@ -226,7 +227,7 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
             okx = role_wait(HALVES == 1 ? &a_empty[slot] : &b_empty[slot], ((gi / kXG) - 1) & 1,
                             p.diag, abort_flag);
           if (okx) {
-            mbar_arrive_expect_tx(&b_full[slot], 2 * kXStage);
+            mbar_arrive_expect_tx(&b_full[slot], 2 * p.tn * 128);
             tma_load_3d(smem + C::kOffX + slot * 2 * kXStage, &tmx, 0, m0, (g0 + s) * 2,
                         &b_full[slot]);
           }
@@ -256,7 +257,11 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
   } else if (warp == 1) {
     // ---------------------------------------------------- MMA issuer ---
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, kTM);
+      // N = p.tn tokens: a 64-token MMA when M <= 64 (the rows past it would
+      // be zeros), which costs about half a 128-token one
+      const uint32_t idesc = p.tn == 64 ? idesc_bf16_f32(128, 64) : idesc_bf16_f32(128, kTM);
+      // a group's X copy lands as [stage][p.tn rows][128 bytes]
+      const uint32_t x_stage = HALVES == 2 ? kXStage : p.tn * 128;
       int u = 0;  // global group index of this CTA
       bool ok = true;
       for (int tl = 0; ok && tl < my_tiles; ++tl) {
@@ -285,7 +290,7 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ 
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const uint64_t b_desc =
-                smem_desc_sw128(smem_addr(smem + C::kOffX + (2 * xs + h) * kXStage));
+                smem_desc_sw128(smem_addr(smem + C::kOffX + 2 * xs * kXStage + h * x_stage));
 #pragma unroll
             for (int hf = 0; hf < HALVES; ++hf) {
               // half hf of the weight columns: its own accumulator and A
@@ -561,7 +566,8 @@ cudaError_t launch_wt(const GemmArgs& a, cudaStream_t stream, TensorMapEncodeFn 
   CUtensorMap tmx;
   const cuuint64_t gdim[3] = {64, static_cast<cuuint64_t>(a.M), static_cast<cuuint64_t>(a.K / 64)};
   const cuuint64_t gstride[2] = {static_cast<cuuint64_t>(a.K) * 2, 128};
-  const cuuint32_t box[3] = {64, kTM, 2};
+  const int tn = a.M <= 64 ? 64 : kTM;  // tokens per MMA and per X box
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(tn), 2};
   const cuuint32_t estride[3] = {1, 1, 1};
   CUresult r = enc(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.X), gdim,
                    gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -592,6 +598,7 @@ cudaError_t launch_wt(const GemmArgs& a, cudaStream_t stream, TensorMapEncodeFn 
   p.G = static_cast<int>(a.K / 128);
   p.mt = static_cast<int>((a.M + kTM - 1) / kTM);
   p.nt = static_cast<int>((a.N + kTN - 1) / kTN);
+  p.tn = tn;
   p.diag.err = a.diag.err;
   p.diag.wait_limit_ns = a.diag.wait_limit_ns;
   p.diag.force_timeout = a.diag.force_timeout;
