@@ -115,9 +115,12 @@ wq_status check_gemm(const void* X, const uint32_t* Wp, const void* scales, cons
 // kernel applied it (the warp-MMA and tensor-memory tiled kernels do).
 // pf / pf_bytes: weights of the GEMM that follows, pulled into L2 by the
 // warp-MMA kernel after its own weights have landed.
+// pf / pf_bytes: the next GEMM's weights, for the small-M kernel to pull
+// into L2; weights_in_l2: this GEMM's weights were pulled so by the one
+// before it.
 wq_status gemm_run(int bits, const void* X, const uint32_t* Wp, const void* scales, void* Y,
                    int64_t M, int64_t N, int64_t K, cudaStream_t stream, int act,
-                   const void* pf, int64_t pf_bytes, bool* act_done) {
+                   const void* pf, int64_t pf_bytes, bool weights_in_l2, bool* act_done) {
   *act_done = act == 0;
   if (M == 0) return WQ_OK;
   int dev;
@@ -140,6 +143,7 @@ wq_status gemm_run(int bits, const void* X, const uint32_t* Wp, const void* scal
   a.act = 0;
   a.l2_prefetch = nullptr;
   a.l2_prefetch_bytes = 0;
+  a.weights_in_l2 = weights_in_l2 ? 1 : 0;
   a.diag = diag_for(d);
   int regime = pick_regime(M);
   if (regime == 0 && !wq::gemm_small_fits(bits, K, N, a.split_hint)) regime = 1;
@@ -183,7 +187,7 @@ wq_status gemm_common(int bits, const void* X, const uint32_t* Wp, const void* s
   wq_status st = check_gemm(X, Wp, scales, Y, M, N, K, group);
   if (st != WQ_OK || M == 0) return st;
   bool act_done;
-  return gemm_run(bits, X, Wp, scales, Y, M, N, K, stream, 0, nullptr, 0, &act_done);
+  return gemm_run(bits, X, Wp, scales, Y, M, N, K, stream, 0, nullptr, 0, false, &act_done);
 }
 
 // The fused MLP pair: H = act(bf16(X . Wu)), Y = bf16(H . Wd).
@@ -197,13 +201,13 @@ wq_status mlp_common(int bits, const void* X, const uint32_t* Wu, const void* Su
   if (st != WQ_OK || M == 0) return st;
   const int64_t wd_bytes = bits == 4 ? N1 * N2 / 2 : N1 * N2;
   bool act_done = false;
-  st = gemm_run(bits, X, Wu, Su, H, M, N1, K, stream, act, Wd, wd_bytes, &act_done);
+  st = gemm_run(bits, X, Wu, Su, H, M, N1, K, stream, act, Wd, wd_bytes, false, &act_done);
   if (st != WQ_OK) return st;
   if (!act_done) {
     st = cuda_status(wq::launch_silu_inplace(static_cast<uint16_t*>(H), M * N1, stream));
     if (st != WQ_OK) return st;
   }
-  return gemm_run(bits, H, Wd, Sd, Y, M, N2, N1, stream, 0, nullptr, 0, &act_done);
+  return gemm_run(bits, H, Wd, Sd, Y, M, N2, N1, stream, 0, nullptr, 0, true, &act_done);
 }
 
 }  // namespace

@@ -485,10 +485,10 @@ cudaError_t launch_gemm_small(const GemmArgs& a, cudaStream_t stream) {
   const int ng_max = (p.G + cs - 1) / cs;
   p.xstride = x_stride(ng_max);
   // Chunks of four groups; of two for a K split with long CTA ranges
-  // (measured at M = 16: 9728 x 2560, 26 groups per CTA, 8.23 -> 8.09 us;
-  // short ranges such as 2560 x 2560, 7 groups, and unsplit tiles are
-  // slower with them).
-  const int ch = cs > 1 && ng_max >= 16 ? 2 : 4;
+  // streamed from HBM (measured at M = 16: 9728 x 2560, 26 groups per CTA,
+  // 8.23 -> 8.09 us; short ranges such as 2560 x 2560, 7 groups, unsplit
+  // tiles and weights already in L2 are slower with them).
+  const int ch = cs > 1 && ng_max >= 16 && !a.weights_in_l2 ? 2 : 4;
   const int nch_max = (ng_max + ch - 1) / ch;
   const int sb = slot_bytes(a.bits, ch);
   int dw = nch_max;

@@ -46,6 +46,7 @@ struct GemmArgs {
   int act;          // 0: none; 1: Y = bf16(silu(bf16(X . W))) (small and wt kernels only)
   const void* l2_prefetch;    // small kernel: bytes to pull into L2 once its weights have
   int64_t l2_prefetch_bytes;  // landed (the next GEMM's weights); 16-byte aligned and sized
+  int weights_in_l2;          // the preceding GEMM pulled these weights into L2
   DiagHost diag;
 };
 // Returns cudaErrorNotSupported when the shape does not fit this kernel.
