@@ -453,3 +453,19 @@ def test_wt_workload_prefill_sampled_rows(wq, wt_regime, case):
                                      np.arange(case.M - 8, case.M),
                                      rng.integers(0, case.M, 24)]))
     _run_codes_case(wq, d["X"], d["q"], d["s"], case.bits, rows=rows)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("cs", [2, 3])
+def test_two_group_chunks_ragged(wq, bits, cs):
+    """Warp-MMA kernel with two-group weight chunks (a K split over 16 or
+    more groups per CTA): 33 groups split 2 or 3 ways, so a CTA's last chunk
+    holds a single group; 7 rows, 3 tiles."""
+    M, K, N = 7, 128 * 33, 192
+    X, q, s = synth.small_case(M, K, N, bits, seed=70 + cs + bits)
+    assert wq.wq_gemm_regime(bits, M, N, K) == 0
+    try:
+        wq.wq_debug_set_split(cs)
+        _run_codes_case(wq, X, q, s, bits)
+    finally:
+        wq.wq_debug_set_split(0)
