@@ -80,8 +80,23 @@ typedef enum { WQ_F32 = 0, WQ_BF16 = 1 } wq_dtype;
 typedef enum { WQ_ACT_NONE = 0, WQ_ACT_SILU = 1 } wq_act;
 
 /* Number of uint32 words in a packed [K,N] weight with `bits` (4 or 8)
-   bits per code: K*N/8 or K*N/4.  Returns 0 for unsupported arguments. */
+   bits per code: K*N/8 or K*N/4 -- the "8 per int32" packing of the INT4
+   target ("Quantize the Target, Quantize the Drafter", packing paragraph:
+   the weights are served as W4A16, group-wise INT4) and one byte per code
+   for the int8 drafter ("Qwen3.5-4B-DFlash-W8A16" card, "What changed vs
+   upstream" table, int8 weight-only).  Returns 0 for unsupported arguments
+   (bits not 4/8, K % 128, N % 64, sizes out of range).  Pure host
+   arithmetic: no device is needed. */
 WQ_API size_t wq_packed_words(int bits, int64_t K, int64_t N);
+
+/* Device bytes a packed [K,N] layer occupies: the codes (bits*K*N/8) plus
+   its bf16 scales, one per 128-deep group and column (2*(K/128)*N).  This is
+   the storage accounting of the "Qwen3.5-4B-DFlash-W8A16" card's "What
+   changed vs upstream" table (1.00 GB of bf16 weights -> 521 MB as W8A16):
+   one byte per INT8 weight (half a byte per INT4 weight) plus 2/128 of a
+   byte per weight for the scales.  Returns 0 for unsupported arguments, as
+   wq_packed_words.  Pure host arithmetic. */
+WQ_API size_t wq_packed_bytes(int bits, int64_t K, int64_t N);
 
 /*
  * Pack step (one-off per weight, "at packing time" in the packing paragraph
@@ -103,9 +118,17 @@ WQ_API wq_status wq_pack_symmetric(const void* W, wq_dtype wdt, int64_t K, int64
                             uint16_t* scales_out, uint32_t* packed,
                             cudaStream_t stream);
 
-/* Interleave ready-made int8 codes [K,N] (e.g. from an external GPTQ/AWQ
-   export; each code must lie in [qmin,qmax], other values are wrapped to the
-   field width) into the packed layout. */
+/* Interleave ready-made int8 codes [K,N] into the packed layout, without
+   rounding: the codes are already on the grid, as when a GPTQ-quantized
+   layer is packed ("Quantize the Target, Quantize the Drafter" project
+   README, pipeline table: the GPTQ drafter export and pack_ct.sh; the
+   packing paragraph of the paper: codes on a fixed symmetric grid).  Each
+   code must lie in [qmin,qmax] ([-8,7] for bits 4, [-128,127] for bits 8);
+   other values are wrapped to the field width.  `codes` and `packed` are
+   caller-owned device memory, 16-byte aligned; `packed` holds
+   wq_packed_words(bits,K,N) words.  Errors: WQ_ERR_NULL, WQ_ERR_UNSUPPORTED
+   (bits), WQ_ERR_SHAPE (K % 128, N % 64), WQ_ERR_ALIGN, WQ_ERR_CUDA.
+   Stream-ordered; allocates nothing. */
 WQ_API wq_status wq_pack_codes(const int8_t* codes, int64_t K, int64_t N, int bits,
                         uint32_t* packed, cudaStream_t stream);
 
@@ -143,7 +166,12 @@ WQ_API wq_status wq_dequantize(const uint32_t* packed, const uint16_t* scales, i
                                int64_t K, int64_t N, int group, uint16_t* W,
                                cudaStream_t stream);
 
-/* Inverse of the interleave: int8 codes [K,N] from a packed weight. */
+/* Inverse of the interleave: the int8 codes q [K,N] (row-major, values in
+   [qmin,qmax]) of a packed weight -- the codes the QAD paragraph of
+   "Quantize the Target, Quantize the Drafter" multiplies by the frozen
+   scales (student weights s (.) Wq).  `packed` (wq_packed_words words) and
+   `codes` (K*N bytes) are caller-owned device memory, 16-byte aligned.
+   Errors as wq_pack_codes.  Stream-ordered; allocates nothing. */
 WQ_API wq_status wq_unpack(const uint32_t* packed, int bits, int64_t K, int64_t N,
                     int8_t* codes, cudaStream_t stream);
 
@@ -248,7 +276,10 @@ WQ_API void wq_debug_force_timeout(int mode);
    finishes, and lets the attention kernel launch and set up meanwhile (it
    reads nothing before that kernel completes).  With it on, the weights and
    scales of a GEMM must not be written by the kernel immediately before it
-   on the same stream (X and Y may be).  Both settings are process-wide. */
+   on the same stream (X and Y may be).  Both settings are process-wide:
+   they apply to every later call from every thread of the process (not
+   thread-safe with respect to calls in flight on other threads), and
+   programmatic launch is off until a caller turns it on. */
 WQ_API void wq_debug_set_split(int cs);
 WQ_API void wq_set_programmatic_launch(int on);
 

@@ -20,7 +20,7 @@ def wq():
     return m
 
 
-@pytest.fixture(params=[0, 1, 2, 3], ids=["warpmma", "tc", "tmem", "wt"])
+@pytest.fixture(params=[0, 1, 2, 3, 4], ids=["warpmma", "tc", "tmem", "wt", "stream"])
 def regime(wq, request):
     wq.wq_debug_force_regime(request.param)
     yield request.param
@@ -54,7 +54,7 @@ def test_forced_timeout_reports_and_recovers(wq, regime, bits):
 
 
 @pytest.mark.parametrize("bits", [4, 8])
-@pytest.mark.parametrize("small", [0, 2, 3], ids=["warpmma", "tmem", "wt"])
+@pytest.mark.parametrize("small", [0, 2, 3, 4], ids=["warpmma", "tmem", "wt", "stream"])
 def test_abandoned_data_wait_drains_and_recovers(wq, small, bits):
     """The data waits look for a phase that never completes: the kernel gives
     up, lets its copies land, reports the timeout, and a normal call

@@ -38,10 +38,11 @@ def _run_codes_case(wq, X, q, s, bits, rows=None):
     return assert_close_to_oracle(Ysel, Yref, f"W{bits} M={X.shape[0]} K={K} N={N}")
 
 
-@pytest.fixture(params=[0, 2], ids=["warpmma", "tmem"])
+@pytest.fixture(params=[0, 2, 4], ids=["warpmma", "tmem", "stream"])
 def small_kernel(wq, request):
     """Run the test on each small-M kernel: 0 the warp-MMA kernel (the
-    default for M <= 32), 2 the tensor-memory kernel."""
+    default for M <= 32), 2 the tensor-memory kernel, 4 the tensor-memory
+    kernel whose launches overlap."""
     wq.wq_debug_force_regime(request.param)
     yield request.param
     wq.wq_debug_force_regime(-1)
@@ -463,9 +464,144 @@ def test_two_group_chunks_ragged(wq, bits, cs):
     holds a single group; 7 rows, 3 tiles."""
     M, K, N = 7, 128 * 33, 192
     X, q, s = synth.small_case(M, K, N, bits, seed=70 + cs + bits)
-    assert wq.wq_gemm_regime(bits, M, N, K) == 0
     try:
+        wq.wq_debug_force_regime(0)
         wq.wq_debug_set_split(cs)
+        assert wq.wq_gemm_regime(bits, M, N, K) == 0
         _run_codes_case(wq, X, q, s, bits)
     finally:
         wq.wq_debug_set_split(0)
+        wq.wq_debug_force_regime(-1)
+
+
+# ------------------------- tensor-memory small-M kernel with overlapping launches ---
+@pytest.fixture
+def stream_regime(wq):
+    wq.wq_debug_force_regime(4)
+    yield
+    wq.wq_debug_force_regime(-1)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M", [1, 7, 16, 24])
+@pytest.mark.parametrize("K,N", [(128, 64), (384, 192), (1280, 576), (3840, 128),
+                                 (9728, 2560), (2560, 9728)])
+def test_stream_shapes(wq, stream_regime, bits, M, K, N):
+    """Ragged tiles (N = 64, 192, 576 leave a half tile), one to many groups
+    per CTA, the splits the SM count picks, and M > 16 in 16-row slices."""
+    assert wq.wq_gemm_regime(bits, M, N, K) == 4
+    X, q, s = synth.small_case(M, K, N, bits, seed=M * 5 + K + N + bits)
+    _run_codes_case(wq, X, q, s, bits)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_stream_every_split(wq, stream_regime, bits):
+    """Each K split 1..8 of the cluster reduction: 16 groups, 3 column tiles
+    (the last one half), 11 rows."""
+    M, K, N = 11, 2048, 320
+    X, q, s = synth.small_case(M, K, N, bits, seed=67 + bits)
+    try:
+        for cs in range(1, 9):
+            wq.wq_debug_set_split(cs)
+            _run_codes_case(wq, X, q, s, bits)
+    finally:
+        wq.wq_debug_set_split(0)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("G", [9, 30, 32])
+def test_stream_ring_refills(wq, stream_regime, bits, G):
+    """One CTA per tile (split 1) walks G groups: more than the weight ring
+    (7 groups INT4, 3 INT8), the X ring (8) and the tensor-memory A slots
+    (3) hold, up to the 32 groups its scales buffer takes."""
+    M, K, N = 16, 128 * G, 192
+    X, q, s = synth.small_case(M, K, N, bits, seed=G + bits)
+    try:
+        wq.wq_debug_set_split(1)
+        assert wq.wq_gemm_regime(bits, M, N, K) == 4
+        _run_codes_case(wq, X, q, s, bits)
+    finally:
+        wq.wq_debug_set_split(0)
+
+
+def test_stream_too_many_groups_per_cta_falls_back(wq, stream_regime):
+    """33 groups in one CTA exceed the scales buffer: the warp-MMA kernel
+    takes the shape."""
+    M, K, N = 16, 128 * 33, 128
+    X, q, s = synth.small_case(M, K, N, 4, seed=33)
+    try:
+        wq.wq_debug_set_split(1)
+        assert wq.wq_gemm_regime(4, M, N, K) == 0
+        _run_codes_case(wq, X, q, s, 4)
+    finally:
+        wq.wq_debug_set_split(0)
+
+
+def _chain_weights(wq, bits, L, K, seed):
+    """L square weights whose scales keep |Y| about |X| along a chain."""
+    rng = np.random.default_rng(seed)
+    lo, hi = (-8, 7) if bits == 4 else (-128, 127)
+    out = []
+    for _ in range(L):
+        q = rng.integers(lo, hi + 1, size=(K, K)).astype(np.int8)
+        s_f = (0.25 / (np.sqrt(K) * (4.6 if bits == 4 else 73.0))) * \
+            (np.abs(rng.standard_normal((K // 128, K))) + 0.5)
+        s = oracle.f32_to_bf16_bits(s_f.astype(np.float32))
+        out.append((q, s, wq.pack_codes(i8_to_dev(q), bits), bf16_to_dev(s)))
+    return out
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_stream_chain_reads_the_preceding_output(wq, bits):
+    """Eight GEMMs on one stream with programmatic launch on, each reading
+    the previous one's output as X: the launches overlap, so each must still
+    see its predecessor's complete result.  Every step is checked against
+    the oracle run on the step's actual input."""
+    M, K, L = 16, 2560, 8
+    ws = _chain_weights(wq, bits, L, K, seed=100 + bits)
+    rng = np.random.default_rng(7)
+    X0 = oracle.f32_to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    assert wq.wq_gemm_regime(bits, M, K, K) == 4
+    outs = []
+    try:
+        wq.wq_set_programmatic_launch(True)
+        x = bf16_to_dev(X0)
+        for q, s, Wp, st in ws:
+            x = _gemm(wq, bits, x, Wp, st)
+            outs.append(x)
+        torch.cuda.synchronize()
+    finally:
+        wq.wq_set_programmatic_launch(False)
+    assert wq.wq_last_device_error() == wq.WQ_OK
+    xin = X0
+    for i, ((q, s, _, _), y) in enumerate(zip(ws, outs)):
+        Yref = oracle.gemm(xin, oracle.pack(q, bits), s, K, K, bits)
+        assert_close_to_oracle(y, Yref, f"chain step {i}")
+        xin = bf16_to_host_bits(y)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_stream_ping_pong_matches_serial_launches(wq, bits):
+    """The same chain through two ping-pong buffers, so each launch also
+    overwrites the buffer its predecessor read: with programmatic launch the
+    bits equal those of launches that do not overlap."""
+    M, K, L = 16, 2560, 8
+    ws = _chain_weights(wq, bits, L, K, seed=200 + bits)
+    rng = np.random.default_rng(8)
+    X0 = bf16_to_dev(oracle.f32_to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32)))
+
+    def run(pdl):
+        bufs = [X0.clone(), torch.empty_like(X0)]
+        try:
+            wq.wq_set_programmatic_launch(pdl)
+            for i, (_, _, Wp, st) in enumerate(ws):
+                _gemm(wq, bits, bufs[i % 2], Wp, st, Y=bufs[(i + 1) % 2])
+            torch.cuda.synchronize()
+        finally:
+            wq.wq_set_programmatic_launch(False)
+        return bufs[L % 2].clone()
+
+    serial = run(False)
+    for _ in range(3):
+        assert torch.equal(run(True), serial)
+    assert wq.wq_last_device_error() == wq.WQ_OK

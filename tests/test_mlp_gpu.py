@@ -51,11 +51,12 @@ def test_mlp_pair_shapes(wq, bits, act, M, K, N1, N2):
     _run_pair(wq, M, K, N1, N2, bits, act, seed=M + K + bits)
 
 
-@pytest.mark.parametrize("regime,M", [(1, 40), (2, 16), (0, 33)])
+@pytest.mark.parametrize("regime,M", [(1, 40), (2, 16), (0, 33), (4, 33)])
 def test_mlp_pair_every_family(wq, regime, M):
     """Forced kernel families: the tiled shared-memory kernel and the
     tensor-memory small-M kernel take the activation as a separate pass; the
-    warp-MMA kernel at M = 33 runs in two 16-row slices plus one row."""
+    warp-MMA kernel and the overlapping-launch kernel at M = 33 run in two
+    16-row slices plus one row."""
     try:
         wq.wq_debug_force_regime(regime)
         _run_pair(wq, M, 512, 256, 192, 4, "silu", seed=7 + regime)

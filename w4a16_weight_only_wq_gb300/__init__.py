@@ -36,7 +36,7 @@ WQ_ACT_SILU = 1
 GROUP = 128
 
 EXPORTED = (
-    "wq_packed_words", "wq_pack_symmetric", "wq_pack_codes", "wq_unpack", "wq_dequantize",
+    "wq_packed_words", "wq_packed_bytes", "wq_pack_symmetric", "wq_pack_codes", "wq_unpack", "wq_dequantize",
     "wq_import_packed_nk",
     "wq_gemm_w4a16", "wq_gemm_w8a16", "wq_mlp_w4a16", "wq_mlp_w8a16", "wq_swa_attention",
     "wq_last_device_error",
@@ -64,6 +64,7 @@ def _load() -> ctypes.CDLL:
     P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     sig = {
         "wq_packed_words": ([I, I64, I64], ctypes.c_size_t),
+        "wq_packed_bytes": ([I, I64, I64], ctypes.c_size_t),
         "wq_pack_symmetric": ([P, I, I64, I64, I, I, P, P, P, P], I),
         "wq_pack_codes": ([P, I64, I64, I, P, P], I),
         "wq_unpack": ([P, I, I64, I64, P, P], I),
@@ -98,6 +99,10 @@ _lib = _load()
 # ------------------------------------------------------------ raw C ABI ---
 def wq_packed_words(bits: int, K: int, N: int) -> int:
     return int(_lib.wq_packed_words(bits, K, N))
+
+
+def wq_packed_bytes(bits: int, K: int, N: int) -> int:
+    return int(_lib.wq_packed_bytes(bits, K, N))
 
 
 def wq_pack_symmetric(W, wdt, K, N, bits, group, scales_in, scales_out, packed,

@@ -21,7 +21,7 @@ OBJ_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libwq.so")
 
 SOURCES = ["wq_api.cu", "wq_pack.cu", "wq_gemm_small.cu", "wq_gemm_tc.cu",
-           "wq_gemm_skinny.cu", "wq_gemm_wt.cu", "wq_swa.cu"]
+           "wq_gemm_skinny.cu", "wq_gemm_wt.cu", "wq_swa.cu", "wq_gemm_stream.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr",

@@ -28,10 +28,12 @@ constexpr int64_t kSmallMaxM = 32;
 // 0: warp-MMA small-M kernel (16 rows per launch), 1: tensor-core tiled
 // kernel with dequantised weights in shared memory, 2: tensor-memory
 // small-M kernel (16 rows per launch), 3: tensor-core tiled kernel with
-// dequantised weights in tensor memory.
+// dequantised weights in tensor memory, 4: tensor-memory small-M kernel
+// whose launches overlap (16 rows per launch).
+constexpr int kNumRegimes = 5;
 int pick_regime(int64_t M) {
   const int f = g_force_regime.load();
-  if (f >= 0 && f <= 3) return f;
+  if (f >= 0 && f < kNumRegimes) return f;
   // measured at K = 2560, N = 9728: kernel 3 is faster than kernel 1 at
   // every M from 64 to 8192; kernel 1 takes the shapes kernel 3 cannot
   return M <= kSmallMaxM ? 0 : 3;
@@ -79,6 +81,17 @@ wq_status device_info(int* dev_out, DeviceInfo* info) {
   return WQ_OK;
 }
 
+// SM count of the current device for host-side queries; 152 (a GB300) when
+// no device is visible, so that the answer is defined on a build machine.
+int sm_count_or_default() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+    return n;
+  cudaGetLastError();  // no device: not an error of a later call
+  return 152;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 wq_status check_kn(int64_t K, int64_t N) {
@@ -113,15 +126,16 @@ wq_status check_gemm(const void* X, const uint32_t* Wp, const void* scales, cons
 // One GEMM on the chosen kernel family, arguments already checked.  act: the
 // activation of the fused MLP's up-projection; *act_done tells whether the
 // kernel applied it (the warp-MMA and tensor-memory tiled kernels do).
-// pf / pf_bytes: weights of the GEMM that follows, pulled into L2 by the
-// warp-MMA kernel after its own weights have landed.
-// pf / pf_bytes: the next GEMM's weights, for the small-M kernel to pull
-// into L2; weights_in_l2: this GEMM's weights were pulled so by the one
-// before it.
+// pf / pf_bytes: the next GEMM's weights, for the warp-MMA small-M kernel
+// to pull into L2 once its own weights have landed; *prefetched tells
+// whether a launch was given them.  weights_in_l2: this GEMM's weights were
+// pulled so by the one before it.
 wq_status gemm_run(int bits, const void* X, const uint32_t* Wp, const void* scales, void* Y,
                    int64_t M, int64_t N, int64_t K, cudaStream_t stream, int act,
-                   const void* pf, int64_t pf_bytes, bool weights_in_l2, bool* act_done) {
+                   const void* pf, int64_t pf_bytes, bool weights_in_l2, bool* act_done,
+                   bool* prefetched) {
   *act_done = act == 0;
+  *prefetched = false;
   if (M == 0) return WQ_OK;
   int dev;
   DeviceInfo d;
@@ -146,7 +160,8 @@ wq_status gemm_run(int bits, const void* X, const uint32_t* Wp, const void* scal
   a.weights_in_l2 = weights_in_l2 ? 1 : 0;
   a.diag = diag_for(d);
   int regime = pick_regime(M);
-  if (regime == 0 && !wq::gemm_small_fits(bits, K, N, a.split_hint)) regime = 1;
+  if (regime == 4 && !wq::gemm_stream_fits(bits, K, N, a.split_hint, d.num_sms)) regime = 0;
+  if (regime == 0 && !wq::gemm_small_fits(bits, K, N, a.split_hint, d.num_sms)) regime = 1;
   if (regime == 3 && !wq::gemm_wt_fits(bits, M, K, N)) regime = 1;
   if (regime == 3) {
     a.act = act;
@@ -163,7 +178,8 @@ wq_status gemm_run(int bits, const void* X, const uint32_t* Wp, const void* scal
   // The small-M kernels take up to 16 rows per launch; taller inputs are
   // processed in 16-row slices.
   const size_t xrow = static_cast<size_t>(K) * 2, yrow = static_cast<size_t>(N) * 2;
-  if (regime == 0) a.act = act;  // the tensor-memory small-M kernel has no activation
+  // the activation is applied in the store of kernels 0 and 4; kernel 2 has none
+  if (regime == 0 || regime == 4) a.act = act;
   for (int64_t m0 = 0; m0 < M; m0 += 16) {
     a.X = static_cast<const char*>(X) + m0 * xrow;
     a.Y = static_cast<char*>(Y) + m0 * yrow;
@@ -172,13 +188,29 @@ wq_status gemm_run(int bits, const void* X, const uint32_t* Wp, const void* scal
     a.l2_prefetch = last && pf != nullptr && regime == 0 ? pf : nullptr;
     a.l2_prefetch_bytes = a.l2_prefetch != nullptr ? pf_bytes : 0;
     cudaError_t e = cudaErrorNotSupported;
+    if (regime == 4) e = wq::launch_gemm_stream(a, stream);
     if (regime == 2) e = wq::launch_gemm_skinny(a, stream);
-    // shapes the tensor-memory kernel cannot index go to the warp-MMA kernel
+    // shapes the tensor-memory kernels cannot index go to the warp-MMA kernel
     if (regime == 0 || e == cudaErrorNotSupported) e = wq::launch_gemm_small(a, stream);
-    if (e == cudaErrorNotSupported) return WQ_ERR_SHAPE;
+    if (e == cudaErrorNotSupported) {
+      // the slice does not fit the small-M kernel: the tiled kernel takes it
+      const int slice_act = a.act;
+      a.act = 0;
+      e = wq::launch_gemm_tc(a, stream);
+      if (e == cudaErrorNotSupported) return WQ_ERR_UNSUPPORTED;
+      if (e != cudaSuccess) return cuda_status(e);
+      if (slice_act != 0) {  // the caller counts on this slice being activated
+        const wq_status st2 = cuda_status(wq::launch_silu_inplace(
+            static_cast<uint16_t*>(a.Y), a.M * N, stream));
+        if (st2 != WQ_OK) return st2;
+      }
+      a.act = slice_act;
+      continue;
+    }
     if (e != cudaSuccess) return cuda_status(e);
+    if (a.l2_prefetch != nullptr) *prefetched = true;
   }
-  *act_done = act == 0 || regime == 0;
+  *act_done = act == 0 || regime == 0 || regime == 4;
   return WQ_OK;
 }
 
@@ -186,8 +218,9 @@ wq_status gemm_common(int bits, const void* X, const uint32_t* Wp, const void* s
                       int64_t M, int64_t N, int64_t K, int group, cudaStream_t stream) {
   wq_status st = check_gemm(X, Wp, scales, Y, M, N, K, group);
   if (st != WQ_OK || M == 0) return st;
-  bool act_done;
-  return gemm_run(bits, X, Wp, scales, Y, M, N, K, stream, 0, nullptr, 0, false, &act_done);
+  bool act_done, prefetched;
+  return gemm_run(bits, X, Wp, scales, Y, M, N, K, stream, 0, nullptr, 0, false, &act_done,
+                  &prefetched);
 }
 
 // The fused MLP pair: H = act(bf16(X . Wu)), Y = bf16(H . Wd).
@@ -200,14 +233,18 @@ wq_status mlp_common(int bits, const void* X, const uint32_t* Wu, const void* Su
   st = check_gemm(H, Wd, Sd, Y, M, N2, N1, group);
   if (st != WQ_OK || M == 0) return st;
   const int64_t wd_bytes = bits == 4 ? N1 * N2 / 2 : N1 * N2;
-  bool act_done = false;
-  st = gemm_run(bits, X, Wu, Su, H, M, N1, K, stream, act, Wd, wd_bytes, false, &act_done);
+  bool act_done = false, prefetched = false, unused = false;
+  st = gemm_run(bits, X, Wu, Su, H, M, N1, K, stream, act, Wd, wd_bytes, false, &act_done,
+                &prefetched);
   if (st != WQ_OK) return st;
   if (!act_done) {
     st = cuda_status(wq::launch_silu_inplace(static_cast<uint16_t*>(H), M * N1, stream));
     if (st != WQ_OK) return st;
   }
-  return gemm_run(bits, H, Wd, Sd, Y, M, N2, N1, stream, 0, nullptr, 0, true, &act_done);
+  // the down-projection's copy sizes assume its weights are in L2 only when
+  // the up-projection actually pulled them there
+  return gemm_run(bits, H, Wd, Sd, Y, M, N2, N1, stream, 0, nullptr, 0, prefetched, &act_done,
+                  &unused);
 }
 
 }  // namespace
@@ -217,6 +254,12 @@ extern "C" {
 size_t wq_packed_words(int bits, int64_t K, int64_t N) {
   if ((bits != 4 && bits != 8) || check_kn(K, N) != WQ_OK) return 0;
   return static_cast<size_t>(bits == 4 ? K * N / 8 : K * N / 4);
+}
+
+size_t wq_packed_bytes(int bits, int64_t K, int64_t N) {
+  const size_t words = wq_packed_words(bits, K, N);
+  if (words == 0) return 0;
+  return words * 4 + static_cast<size_t>(K / 128) * static_cast<size_t>(N) * 2;
 }
 
 wq_status wq_pack_symmetric(const void* W, wq_dtype wdt, int64_t K, int64_t N,
@@ -403,15 +446,17 @@ void wq_debug_set_split(int cs) { g_split_hint.store(cs < 0 || cs > 8 ? 0 : cs);
 void wq_set_programmatic_launch(int on) { g_pdl.store(on ? 1 : 0); }
 
 void wq_debug_force_regime(int regime) {
-  g_force_regime.store(regime >= 0 && regime <= 3 ? regime : -1);
+  g_force_regime.store(regime >= 0 && regime < kNumRegimes ? regime : -1);
 }
 
 int wq_gemm_regime(int bits, int64_t M, int64_t N, int64_t K) {
   if ((bits != 4 && bits != 8) || M < 0 || check_kn(K, N) != WQ_OK) return -1;
   int r = pick_regime(M);
+  const int sms = sm_count_or_default();
+  if (r == 4 && !wq::gemm_stream_fits(bits, K, N, g_split_hint.load(), sms)) r = 0;
   if (r == 2 && !wq::gemm_skinny_fits(bits, K, N)) r = 0;
   // shapes whose X slice does not fit the small-M kernel run on the tiled one
-  if (r == 0 && !wq::gemm_small_fits(bits, K, N, g_split_hint.load())) r = 1;
+  if (r == 0 && !wq::gemm_small_fits(bits, K, N, g_split_hint.load(), sms)) r = 1;
   if (r == 3 && !wq::gemm_wt_fits(bits, M, K, N)) r = 1;
   return r;
 }

@@ -383,7 +383,15 @@ gemm_small_kernel(const SmallParams p) {
     }
   }
   if (cs == 1 || e0 + static_cast<int>(threadIdx.x) >= e1) return;
-  if (!mbar_wait_bounded(part_full, 0, p.diag)) return;
+  if (!mbar_wait_bounded(part_full, 0, p.diag)) {
+    // A peer can be late by its own timed-out wait plus its drain (at least
+    // 1 s) before it sends; this CTA's shared memory must outlive those
+    // remote stores, so keep waiting (bounded) for them before exiting.
+    KernelDiag late = p.diag;
+    late.wait_limit_ns = p.diag.wait_limit_ns + 2000000000ull;
+    mbar_wait_bounded(part_full, 0, late);
+    return;
+  }
   for (int e = e0 + threadIdx.x; e < e1; e += kThreads) {
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int q = 0; q < cs; ++q) {
@@ -453,8 +461,8 @@ int choose_split(int64_t K, int64_t N, int num_sms, int hint) {
 
 }  // namespace
 
-bool gemm_small_fits(int bits, int64_t K, int64_t N, int split_hint) {
-  const int cs = choose_split(K, N, 152, split_hint);
+bool gemm_small_fits(int bits, int64_t K, int64_t N, int split_hint, int num_sms) {
+  const int cs = choose_split(K, N, num_sms, split_hint);
   if (cs <= 0) return false;
   // X for the CTA's K range and at least one weight chunk must fit the
   // 227 KiB a CTA may use on sm_103.

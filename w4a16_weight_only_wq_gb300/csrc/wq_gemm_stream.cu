@@ -1,0 +1,581 @@
+// wq_gemm_stream.cu -- tcgen05 W4A16 / W8A16 GEMM for M <= 16 that keeps
+// the weight stream going across consecutive launches.
+//
+// Y[M,N] = X[M,K] . (s (.) q)[K,N] for the verifier's 16-token block
+// ("Quantize the Target, Quantize the Drafter": the INT4 target checks an
+// anchor plus 15 drafted tokens in one forward), computed as
+// Y^T = W^T . X^T on the tensor cores: the dequantised weights bf16(s*q) are
+// the tcgen05.mma A operand in tensor memory (M = 128 weight columns, one per
+// TMEM lane) and the 16 tokens are the N = 16 operand in shared memory.
+//
+// At M = 16 a call is bound by streaming the packed weights, and a lone
+// launch cannot keep HBM busy: it starts, waits for its first bytes, and
+// ends with a reduction while no weight bytes move.  So a CTA here takes
+// under half an SM (448 threads, ~108 KiB of shared memory, 256 TMEM
+// columns) and the next launch on the stream, started early by programmatic
+// dependent launch, shares the SM with it: while this launch multiplies and
+// reduces, the next one streams its weights into shared memory and
+// dequantises its first groups into tensor memory.  Only the parts that read
+// X (the MMAs) or write Y wait for the preceding kernel.
+//
+//  * Work unit: 128 weight columns x a contiguous range of 128-deep groups;
+//    a cluster of `cs` CTAs splits one column tile's K range and each CTA
+//    accumulates its range in one TMEM accumulator [128 x 16].  Partial sums
+//    go to the owning CTA's shared memory (distributed shared memory, byte-
+//    counted asynchronous stores) and are added there in rank order.
+//  * Producer (warp 0): the scales of the CTA's range (one TMA), the packed
+//    cells of each group (one TMA per group, both 64-column cells, 128-byte
+//    swizzle) into a ring, and an L2 prefetch of the groups beyond the ring,
+//    all before the programmatic-launch wait.
+//  * Dequant (warps 6-13, two per TMEM lane quadrant, each half a group):
+//    LOP3 extraction, an exact bf16x2 subtraction of the offset and one
+//    bf16x2 multiply by the scale give bf16(s*q), stored with tcgen05.st.
+//  * MMA (warp 1, warp-uniform, elect.sync issue): waits for the preceding
+//    kernel, lets the next launch start, loads X per group (TMA) and issues
+//    eight 128x16x16 MMAs per group into the accumulator.
+//  * Epilogue (warps 2-5): tcgen05.ld of the accumulator, then Y or the
+//    cluster reduction.
+//  Every wait is bounded; an abort drains copies and MMAs, completes the
+//  cluster exchange and frees TMEM.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "wq_device.cuh"
+#include "wq_internal.h"
+#include "wq_tcgen05.cuh"
+#include "wq_tensor_map.h"
+#include "wq_tmem_dequant.cuh"
+
+namespace wq {
+namespace {
+
+constexpr int kTok = 16;             // tokens (MMA N)
+constexpr int kCols = 128;           // weight columns per CTA (MMA M, TMEM lanes)
+constexpr int kGA = 3;               // groups of A in tensor memory
+constexpr uint32_t kTmemCols = 256;  // half of an SM's tensor memory
+constexpr int kACol = 64;            // A slots: TMEM columns 64..255
+constexpr int kXG = 8;               // X ring: groups of 16 tokens x 128 k
+constexpr int kXGroupBytes = kTok * 128 * 2;  // 4 KiB: two 64-deep blocks
+constexpr int kXBlockBytes = kTok * 128;      // 2 KiB: 16 rows x 128 bytes
+constexpr int kMaxGroups = 32;       // groups per CTA (the scales buffer)
+constexpr int kPartStride = 20;      // floats per partial column (16 + pad)
+constexpr int kMaxSplit = 8;
+constexpr int kPartBytes = 10752;    // >= max over cs of cs * ceil(128/cs) * 80
+constexpr int kProducerWarp = 0, kMmaWarp = 1, kFirstEpiWarp = 2, kFirstDqWarp = 6;
+constexpr int kDqWarps = 8;
+constexpr int kThreads = (kFirstDqWarp + kDqWarps) * 32;  // 448
+
+template <int BITS>
+struct StCfg {
+  static constexpr int kCellBytes = BITS == 4 ? 4096 : 8192;
+  static constexpr int kCellRows = kCellBytes / 128;
+  static constexpr int kWBytes = 2 * kCellBytes;    // one group of both cells
+  static constexpr int kRing = BITS == 4 ? 7 : 3;   // weight groups in the ring
+  static constexpr int kOffW = 0;
+  static constexpr int kOffX = kOffW + kRing * kWBytes;
+  static constexpr int kOffS = kOffX + kXG * kXGroupBytes;
+  static constexpr int kOffP = kOffS + kMaxGroups * kCols * 2;
+  static constexpr int kOffBar = kOffP + kPartBytes;
+  static constexpr int kNumBars = 2 * kRing + 2 * kXG + 2 * kGA + 4;
+  static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
+  static_assert(kSmem <= 113 * 1024, "two CTAs must fit one SM");
+};
+
+struct StParams {
+  __nv_bfloat16* Y;
+  int M, N, G, cs;
+  int ngmax;          // groups of the longest CTA range (scales box rows)
+  int act;            // 0 none, 1 SiLU applied to the stored bf16 result
+  int prefetch_x;     // pull the CTA's X rows into L2 before the wait
+  const uint8_t* Wp;  // packed words (for the L2 prefetch)
+  const uint8_t* X;   // X rows (for the L2 prefetch)
+  KernelDiag diag;
+};
+
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kThreads, 2)
+gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
+                   const __grid_constant__ CUtensorMap tms, const StParams p) {
+  using C = StCfg<BITS>;
+  constexpr int kRing = C::kRing;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+
+  float* part = reinterpret_cast<float*>(smem + C::kOffP);  // same offset in every CTA
+  const uint16_t* sc = reinterpret_cast<const uint16_t*>(smem + C::kOffS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* w_full = bars;              // [kRing] a group's packed cells landed
+  uint64_t* w_empty = w_full + kRing;   // [kRing] dequantised
+  uint64_t* x_full = w_empty + kRing;   // [kXG] a group of X landed
+  uint64_t* x_empty = x_full + kXG;     // [kXG] MMAs done with it
+  uint64_t* a_full = x_empty + kXG;     // [kGA] group of A written
+  uint64_t* a_empty = a_full + kGA;     // [kGA] MMAs done with it
+  uint64_t* s_full = a_empty + kGA;     // scales landed
+  uint64_t* d_full = s_full + 1;        // every MMA of this CTA has completed
+  uint64_t* part_full = d_full + 1;     // every rank's partials of my columns landed
+  uint64_t* never_bar = part_full + 1;  // test hook
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cs = p.cs;
+  const int tile = blockIdx.x / cs;
+  const int rank = blockIdx.x % cs;  // == %cluster_ctarank for cluster (cs,1,1)
+  const int g0 = (p.G * rank) / cs;
+  const int ng = (p.G * (rank + 1)) / cs - g0;
+  const int n0 = tile * kCols;
+  const int rows = min(kTok, p.M);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&w_full[i], 1);
+      mbar_init(&w_empty[i], kDqWarps);
+    }
+    for (int i = 0; i < kXG; ++i) {
+      mbar_init(&x_full[i], 1);
+      mbar_init(&x_empty[i], 1);
+    }
+    for (int i = 0; i < kGA; ++i) {
+      mbar_init(&a_full[i], kDqWarps);
+      mbar_init(&a_empty[i], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(d_full, 1);
+    mbar_init(part_full, 1);
+    mbar_init(never_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // every CTA of the cluster has initialised its barriers before any remote
+  // store (matched by the wait before the partials are sent)
+  if (cs > 1) cluster_arrive_relaxed();
+  const uint32_t tmem_base = *tmem_slot;
+  if (p.diag.force_timeout == 1) mbar_wait_bounded(never_bar, 0, p.diag);
+
+  int issued_w = 0, issued_x = 0;
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------- producer ---
+    // Weights and scales do not depend on the preceding kernel: everything
+    // here may run before it completes.
+    bool ok = true;
+    if (lane == 0) {
+      prefetch_tensor_map(&tmw);
+      prefetch_tensor_map(&tms);
+      mbar_arrive_expect_tx(s_full, p.ngmax * kCols * 2);
+      tma_load_2d(smem + C::kOffS, &tms, n0, g0, s_full);
+      for (int c = 0; c < min(kRing, ng); ++c) {
+        mbar_arrive_expect_tx(&w_full[c], C::kWBytes);
+        tma_load_3d(smem + C::kOffW + c * C::kWBytes, &tmw, 0, (g0 + c) * C::kCellRows, 2 * tile,
+                    &w_full[c]);
+        issued_w = c + 1;
+      }
+      // the groups beyond the ring: into L2 now, into the ring when a slot
+      // frees up (after this launch's MMAs start)
+      if (ng > kRing) {
+        const int ncells = min(2, (p.N - n0) / 64);
+        for (int ci = 0; ci < ncells; ++ci) {
+          const size_t cell0 = (static_cast<size_t>(2 * tile + ci) * p.G + g0 + kRing);
+          prefetch_l2_bulk(p.Wp + cell0 * C::kCellBytes,
+                           static_cast<uint32_t>((ng - kRing) * C::kCellBytes));
+        }
+      }
+      for (int c = kRing; c < ng && ok; ++c) {
+        const int slot = c % kRing;
+        ok = role_wait(&w_empty[slot], ((c / kRing) - 1) & 1, p.diag, abort_flag);
+        if (ok) {
+          mbar_arrive_expect_tx(&w_full[slot], C::kWBytes);
+          tma_load_3d(smem + C::kOffW + slot * C::kWBytes, &tmw, 0, (g0 + c) * C::kCellRows,
+                      2 * tile, &w_full[slot]);
+          issued_w = c + 1;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------- MMA issuer ---
+    if (p.prefetch_x && lane < rows) {
+      // X rows of this CTA's K range into L2: harmless before the wait (a
+      // prefetch changes no data) and it hides HBM latency when X is cold
+      prefetch_l2_bulk(p.X + (static_cast<size_t>(lane) * p.G + g0) * 256,
+                       static_cast<uint32_t>(ng) * 256);
+    }
+    if (lane == 0) prefetch_tensor_map(&tmx);
+    pdl_wait_primary();     // X may be the preceding kernel's output
+    pdl_launch_dependents(); // the next launch may start streaming its weights
+    auto issue_x = [&](int u) {
+      if (elect_one()) {
+        const int xs = u % kXG;
+        mbar_arrive_expect_tx(&x_full[xs], kXGroupBytes);
+        tma_load_3d(smem + C::kOffX + xs * kXGroupBytes, &tmx, 0, 0, 2 * (g0 + u), &x_full[xs]);
+      }
+      __syncwarp();
+    };
+    for (int u = 0; u < min(kXG, ng); ++u) issue_x(u);
+    issued_x = min(kXG, ng);
+    constexpr uint32_t idesc = idesc_bf16_f32(kCols, kTok);
+    const uint32_t xbase = smem_addr(smem + C::kOffX);
+    for (int u = 0; u < ng; ++u) {
+      const int as = u % kGA, xs = u % kXG;
+      const bool hook = p.diag.force_timeout == 2 && u == ng / 2;
+      if (!role_wait(hook ? never_bar : &a_full[as], hook ? 0u : (u / kGA) & 1, p.diag,
+                     abort_flag) ||
+          !role_wait(&x_full[xs], (u / kXG) & 1, p.diag, abort_flag))
+        break;
+      tc_fence_after();
+      const uint32_t a_tmem = tmem_base + kACol + as * 64;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint64_t b_desc =
+            smem_desc_sw128(xbase + xs * kXGroupBytes + (j >> 2) * kXBlockBytes) + 2 * (j & 3);
+        if (elect_one()) umma_bf16_ts(tmem_base, a_tmem + 8 * j, b_desc, idesc, (u | j) != 0);
+        __syncwarp();
+      }
+      if (elect_one()) {
+        umma_commit(&a_empty[as]);
+        umma_commit(&x_empty[xs]);
+      }
+      __syncwarp();
+      // refill the X stage of the previous group, whose MMAs have most
+      // likely completed by now
+      if (u >= 1 && u - 1 + kXG < ng) {
+        const int ps = (u - 1) % kXG;
+        if (!role_wait(&x_empty[ps], ((u - 1) / kXG) & 1, p.diag, abort_flag)) break;
+        issue_x(u - 1 + kXG);
+        issued_x = u - 1 + kXG + 1;
+      }
+    }
+    // arrives when every MMA issued above has completed
+    if (elect_one()) umma_commit(d_full);
+    __syncwarp();
+  } else if (warp >= kFirstDqWarp) {
+    // ------------------------------------------------- dequant warps ---
+    // Quadrant q = warp % 4 (the TMEM lanes this warp may write); half h
+    // of every group (k in [64h, 64h + 64)).
+    const int q = warp & 3, h = (warp - kFirstDqWarp) >> 2;
+    const int n = 32 * q + lane;  // weight column within the tile = TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+    const uint32_t cell_off = (n >> 6) * C::kCellBytes;
+    if (role_wait(s_full, 0, p.diag, abort_flag)) {
+      for (int u = 0; u < ng; ++u) {
+        const int slot = u % kRing, as = u % kGA;
+        if (!role_wait(&w_full[slot], (u / kRing) & 1, p.diag, abort_flag) ||
+            (u >= kGA && !role_wait(&a_empty[as], ((u / kGA) - 1) & 1, p.diag, abort_flag)))
+          break;
+        tc_fence_after();
+        const uint32_t s1 = sc[u * kCols + n];
+        dequant_half_to_tmem<BITS>(smem_addr(smem + C::kOffW + slot * C::kWBytes) + cell_off,
+                                   n & 63, h, s1 | (s1 << 16),
+                                   tmem_base + lane_addr + kACol + as * 64 + 32 * h);
+        tmem_st_wait();
+        tc_fence_before();
+        fence_proxy_async_smem();  // our reads of the slot precede its refill
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&a_full[as]);
+          mbar_arrive(&w_empty[slot]);
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------- epilogue ---
+  // Accumulator D[column n][token m]: thread n of the epilogue warps holds
+  // the 16 token sums of column n.
+  float v[kTok];
+#pragma unroll
+  for (int m = 0; m < kTok; ++m) v[m] = 0.f;
+  const bool epi = warp >= kFirstEpiWarp && warp < kFirstDqWarp;
+  const int en = 32 * (warp & 3) + lane;  // the epilogue thread's column
+  if (epi) {
+    if (role_wait(d_full, 0, p.diag, abort_flag, 200)) {
+      tc_fence_after();
+      uint32_t r[16];
+      tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16), r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int m = 0; m < kTok; ++m) v[m] = __uint_as_float(r[m]);
+    }
+  }
+  // Roles that ran on one lane rejoin their warp before the block-wide
+  // barrier, which a diverged warp must not reach.
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // Let every issued copy land and every issued MMA finish (bounded, at
+    // least 1 s) before shared and tensor memory are released.
+    KernelDiag drain = p.diag;
+    if (drain.wait_limit_ns < 1000000000ull) drain.wait_limit_ns = 1000000000ull;
+    if (warp == kProducerWarp && lane == 0) {
+      mbar_wait_bounded(s_full, 0, drain);
+      for (int s = 0; s < kRing && s < issued_w; ++s) {
+        const int last = s + ((issued_w - 1 - s) / kRing) * kRing;
+        mbar_wait_bounded(&w_full[s], (last / kRing) & 1, drain);
+      }
+    }
+    if (warp == kMmaWarp && lane == 0) {
+      for (int s = 0; s < kXG && s < issued_x; ++s) {
+        const int last = s + ((issued_x - 1 - s) / kXG) * kXG;
+        mbar_wait_bounded(&x_full[s], (last / kXG) & 1, drain);
+      }
+      mbar_wait_bounded(d_full, 0, drain);
+    }
+    __syncwarp();
+    __syncthreads();
+  }
+  if (epi) pdl_wait_primary();  // Y may be read or written by the preceding kernel
+  if (cs == 1) {
+    if (epi && n0 + en < p.N) {
+#pragma unroll
+      for (int m = 0; m < kTok; ++m)
+        if (m < rows)
+          p.Y[static_cast<size_t>(m) * p.N + n0 + en] = __float2bfloat16_rn(apply_act(v[m], p.act));
+    }
+  } else {
+    // Rank r owns the tile's columns [128 r / cs, 128 (r + 1) / cs) and
+    // receives, per source rank q, the 16 token partials of each of its
+    // columns at part[(q * slice + local column) * 20 ..] (four 16-byte
+    // remote stores per column, counted on the owner's part_full).  Every
+    // rank sends its bytes even after an abort, so every owner's count
+    // completes.
+    const int slice = (kCols + cs - 1) / cs;
+    const int cb0 = (rank * kCols) / cs, ncol = ((rank + 1) * kCols) / cs - cb0;
+    if (threadIdx.x == kFirstEpiWarp * 32)
+      mbar_arrive_expect_tx(part_full, static_cast<uint32_t>(cs * ncol * kTok * 4));
+    cluster_wait();  // every CTA of the cluster has initialised its barriers
+    if (epi) {
+      int owner = (en * cs) / kCols;
+      while (owner + 1 < cs && en >= ((owner + 1) * kCols) / cs) ++owner;
+      while (en < (owner * kCols) / cs) --owner;
+      const int lc = en - (owner * kCols) / cs;
+      const uint32_t dst = dsmem_map(part + (rank * slice + lc) * kPartStride, owner);
+      const uint32_t bar = dsmem_map(part_full, owner);
+#pragma unroll
+      for (int i = 0; i < kTok / 4; ++i)
+        dsmem_st_async_v4_f32(dst + 16 * i, bar, v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    }
+    if (epi) {
+      const int c = en;
+      if (c < ncol) {
+        if (!mbar_wait_bounded(part_full, 0, p.diag)) {
+          // a peer can be late by its own timed-out wait plus its drain
+          KernelDiag late = p.diag;
+          late.wait_limit_ns = p.diag.wait_limit_ns + 2000000000ull;
+          mbar_wait_bounded(part_full, 0, late);
+        }
+        float acc[kTok];
+#pragma unroll
+        for (int m = 0; m < kTok; ++m) acc[m] = 0.f;
+        for (int qq = 0; qq < cs; ++qq) {
+          const uint32_t src = smem_addr(part + (qq * slice + c) * kPartStride);
+#pragma unroll
+          for (int i = 0; i < kTok / 4; ++i) {
+            const float4 w = ld_shared_v4_f32(src + 16 * i);
+            acc[4 * i] += w.x;
+            acc[4 * i + 1] += w.y;
+            acc[4 * i + 2] += w.z;
+            acc[4 * i + 3] += w.w;
+          }
+        }
+        if (n0 + cb0 + c < p.N) {
+#pragma unroll
+          for (int m = 0; m < kTok; ++m)
+            if (m < rows)
+              p.Y[static_cast<size_t>(m) * p.N + n0 + cb0 + c] =
+                  __float2bfloat16_rn(apply_act(acc[m], p.act));
+        }
+      }
+    }
+    // no CTA leaves while a peer may still store into its shared memory
+    __syncwarp();
+    cluster_sync();
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------ host side ---
+
+// Per device: the kernel's shared-memory attributes, and for every cluster
+// size 1..8 how many clusters can be resident at once.
+template <int BITS>
+struct StInit {
+  std::atomic<uint64_t> done{0};
+  std::mutex mu;
+  int max_clusters[64][kMaxSplit + 1] = {};
+  cudaError_t ensure(int device, int (&out)[kMaxSplit + 1]) {
+    const uint64_t bit = 1ull << (device & 63);
+    if (!(done.load(std::memory_order_acquire) & bit)) {
+      std::lock_guard<std::mutex> lk(mu);
+      if (!(done.load() & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_stream_kernel<BITS>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             StCfg<BITS>::kSmem);
+        if (e != cudaSuccess) return e;
+        // all of the unified L1/shared memory as shared, so that two CTAs
+        // (this launch's and the next one's) fit one SM
+        e = cudaFuncSetAttribute(gemm_stream_kernel<BITS>,
+                                 cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        if (e != cudaSuccess) return e;
+        for (int c = 1; c <= kMaxSplit; ++c) {
+          cudaLaunchConfig_t cfg = {};
+          cfg.gridDim = dim3(c);
+          cfg.blockDim = dim3(kThreads);
+          cfg.dynamicSmemBytes = StCfg<BITS>::kSmem;
+          cudaLaunchAttribute at;
+          at.id = cudaLaunchAttributeClusterDimension;
+          at.val.clusterDim.x = c;
+          at.val.clusterDim.y = 1;
+          at.val.clusterDim.z = 1;
+          cfg.attrs = &at;
+          cfg.numAttrs = 1;
+          int n = 0;
+          if (cudaOccupancyMaxActiveClusters(&n, gemm_stream_kernel<BITS>, &cfg) != cudaSuccess)
+            n = 0;
+          max_clusters[device & 63][c] = n;
+        }
+        cudaGetLastError();  // a refused size above is not an error of this call
+        done.fetch_or(bit, std::memory_order_release);
+      }
+    }
+    for (int c = 0; c <= kMaxSplit; ++c) out[c] = max_clusters[device & 63][c];
+    return cudaSuccess;
+  }
+};
+StInit<4> g_st4;
+StInit<8> g_st8;
+
+// The K split: the largest cs <= 8 (and <= the groups) whose CTAs fill at
+// most one slot per SM (the other slot is for the neighbouring launch).
+int st_split(int64_t tiles, int64_t G, int num_sms, int hint) {
+  if (hint > 0) return (hint <= kMaxSplit && hint <= G) ? hint : -1;
+  int best = 1;
+  for (int cs = 1; cs <= kMaxSplit && cs <= G; ++cs)
+    if (tiles * cs <= num_sms) best = cs;
+  return best;
+}
+
+}  // namespace
+
+bool gemm_stream_fits(int bits, int64_t K, int64_t N, int split_hint, int num_sms) {
+  const int64_t G = K / 128, tiles = (N + kCols - 1) / kCols;
+  const int cs = st_split(tiles, G, num_sms, split_hint);
+  if (cs < 1) return false;
+  if ((G + cs - 1) / cs > kMaxGroups) return false;  // the scales of a CTA's range
+  const int64_t cell_rows = bits == 4 ? 32 : 64;
+  return G * cell_rows < (int64_t(1) << 31) && N / 64 < (int64_t(1) << 31);
+}
+
+cudaError_t launch_gemm_stream(const GemmArgs& a, cudaStream_t stream) {
+  if (a.M > kTok || a.M < 1) return cudaErrorNotSupported;
+  if (!gemm_stream_fits(a.bits, a.K, a.N, a.split_hint, a.num_sms)) return cudaErrorNotSupported;
+  TensorMapEncodeFn enc = tensor_map_encoder();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  int max_cl[kMaxSplit + 1];
+  cudaError_t e = a.bits == 4 ? g_st4.ensure(a.device, max_cl) : g_st8.ensure(a.device, max_cl);
+  if (e != cudaSuccess) return e;
+  const int64_t G = a.K / 128, tiles = (a.N + kCols - 1) / kCols;
+  const int cs = st_split(tiles, G, a.num_sms, a.split_hint);
+  if (cs < 1 || max_cl[cs] < 1) return cudaErrorNotSupported;
+  const int ngmax = static_cast<int>((G + cs - 1) / cs);
+
+  // X as a 3-D bf16 tensor [K/64 blocks][M rows][64]; one box is a group's
+  // two 64-deep blocks for 16 rows (128-byte swizzle); rows past M read as
+  // zeros.
+  CUtensorMap tmx;
+  const cuuint64_t xdim[3] = {64, static_cast<cuuint64_t>(a.M), static_cast<cuuint64_t>(a.K / 64)};
+  const cuuint64_t xstride[2] = {static_cast<cuuint64_t>(a.K) * 2, 128};
+  const cuuint32_t xbox[3] = {64, kTok, 2};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = enc(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.X), xdim,
+                   xstride, xbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  // The packed weights as a 3-D u32 tensor [N/64 cell columns][G cells x
+  // 128-byte rows][32 words]; one box is one group's cell of both cell
+  // columns of a tile (a column past N reads as zeros).
+  CUtensorMap tmw;
+  const int cell_rows = a.bits == 4 ? StCfg<4>::kCellRows : StCfg<8>::kCellRows;
+  const int cell_bytes = a.bits == 4 ? StCfg<4>::kCellBytes : StCfg<8>::kCellBytes;
+  const cuuint64_t wdim[3] = {32, static_cast<cuuint64_t>(G) * cell_rows,
+                              static_cast<cuuint64_t>(a.N / 64)};
+  const cuuint64_t wstride[2] = {128, static_cast<cuuint64_t>(G) * cell_bytes};
+  const cuuint32_t wbox[3] = {32, static_cast<cuuint32_t>(cell_rows), 2};
+  r = enc(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(a.Wp), wdim, wstride,
+          wbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  // The scales as a 2-D bf16 tensor [G rows][N]; one box is 128 columns of
+  // the longest CTA range (rows and columns past the tensor read as zeros).
+  CUtensorMap tms;
+  const cuuint64_t sdim[2] = {static_cast<cuuint64_t>(a.N), static_cast<cuuint64_t>(G)};
+  const cuuint64_t sstride[1] = {static_cast<cuuint64_t>(a.N) * 2};
+  const cuuint32_t sbox[2] = {kCols, static_cast<cuuint32_t>(ngmax)};
+  r = enc(&tms, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.S), sdim, sstride, sbox,
+          estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+
+  StParams p;
+  p.Y = static_cast<__nv_bfloat16*>(a.Y);
+  p.M = static_cast<int>(a.M);
+  p.N = static_cast<int>(a.N);
+  p.G = static_cast<int>(G);
+  p.cs = cs;
+  p.ngmax = ngmax;
+  p.act = a.act;
+  p.prefetch_x = 1;
+  p.Wp = reinterpret_cast<const uint8_t*>(a.Wp);
+  p.X = static_cast<const uint8_t*>(a.X);
+  p.diag.err = a.diag.err;
+  p.diag.wait_limit_ns = a.diag.wait_limit_ns;
+  p.diag.force_timeout = a.diag.force_timeout;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles * cs));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = a.bits == 4 ? StCfg<4>::kSmem : StCfg<8>::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  int na = 0;
+  attrs[na].id = cudaLaunchAttributeClusterDimension;
+  attrs[na].val.clusterDim.x = cs;
+  attrs[na].val.clusterDim.y = 1;
+  attrs[na].val.clusterDim.z = 1;
+  ++na;
+  if (a.pdl) {
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = na;
+  if (a.bits == 4) return cudaLaunchKernelEx(&cfg, gemm_stream_kernel<4>, tmx, tmw, tms, p);
+  return cudaLaunchKernelEx(&cfg, gemm_stream_kernel<8>, tmx, tmw, tms, p);
+}
+
+}  // namespace wq

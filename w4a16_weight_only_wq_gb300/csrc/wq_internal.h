@@ -51,12 +51,18 @@ struct GemmArgs {
 };
 // Returns cudaErrorNotSupported when the shape does not fit this kernel.
 cudaError_t launch_gemm_small(const GemmArgs& a, cudaStream_t stream);
-bool gemm_small_fits(int bits, int64_t K, int64_t N, int split_hint);
+// num_sms: the device's SM count (the cluster split fills the SMs).
+bool gemm_small_fits(int bits, int64_t K, int64_t N, int split_hint, int num_sms);
 
 // Tensor-memory GEMM for M <= 16 (wq_gemm_skinny.cu).  Needs K / 128 to
 // be even.
 cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t stream);
 bool gemm_skinny_fits(int bits, int64_t K, int64_t N);
+
+// Tensor-memory GEMM for M <= 16 whose CTAs take half an SM, so that
+// consecutive launches overlap (wq_gemm_stream.cu).
+cudaError_t launch_gemm_stream(const GemmArgs& a, cudaStream_t stream);
+bool gemm_stream_fits(int bits, int64_t K, int64_t N, int split_hint, int num_sms);
 
 // Tensor-core GEMM for large M, dequantised weights staged in shared
 // memory (wq_gemm_tc.cu).
