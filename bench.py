@@ -52,6 +52,12 @@ def algorithmic_bytes(m, k, n, bits=4):
     return k * n * bits // 8 + (k // GROUP) * n * 2 + m * k * 2 + m * n * 2
 
 
+# A spin of this many SM cycles (~0.1 ms) is queued on the stream before
+# each start event, so that the CPU-side submission of the timed graph is
+# over before the GPU reaches it: the region then holds the device time of
+# the timed steps and nothing before them.
+SPIN_CYCLES = 200_000
+
 BYTES_UP = algorithmic_bytes(M, K_UP, N_UP)
 BYTES_DN = algorithmic_bytes(M, K_DN, N_DN)
 BYTES_STEP = BYTES_UP + BYTES_DN
@@ -64,15 +70,18 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["wq", "reference"], default="wq")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration timings (C1, C3, C4, C5)")
     ap.add_argument("--pdl", type=int, default=1,
                     help="programmatic dependent launch between the GEMMs")
     ap.add_argument("--sweep", action="store_true",
                     help="time every benchmark GEMM shape and print a table "
                          "(one JSON object per shape) instead of the bench line")
     ap.add_argument("--regime", type=int, default=-1,
-                    help="with --sweep: run every GEMM on one kernel family "
-                         "(0 warp-MMA small-M, 1 tiled tensor-core, "
-                         "2 tensor-memory small-M); -1 automatic")
+                    help="run every GEMM on one kernel family (0 warp-MMA small-M, "
+                         "1 tiled tensor-core, 2 tensor-memory small-M, 3 tensor-memory "
+                         "tiled, 4 tensor-memory small-M with overlapping launches); "
+                         "-1 automatic")
     ap.add_argument("--only", default="",
                     help="sweep: only cases whose name contains this text")
     ap.add_argument("--shape", default="",
@@ -113,21 +122,30 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-def kernel_source_hash():
+# The kernel family the headline step runs, its source files (the ncu
+# traffic figure is keyed by their hash) and its name in the launch list.
+FAMILY_SOURCES = {0: ("wq_gemm_small.cu", "wq_device.cuh"),
+                  4: ("wq_gemm_stream.cu", "wq_device.cuh", "wq_tmem_dequant.cuh",
+                      "wq_tcgen05.cuh")}
+FAMILY_KERNELS = {0: "gemm_small_kernel<4, CH> (CH = 4 up, 2 down)",
+                  4: "gemm_stream_kernel<4>"}
+
+
+def kernel_source_hash(family):
     h = hashlib.sha256()
-    for f in ("wq_gemm_small.cu", "wq_device.cuh"):
+    for f in FAMILY_SOURCES.get(family, ()):
         with open(os.path.join(ROOT, "w4a16_weight_only_wq_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_key):
+def recorded_traffic(workload_key, family):
     """DRAM bytes per launch from a committed ncu summary, if it was taken
     on the current kernel source (else None)."""
     path = os.path.join(ROOT, "profiles", "small_gemm_dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    src = kernel_source_hash()
+    src = kernel_source_hash(family)
     for line in open(path):
         parts = line.split()
         if len(parts) == 3 and not line.startswith("#") and parts[0] == src \
@@ -289,6 +307,7 @@ def run_wq(args):
             yd=torch.empty((M, N_DN), dtype=torch.bfloat16, device=dev)))
     torch.cuda.synchronize()
     wq.wq_set_programmatic_launch(bool(args.pdl))
+    wq.wq_debug_force_regime(args.regime)
 
     stream = torch.cuda.Stream(device=dev)
     sh = int(stream.cuda_stream)
@@ -344,6 +363,8 @@ def run_wq(args):
     ev1 = torch.cuda.Event(enable_timing=True)
     clocks.start()
     barrier()
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(SPIN_CYCLES)  # covers the CPU-side graph submission
     ev0.record(stream)
     for _ in range(full):
         replay(g_full)
@@ -391,6 +412,8 @@ def run_wq(args):
         replay(g)
         torch.cuda.synchronize()
         a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(SPIN_CYCLES)
         a.record(stream)
         for _ in range(5):
             replay(g)
@@ -400,6 +423,15 @@ def run_wq(args):
 
     us_up = time_single("up")
     us_dn = time_single("down")
+
+    # Every other benchmark configuration, each timed on its own (rank 0).
+    configs = {}
+    if rank == 0 and not args.no_configs:
+        from tests import synth
+        for case in synth.C1 + synth.C3 + [c for c in synth.C4 if c.kind == "codes"] + synth.C5:
+            r = time_gemm_case(wq, case, stream, sh, l2)
+            configs[case.name] = {k_: r[k_] for k_ in ("us", "GB/s", "TFLOP/s", "bound", "frac",
+                                                       "regime", "bytes")}
 
     # End to end through the API with host buffers.
     hx_up = torch.empty((M, K_UP), dtype=torch.bfloat16).pin_memory()
@@ -451,10 +483,11 @@ def run_wq(args):
     peak, peak_kind = measured_peaks()
     us_per_launch = ms_step * 1e3 / 2.0      # both launches move the same bytes
     achieved = (BYTES_STEP / 2) / (us_per_launch * 1e-6) / 1e9
+    family = wq.wq_gemm_regime(4, M, N_UP, K_UP)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak,
-                "traffic": recorded_traffic(WORKLOAD),
-                "kernel": "gemm_small_kernel<4, CH> (CH = 4 up, 2 down)",
+                "traffic": recorded_traffic(WORKLOAD, family),
+                "kernel": FAMILY_KERNELS.get(family, f"kernel family {family}"),
                 "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
                 "bytes_per_launch": BYTES_STEP // 2}
 
@@ -468,7 +501,8 @@ def run_wq(args):
                    "l2": f"inputs rotated over {reps} buffer sets "
                          f"({reps * BYTES_STEP / 2**20:.0f} MiB > 2 x L2)",
                    "timing": f"CUDA graph of {S} steps replayed, events on the "
-                             "launching stream",
+                             "launching stream; a 0.1 ms spin queued before the start "
+                             "event covers the CPU-side graph submission",
                    "pdl": bool(args.pdl), "parallelism": f"replicas x{world}"},
         "us_per_call": us_per_launch,
         "us_per_call_isolated": {"up": us_up, "down": us_dn},
@@ -478,6 +512,7 @@ def run_wq(args):
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": n_e2e,
                 "ms_per_step": t_e2e / n_e2e * 1e3},
+        "configs": configs,
         "gpu_launches": 2 * args.steps,
         "clocks": dict(csum or {}, note=clock_note),
     }
@@ -493,6 +528,88 @@ def run_wq(args):
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def measured_tflops():
+    """Dense bf16 tensor peak (burst) of this machine's GPUs, TFLOP/s."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:  # noqa: BLE001
+        return 1900.0, "fallback"
+
+
+def time_gemm_case(wq, case, stream, sh, l2, max_calls=200):
+    """Device time of one GEMM shape: a CUDA graph of calls replayed with
+    events on the launching stream, the inputs rotated over enough copies
+    (> 2 x L2) that every call reads its weights from HBM.  Returns a dict
+    with µs per call, GB/s, TFLOP/s, the kernel family and the fraction of
+    the roofline that binds (HBM for memory-bound shapes, dense bf16 for
+    the rest)."""
+    import torch
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = case.draw()
+    bits, m, k, n = case.bits, case.M, case.K, case.N
+    q = torch.from_numpy(d["q"]).to(dev)
+    wp = wq.pack_codes(q, bits)
+    sc = torch.from_numpy(d["s"].view(np.int16)).view(torch.bfloat16).to(dev)
+    x = torch.from_numpy(d["X"].view(np.int16)).view(torch.bfloat16).to(dev)
+    nbytes = algorithmic_bytes(m, k, n, bits)
+    reps = max(2, math.ceil(2.0 * l2 / nbytes) + 1)
+    if reps * nbytes > 8 * 2**30:
+        reps = 2
+    bufs = [(x.clone(), wp.clone(), sc.clone(),
+             torch.empty((m, n), dtype=torch.bfloat16, device=dev))
+            for _ in range(reps)]
+    fn = wq.wq_gemm_w4a16 if bits == 4 else wq.wq_gemm_w8a16
+
+    def call(i):
+        xb, wb, sb, yb = bufs[i % reps]
+        st = fn(xb.data_ptr(), wb.data_ptr(), sb.data_ptr(), yb.data_ptr(), m, n, k, GROUP, sh)
+        if st != 0:
+            raise RuntimeError(wq.status_string(st))
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            call(i)
+    stream.synchronize()
+    per_graph = reps * max(1, min(max_calls, int(2e9 / max(nbytes, 1))) // reps)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(per_graph):
+            call(i)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    nrep = 5
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(SPIN_CYCLES)  # the graph is submitted while this runs
+        a.record(stream)
+        for _ in range(nrep):
+            g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / (nrep * per_graph)
+    flops = 2.0 * m * n * k
+    peak, peak_kind = measured_peaks()
+    tpeak, tpeak_kind = measured_tflops()
+    gbs = nbytes / us / 1e3
+    tfs = flops / us / 1e6
+    # the bound that the shape's arithmetic intensity selects
+    tensor_bound = flops / (tpeak * 1e12) > nbytes / (peak * 1e9)
+    res = {"case": case.name, "bits": bits, "M": m, "K": k, "N": n,
+           "regime": wq.wq_gemm_regime(bits, m, n, k), "us": us, "GB/s": gbs,
+           "TFLOP/s": tfs, "hbm_frac": gbs / peak, "peak_source": peak_kind,
+           "bound": "tensor" if tensor_bound else "hbm",
+           "frac": (tfs / tpeak) if tensor_bound else (gbs / peak),
+           "bytes": nbytes, "rotation": reps}
+    del bufs, g
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_sweep(args):
@@ -519,60 +636,7 @@ def run_sweep(args):
         cases = [synth.GemmCase(f"shape_w{b_}_m{m_}_{k_}x{n_}", m_, k_, n_, b_, 9)]
     cases = [c for c in cases if args.only in c.name]
     for case in cases:
-        d = case.draw()
-        bits, m, k, n = case.bits, case.M, case.K, case.N
-        q = torch.from_numpy(d["q"]).to(dev)
-        wp = wq.pack_codes(q, bits)
-        sc = torch.from_numpy(d["s"].view(np.int16)).view(torch.bfloat16).to(dev)
-        x = torch.from_numpy(d["X"].view(np.int16)).view(torch.bfloat16).to(dev)
-        nbytes = algorithmic_bytes(m, k, n, bits)
-        reps = max(2, math.ceil(2.0 * l2 / nbytes) + 1)
-        if reps * nbytes > 8 * 2**30:
-            reps = 2
-        bufs = [(x.clone(), wp.clone(), sc.clone(),
-                 torch.empty((m, n), dtype=torch.bfloat16, device=dev))
-                for _ in range(reps)]
-        fn = wq.wq_gemm_w4a16 if bits == 4 else wq.wq_gemm_w8a16
-
-        def call(i):
-            xb, wb, sb, yb = bufs[i % reps]
-            st = fn(xb.data_ptr(), wb.data_ptr(), sb.data_ptr(), yb.data_ptr(),
-                    m, n, k, GROUP, sh)
-            if st != 0:
-                raise RuntimeError(wq.status_string(st))
-
-        with torch.cuda.stream(stream):
-            for i in range(3):
-                call(i)
-        stream.synchronize()
-        per_graph = reps * max(1, min(200, int(2e9 / max(nbytes, 1))) // reps)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(per_graph):
-                call(i)
-        with torch.cuda.stream(stream):
-            g.replay()
-        torch.cuda.synchronize()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        nrep = 5
-        with torch.cuda.stream(stream):
-            a.record(stream)
-            for _ in range(nrep):
-                g.replay()
-            b.record(stream)
-        torch.cuda.synchronize()
-        us = a.elapsed_time(b) * 1e3 / (nrep * per_graph)
-        flops = 2.0 * m * n * k
-        gbs = nbytes / us / 1e3
-        print(json.dumps({
-            "case": case.name, "bits": bits, "M": m, "K": k, "N": n,
-            "regime": wq.wq_gemm_regime(bits, m, n, k), "us": us,
-            "GB/s": gbs, "TFLOP/s": flops / us / 1e6,
-            "hbm_frac": gbs / peak, "peak_source": peak_kind,
-            "bytes": nbytes, "rotation": reps}), flush=True)
-        del bufs, g
-        torch.cuda.empty_cache()
+        print(json.dumps(time_gemm_case(wq, case, stream, sh, l2)), flush=True)
     if not args.shape and args.only in "c2_mlp_fused":
         sweep_mlp_pair(wq, synth, stream, sh, l2, peak, peak_kind)
     if not args.shape:

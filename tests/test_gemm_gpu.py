@@ -225,6 +225,31 @@ def test_workload_prefill_sampled_rows(wq, case):
     _run_codes_case(wq, d["X"], d["q"], d["s"], case.bits, rows=rows)
 
 
+@pytest.mark.parametrize("case", synth.C5, ids=_case_ids(synth.C5))
+def test_workload_prefill_full(wq, case):
+    """M = 8192 in full: every one of the 8192 x 9728 outputs against the
+    oracle, on the default kernel (weights in tensor memory, 256-column
+    tiles, persistent tile scheduler over 64 x 38 tiles) and on the tiled
+    kernel with the weights in shared memory."""
+    d = case.draw()
+    K, N = case.K, case.N
+    Wp = wq.pack_codes(i8_to_dev(d["q"]), case.bits)
+    Xt, st = bf16_to_dev(d["X"]), bf16_to_dev(d["s"])
+    assert wq.wq_gemm_regime(case.bits, case.M, N, K) == 3
+    Y3 = _gemm(wq, case.bits, Xt, Wp, st)
+    try:
+        wq.wq_debug_force_regime(1)
+        Y1 = _gemm(wq, case.bits, Xt, Wp, st)
+    finally:
+        wq.wq_debug_force_regime(-1)
+    torch.cuda.synchronize()
+    p_ref = oracle.pack(d["q"], case.bits)
+    assert np.array_equal(words_to_host(Wp), p_ref)
+    Yref = oracle.gemm(d["X"], p_ref, d["s"], K, N, case.bits)
+    assert_close_to_oracle(Y3, Yref, case.name + " (weights in tensor memory)")
+    assert_close_to_oracle(Y1, Yref, case.name + " (weights in shared memory)")
+
+
 # --------------------------------------------- the tensor-core (tcgen05) path ---
 @pytest.fixture
 def tc_regime(wq):
@@ -552,7 +577,7 @@ def _chain_weights(wq, bits, L, K, seed):
 
 
 @pytest.mark.parametrize("bits", [4, 8])
-def test_stream_chain_reads_the_preceding_output(wq, bits):
+def test_stream_chain_reads_the_preceding_output(wq, stream_regime, bits):
     """Eight GEMMs on one stream with programmatic launch on, each reading
     the previous one's output as X: the launches overlap, so each must still
     see its predecessor's complete result.  Every step is checked against
@@ -581,7 +606,7 @@ def test_stream_chain_reads_the_preceding_output(wq, bits):
 
 
 @pytest.mark.parametrize("bits", [4, 8])
-def test_stream_ping_pong_matches_serial_launches(wq, bits):
+def test_stream_ping_pong_matches_serial_launches(wq, stream_regime, bits):
     """The same chain through two ping-pong buffers, so each launch also
     overwrites the buffer its predecessor read: with programmatic launch the
     bits equal those of launches that do not overlap."""

@@ -92,6 +92,18 @@ int sm_count_or_default() {
   return 152;
 }
 
+// The current device if it is an sm_103 GPU, else -1 (host-side queries).
+int current_sm103() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  return major * 10 + minor == 103 ? dev : -1;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 wq_status check_kn(int64_t K, int64_t N) {
@@ -160,7 +172,7 @@ wq_status gemm_run(int bits, const void* X, const uint32_t* Wp, const void* scal
   a.weights_in_l2 = weights_in_l2 ? 1 : 0;
   a.diag = diag_for(d);
   int regime = pick_regime(M);
-  if (regime == 4 && !wq::gemm_stream_fits(bits, K, N, a.split_hint, d.num_sms)) regime = 0;
+  if (regime == 4 && !wq::gemm_stream_fits(bits, K, N, a.split_hint, d.num_sms, dev)) regime = 0;
   if (regime == 0 && !wq::gemm_small_fits(bits, K, N, a.split_hint, d.num_sms)) regime = 1;
   if (regime == 3 && !wq::gemm_wt_fits(bits, M, K, N)) regime = 1;
   if (regime == 3) {
@@ -453,7 +465,8 @@ int wq_gemm_regime(int bits, int64_t M, int64_t N, int64_t K) {
   if ((bits != 4 && bits != 8) || M < 0 || check_kn(K, N) != WQ_OK) return -1;
   int r = pick_regime(M);
   const int sms = sm_count_or_default();
-  if (r == 4 && !wq::gemm_stream_fits(bits, K, N, g_split_hint.load(), sms)) r = 0;
+  if (r == 4 && !wq::gemm_stream_fits(bits, K, N, g_split_hint.load(), sms, current_sm103()))
+    r = 0;
   if (r == 2 && !wq::gemm_skinny_fits(bits, K, N)) r = 0;
   // shapes whose X slice does not fit the small-M kernel run on the tiled one
   if (r == 0 && !wq::gemm_small_fits(bits, K, N, g_split_hint.load(), sms)) r = 1;

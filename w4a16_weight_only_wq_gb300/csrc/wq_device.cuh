@@ -224,6 +224,25 @@ __device__ __forceinline__ void dsmem_st_async_v4_f32(uint32_t cluster_addr, uin
       : "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from this CTA's shared memory to shared memory of a CTA of the cluster,
+// counted as transaction bytes on that CTA's mbarrier `cluster_bar` (the
+// destination and the barrier as mapped by dsmem_map).
+__device__ __forceinline__ void dsmem_bulk_copy(uint32_t cluster_dst, uint32_t src_smem,
+                                                uint32_t bytes, uint32_t cluster_bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(cluster_dst),
+      "r"(src_smem), "r"(bytes), "r"(cluster_bar)
+      : "memory");
+}
+
+// Barrier among the `nthreads` threads (whole warps) that use named barrier
+// `id` (1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ void dsmem_st_f32(uint32_t cluster_addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
 }

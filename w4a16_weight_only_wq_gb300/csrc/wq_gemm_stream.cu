@@ -11,7 +11,7 @@
 // At M = 16 a call is bound by streaming the packed weights, and a lone
 // launch cannot keep HBM busy: it starts, waits for its first bytes, and
 // ends with a reduction while no weight bytes move.  So a CTA here takes
-// under half an SM (448 threads, ~108 KiB of shared memory, 256 TMEM
+// under half an SM (384 threads, ~108 KiB of shared memory, 256 TMEM
 // columns) and the next launch on the stream, started early by programmatic
 // dependent launch, shares the SM with it: while this launch multiplies and
 // reduces, the next one streams its weights into shared memory and
@@ -27,14 +27,19 @@
 //    cells of each group (one TMA per group, both 64-column cells, 128-byte
 //    swizzle) into a ring, and an L2 prefetch of the groups beyond the ring,
 //    all before the programmatic-launch wait.
-//  * Dequant (warps 6-13, two per TMEM lane quadrant, each half a group):
+//  * Dequant (warps 4-11, two per TMEM lane quadrant, each half a group):
 //    LOP3 extraction, an exact bf16x2 subtraction of the offset and one
-//    bf16x2 multiply by the scale give bf16(s*q), stored with tcgen05.st.
-//  * MMA (warp 1, warp-uniform, elect.sync issue): waits for the preceding
-//    kernel, lets the next launch start, loads X per group (TMA) and issues
-//    eight 128x16x16 MMAs per group into the accumulator.
-//  * Epilogue (warps 2-5): tcgen05.ld of the accumulator, then Y or the
-//    cluster reduction.
+//    bf16x2 multiply by the scale give bf16(s*q), stored with tcgen05.st
+//    into one of three A slots (group u into slot u % 3).
+//  * MMA (warps 1-3, warp-uniform, elect.sync issue): warp 1 + s takes the
+//    groups of A slot s and accumulates them in its own TMEM accumulator,
+//    so three issue chains run side by side (one warp issuing 128x16x16
+//    MMAs and waiting on its barriers cannot keep up with the dequant).
+//    Warp 1 also waits for the preceding kernel, lets the next launch start
+//    and requests X (one TMA per group).
+//  * Epilogue (warps 0-3 once their roles are done): tcgen05.ld of the three
+//    accumulators, added in a fixed order, then Y or the cluster
+//    reduction.
 //  Every wait is bounded; an abort drains copies and MMAs, completes the
 //  cluster exchange and frees TMEM.
 #include <cuda.h>
@@ -54,19 +59,19 @@ namespace {
 
 constexpr int kTok = 16;             // tokens (MMA N)
 constexpr int kCols = 128;           // weight columns per CTA (MMA M, TMEM lanes)
-constexpr int kGA = 3;               // groups of A in tensor memory
+constexpr int kGA = 3;               // groups of A in tensor memory = MMA warps
 constexpr uint32_t kTmemCols = 256;  // half of an SM's tensor memory
-constexpr int kACol = 64;            // A slots: TMEM columns 64..255
+constexpr int kACol = 64;            // A slots: TMEM columns 64..255; accumulators 0..47
 constexpr int kXG = 8;               // X ring: groups of 16 tokens x 128 k
 constexpr int kXGroupBytes = kTok * 128 * 2;  // 4 KiB: two 64-deep blocks
 constexpr int kXBlockBytes = kTok * 128;      // 2 KiB: 16 rows x 128 bytes
 constexpr int kMaxGroups = 32;       // groups per CTA (the scales buffer)
-constexpr int kPartStride = 20;      // floats per partial column (16 + pad)
 constexpr int kMaxSplit = 8;
-constexpr int kPartBytes = 10752;    // >= max over cs of cs * ceil(128/cs) * 80
-constexpr int kProducerWarp = 0, kMmaWarp = 1, kFirstEpiWarp = 2, kFirstDqWarp = 6;
+constexpr int kPartBytes = 9216;     // >= max over cs of cs * ceil(128/cs) * 64
+constexpr int kProducerWarp = 0, kMmaWarp = 1, kEpiWarps = 4, kFirstDqWarp = 4;
 constexpr int kDqWarps = 8;
-constexpr int kThreads = (kFirstDqWarp + kDqWarps) * 32;  // 448
+constexpr uint32_t kMmaWaitHintNs = 1000;  // suspend hint of the MMA warps' waits
+constexpr int kThreads = (kFirstDqWarp + kDqWarps) * 32;  // 384
 
 template <int BITS>
 struct StCfg {
@@ -80,7 +85,10 @@ struct StCfg {
   static constexpr int kOffP = kOffS + kMaxGroups * kCols * 2;
   static constexpr int kOffBar = kOffP + kPartBytes;
   static constexpr int kNumBars = 2 * kRing + 2 * kXG + 2 * kGA + 4;
-  static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
+  // after the barriers: the TMEM address word and the abort flag (16 bytes),
+  // then [kXG] the last group requested per X stage
+  static constexpr int kOffXLast = kOffBar + kNumBars * 8 + 16;
+  static constexpr int kSmem = kOffXLast + kXG * 4 + 1024;  // + alignment slack
   static_assert(kSmem <= 113 * 1024, "two CTAs must fit one SM");
 };
 
@@ -127,6 +135,7 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
   uint64_t* never_bar = part_full + 1;  // test hook
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* x_last = reinterpret_cast<int*>(smem + C::kOffXLast);  // [kXG] for the drain
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cs = p.cs;
@@ -145,13 +154,14 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
     for (int i = 0; i < kXG; ++i) {
       mbar_init(&x_full[i], 1);
       mbar_init(&x_empty[i], 1);
+      x_last[i] = -1;
     }
     for (int i = 0; i < kGA; ++i) {
       mbar_init(&a_full[i], kDqWarps);
       mbar_init(&a_empty[i], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(d_full, 1);
+    mbar_init(d_full, kGA);  // one commit per MMA warp
     mbar_init(part_full, 1);
     mbar_init(never_bar, 1);
     *abort_flag = 0;
@@ -170,12 +180,11 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
   const uint32_t tmem_base = *tmem_slot;
   if (p.diag.force_timeout == 1) mbar_wait_bounded(never_bar, 0, p.diag);
 
-  int issued_w = 0, issued_x = 0;
+  int issued_w = 0;
   if (warp == kProducerWarp) {
     // ------------------------------------------------------- producer ---
     // Weights and scales do not depend on the preceding kernel: everything
     // here may run before it completes.
-    bool ok = true;
     if (lane == 0) {
       prefetch_tensor_map(&tmw);
       prefetch_tensor_map(&tms);
@@ -197,75 +206,91 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
                            static_cast<uint32_t>((ng - kRing) * C::kCellBytes));
         }
       }
-      for (int c = kRing; c < ng && ok; ++c) {
-        const int slot = c % kRing;
-        ok = role_wait(&w_empty[slot], ((c / kRing) - 1) & 1, p.diag, abort_flag);
-        if (ok) {
-          mbar_arrive_expect_tx(&w_full[slot], C::kWBytes);
-          tma_load_3d(smem + C::kOffW + slot * C::kWBytes, &tmw, 0, (g0 + c) * C::kCellRows,
-                      2 * tile, &w_full[slot]);
-          issued_w = c + 1;
+      int slot = 0;
+      uint32_t ph = 0;  // phase of the slot's previous use
+      for (int c = kRing; c < ng; ++c) {
+        if (!role_wait(&w_empty[slot], ph, p.diag, abort_flag, 2000)) break;
+        mbar_arrive_expect_tx(&w_full[slot], C::kWBytes);
+        tma_load_3d(smem + C::kOffW + slot * C::kWBytes, &tmw, 0, (g0 + c) * C::kCellRows,
+                    2 * tile, &w_full[slot]);
+        issued_w = c + 1;
+        if (++slot == kRing) {
+          slot = 0;
+          ph ^= 1u;
         }
       }
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------- MMA issuer ---
-    if (p.prefetch_x && lane < rows) {
-      // X rows of this CTA's K range into L2: harmless before the wait (a
-      // prefetch changes no data) and it hides HBM latency when X is cold
-      prefetch_l2_bulk(p.X + (static_cast<size_t>(lane) * p.G + g0) * 256,
-                       static_cast<uint32_t>(ng) * 256);
-    }
-    if (lane == 0) prefetch_tensor_map(&tmx);
-    pdl_wait_primary();     // X may be the preceding kernel's output
-    pdl_launch_dependents(); // the next launch may start streaming its weights
+  } else if (warp < kMmaWarp + kGA) {
+    // --------------------------------------------------- MMA issuers ---
+    // Warp kMmaWarp + w takes the groups u = w, w + 3, ... (A slot w) into
+    // its own accumulator (TMEM columns 16 w .. 16 w + 15).
+    const int w = warp - kMmaWarp;
     auto issue_x = [&](int u) {
       if (elect_one()) {
-        const int xs = u % kXG;
+        const int xs = u & (kXG - 1);
         mbar_arrive_expect_tx(&x_full[xs], kXGroupBytes);
         tma_load_3d(smem + C::kOffX + xs * kXGroupBytes, &tmx, 0, 0, 2 * (g0 + u), &x_full[xs]);
+        x_last[xs] = u;
       }
       __syncwarp();
     };
-    for (int u = 0; u < min(kXG, ng); ++u) issue_x(u);
-    issued_x = min(kXG, ng);
+    if (w == 0) {
+      if (p.prefetch_x && lane < rows) {
+        // X rows of this CTA's K range into L2: harmless before the wait (a
+        // prefetch changes no data) and it hides HBM latency when X is cold
+        prefetch_l2_bulk(p.X + (static_cast<size_t>(lane) * p.G + g0) * 256,
+                         static_cast<uint32_t>(ng) * 256);
+      }
+      if (lane == 0) prefetch_tensor_map(&tmx);
+      pdl_wait_primary();       // X may be the preceding kernel's output
+      pdl_launch_dependents();  // the next launch may start streaming its weights
+      for (int u = 0; u < min(kXG, ng); ++u) issue_x(u);
+    }
     constexpr uint32_t idesc = idesc_bf16_f32(kCols, kTok);
-    const uint32_t xbase = smem_addr(smem + C::kOffX);
-    for (int u = 0; u < ng; ++u) {
-      const int as = u % kGA, xs = u % kXG;
+    const uint64_t xdesc0 = smem_desc_sw128(smem_addr(smem + C::kOffX));
+    const uint32_t a_tmem = tmem_base + kACol + w * 64;
+    const uint32_t d_tmem = tmem_base + 16 * w;
+    uint32_t aph = 0;
+    for (int u = w, it = 0; u < ng; u += kGA, ++it) {
+      const int xs = u & (kXG - 1);
       const bool hook = p.diag.force_timeout == 2 && u == ng / 2;
-      if (!role_wait(hook ? never_bar : &a_full[as], hook ? 0u : (u / kGA) & 1, p.diag,
-                     abort_flag) ||
-          !role_wait(&x_full[xs], (u / kXG) & 1, p.diag, abort_flag))
+      // (the waits suspend the warp instead of spinning: the next launch's
+      // MMA warps wait here for microseconds while this SM's other CTA
+      // dequantises)
+      if (!role_wait(hook ? never_bar : &a_full[w], hook ? 0u : aph, p.diag, abort_flag,
+                     kMmaWaitHintNs) ||
+          !role_wait(&x_full[xs], (u / kXG) & 1, p.diag, abort_flag, kMmaWaitHintNs))
         break;
       tc_fence_after();
-      const uint32_t a_tmem = tmem_base + kACol + as * 64;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint64_t b_desc =
-            smem_desc_sw128(xbase + xs * kXGroupBytes + (j >> 2) * kXBlockBytes) + 2 * (j & 3);
-        if (elect_one()) umma_bf16_ts(tmem_base, a_tmem + 8 * j, b_desc, idesc, (u | j) != 0);
-        __syncwarp();
-      }
+      const uint64_t bd = xdesc0 + static_cast<uint64_t>(xs * (kXGroupBytes >> 4));
+      // one elected thread issues the group's eight MMAs and both commits (a
+      // probe: 173 cycles per group this way, 322 with an election per MMA)
       if (elect_one()) {
-        umma_commit(&a_empty[as]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          umma_bf16_ts(d_tmem, a_tmem + 8 * j,
+                       bd + static_cast<uint64_t>((j >> 2) * (kXBlockBytes >> 4) + 2 * (j & 3)),
+                       idesc, (it | j) != 0);
+        umma_commit(&a_empty[w]);
         umma_commit(&x_empty[xs]);
       }
       __syncwarp();
-      // refill the X stage of the previous group, whose MMAs have most
-      // likely completed by now
-      if (u >= 1 && u - 1 + kXG < ng) {
-        const int ps = (u - 1) % kXG;
-        if (!role_wait(&x_empty[ps], ((u - 1) / kXG) & 1, p.diag, abort_flag)) break;
-        issue_x(u - 1 + kXG);
-        issued_x = u - 1 + kXG + 1;
+      aph ^= 1u;
+      // refill the X stage of this warp's previous group (whose MMAs have
+      // most likely completed) with the group kXG after it
+      const int v = u - kGA;
+      if (v >= 0 && v + kXG < ng) {
+        if (!role_wait(&x_empty[v & (kXG - 1)], (v / kXG) & 1, p.diag, abort_flag,
+                       kMmaWaitHintNs))
+          break;
+        issue_x(v + kXG);
       }
     }
-    // arrives when every MMA issued above has completed
+    // arrives when every MMA this warp issued has completed
     if (elect_one()) umma_commit(d_full);
     __syncwarp();
-  } else if (warp >= kFirstDqWarp) {
+  } else {
     // ------------------------------------------------- dequant warps ---
     // Quadrant q = warp % 4 (the TMEM lanes this warp may write); half h
     // of every group (k in [64h, 64h + 64)).
@@ -273,11 +298,12 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
     const int n = 32 * q + lane;  // weight column within the tile = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t cell_off = (n >> 6) * C::kCellBytes;
-    if (role_wait(s_full, 0, p.diag, abort_flag)) {
+    if (role_wait(s_full, 0, p.diag, abort_flag, 2000)) {
+      int slot = 0, as = 0;
+      uint32_t wph = 0, aph = 0;
       for (int u = 0; u < ng; ++u) {
-        const int slot = u % kRing, as = u % kGA;
-        if (!role_wait(&w_full[slot], (u / kRing) & 1, p.diag, abort_flag) ||
-            (u >= kGA && !role_wait(&a_empty[as], ((u / kGA) - 1) & 1, p.diag, abort_flag)))
+        if (!role_wait(&w_full[slot], wph, p.diag, abort_flag, 2000) ||
+            (u >= kGA && !role_wait(&a_empty[as], aph ^ 1u, p.diag, abort_flag, 2000)))
           break;
         tc_fence_after();
         const uint32_t s1 = sc[u * kCols + n];
@@ -286,32 +312,52 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
                                    tmem_base + lane_addr + kACol + as * 64 + 32 * h);
         tmem_st_wait();
         tc_fence_before();
-        fence_proxy_async_smem();  // our reads of the slot precede its refill
+        // (the slot was only read here; the barrier hand-off orders those
+        // reads before the producer's refill)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&a_full[as]);
           mbar_arrive(&w_empty[slot]);
+        }
+        if (++slot == kRing) {
+          slot = 0;
+          wph ^= 1u;
+        }
+        if (++as == kGA) {
+          as = 0;
+          aph ^= 1u;
         }
       }
     }
   }
 
   // ------------------------------------------------------- epilogue ---
-  // Accumulator D[column n][token m]: thread n of the epilogue warps holds
-  // the 16 token sums of column n.
+  // Accumulators D_w[column n][token m] (w = 0..2): thread n of warps 0-3
+  // (lane quadrant = warp) adds its column's three 16-token partials in
+  // order.
   float v[kTok];
 #pragma unroll
   for (int m = 0; m < kTok; ++m) v[m] = 0.f;
-  const bool epi = warp >= kFirstEpiWarp && warp < kFirstDqWarp;
-  const int en = 32 * (warp & 3) + lane;  // the epilogue thread's column
+  const bool epi = warp < kEpiWarps;
+  const int en = 32 * warp + lane;  // the epilogue thread's column
   if (epi) {
+    pdl_wait_primary();  // Y may be read or written by the preceding kernel
     if (role_wait(d_full, 0, p.diag, abort_flag, 200)) {
       tc_fence_after();
-      uint32_t r[16];
-      tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16), r);
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * warp) << 16);
+      // (an MMA warp with no group, when the CTA has fewer than three, left
+      // its accumulator unwritten)
+      uint32_t r0[16], r1[16], r2[16];
+      tmem_ld_32x32b_x16(taddr, r0);
+      if (ng > 1) tmem_ld_32x32b_x16(taddr + 16, r1);
+      if (ng > 2) tmem_ld_32x32b_x16(taddr + 32, r2);
       tmem_ld_wait();
 #pragma unroll
-      for (int m = 0; m < kTok; ++m) v[m] = __uint_as_float(r[m]);
+      for (int m = 0; m < kTok; ++m) {
+        v[m] = __uint_as_float(r0[m]);
+        if (ng > 1) v[m] += __uint_as_float(r1[m]);
+        if (ng > 2) v[m] += __uint_as_float(r2[m]);
+      }
     }
   }
   // Roles that ran on one lane rejoin their warp before the block-wide
@@ -332,16 +378,13 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       }
     }
     if (warp == kMmaWarp && lane == 0) {
-      for (int s = 0; s < kXG && s < issued_x; ++s) {
-        const int last = s + ((issued_x - 1 - s) / kXG) * kXG;
-        mbar_wait_bounded(&x_full[s], (last / kXG) & 1, drain);
-      }
+      for (int s = 0; s < kXG; ++s)
+        if (x_last[s] >= 0) mbar_wait_bounded(&x_full[s], (x_last[s] / kXG) & 1, drain);
       mbar_wait_bounded(d_full, 0, drain);
     }
     __syncwarp();
     __syncthreads();
   }
-  if (epi) pdl_wait_primary();  // Y may be read or written by the preceding kernel
   if (cs == 1) {
     if (epi && n0 + en < p.N) {
 #pragma unroll
@@ -350,29 +393,36 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
           p.Y[static_cast<size_t>(m) * p.N + n0 + en] = __float2bfloat16_rn(apply_act(v[m], p.act));
     }
   } else {
-    // Rank r owns the tile's columns [128 r / cs, 128 (r + 1) / cs) and
-    // receives, per source rank q, the 16 token partials of each of its
-    // columns at part[(q * slice + local column) * 20 ..] (four 16-byte
-    // remote stores per column, counted on the owner's part_full).  Every
-    // rank sends its bytes even after an abort, so every owner's count
-    // completes.
+    // Rank r owns the tile's columns [128 r / cs, 128 (r + 1) / cs).  Each
+    // CTA stages its 16 token partials per column in its (now idle) X ring,
+    // column-major, so that every owner's columns are one contiguous block,
+    // and sends each owner its block with one bulk copy counted on the
+    // owner's part_full; slice q of the owner's `part` holds rank q's
+    // block.  Measured against the alternatives: byte-counted 16-byte
+    // remote stores serialise on the owner's barrier (1.2 us more), and
+    // plain remote stores need a release/acquire cluster barrier (0.3 us
+    // more).  Every rank sends its blocks even after an abort, so every
+    // owner's count completes.
     const int slice = (kCols + cs - 1) / cs;
     const int cb0 = (rank * kCols) / cs, ncol = ((rank + 1) * kCols) / cs - cb0;
-    if (threadIdx.x == kFirstEpiWarp * 32)
+    float* stage = reinterpret_cast<float*>(smem + C::kOffX);
+    if (threadIdx.x == 0)
       mbar_arrive_expect_tx(part_full, static_cast<uint32_t>(cs * ncol * kTok * 4));
-    cluster_wait();  // every CTA of the cluster has initialised its barriers
+    cluster_wait();  // every CTA of the cluster is running (the arrive at its start)
     if (epi) {
-      int owner = (en * cs) / kCols;
-      while (owner + 1 < cs && en >= ((owner + 1) * kCols) / cs) ++owner;
-      while (en < (owner * kCols) / cs) --owner;
-      const int lc = en - (owner * kCols) / cs;
-      const uint32_t dst = dsmem_map(part + (rank * slice + lc) * kPartStride, owner);
-      const uint32_t bar = dsmem_map(part_full, owner);
+      const uint32_t dst = smem_addr(stage + en * kTok);
 #pragma unroll
       for (int i = 0; i < kTok / 4; ++i)
-        dsmem_st_async_v4_f32(dst + 16 * i, bar, v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-    }
-    if (epi) {
+        st_shared_v4(dst + 16 * i, __float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+                     __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
+      fence_proxy_async_smem();  // the bulk copies read what these threads wrote
+      named_barrier_sync(1, kEpiWarps * 32);
+      if (en < cs) {
+        const int r = en;  // one thread per destination rank
+        const int rb0 = (r * kCols) / cs, rn = ((r + 1) * kCols) / cs - rb0;
+        dsmem_bulk_copy(dsmem_map(part + rank * slice * kTok, r), smem_addr(stage + rb0 * kTok),
+                        static_cast<uint32_t>(rn * kTok * 4), dsmem_map(part_full, r));
+      }
       const int c = en;
       if (c < ncol) {
         if (!mbar_wait_bounded(part_full, 0, p.diag)) {
@@ -385,14 +435,14 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
 #pragma unroll
         for (int m = 0; m < kTok; ++m) acc[m] = 0.f;
         for (int qq = 0; qq < cs; ++qq) {
-          const uint32_t src = smem_addr(part + (qq * slice + c) * kPartStride);
+          const uint32_t src = smem_addr(part + (qq * slice + c) * kTok);
 #pragma unroll
           for (int i = 0; i < kTok / 4; ++i) {
-            const float4 w = ld_shared_v4_f32(src + 16 * i);
-            acc[4 * i] += w.x;
-            acc[4 * i + 1] += w.y;
-            acc[4 * i + 2] += w.z;
-            acc[4 * i + 3] += w.w;
+            const float4 f = ld_shared_v4_f32(src + 16 * i);
+            acc[4 * i] += f.x;
+            acc[4 * i + 1] += f.y;
+            acc[4 * i + 2] += f.z;
+            acc[4 * i + 3] += f.w;
           }
         }
         if (n0 + cb0 + c < p.N) {
@@ -404,9 +454,14 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
         }
       }
     }
-    // no CTA leaves while a peer may still store into its shared memory
+    // No CTA leaves while a peer's copy may still read or write its shared
+    // memory.  The owners have waited for all of their bytes before
+    // arriving, so every copy has completed once all have arrived; the
+    // barrier orders nothing else (relaxed: it does not wait for this CTA's
+    // Y stores to become visible).
     __syncwarp();
-    cluster_sync();
+    cluster_arrive_relaxed();
+    cluster_wait();
   }
   __syncwarp();
   tc_fence_before();
@@ -419,13 +474,21 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
 
 // ------------------------------------------------------------ host side ---
 
+// Never launched: its occupancy answers how many clusters of each size find
+// room when only one CTA fits an SM.
+__global__ void __launch_bounds__(128, 1) st_room_probe_kernel() {}
+constexpr int kProbeSmem = 160 * 1024;  // more than half of an SM
+
 // Per device: the kernel's shared-memory attributes, and for every cluster
-// size 1..8 how many clusters can be resident at once.
+// size 1..8 how many clusters fit at once in one CTA slot per SM -- the room
+// a launch finds while its neighbour holds the other slot.  (The occupancy
+// calculator counts one CTA of this kernel per SM, while two run side by
+// side, so the count is taken on the probe kernel above.)
 template <int BITS>
 struct StInit {
   std::atomic<uint64_t> done{0};
   std::mutex mu;
-  int max_clusters[64][kMaxSplit + 1] = {};
+  int room[64][kMaxSplit + 1] = {};
   cudaError_t ensure(int device, int (&out)[kMaxSplit + 1]) {
     const uint64_t bit = 1ull << (device & 63);
     if (!(done.load(std::memory_order_acquire) & bit)) {
@@ -440,11 +503,14 @@ struct StInit {
         e = cudaFuncSetAttribute(gemm_stream_kernel<BITS>,
                                  cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(st_room_probe_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kProbeSmem);
+        if (e != cudaSuccess) return e;
         for (int c = 1; c <= kMaxSplit; ++c) {
           cudaLaunchConfig_t cfg = {};
           cfg.gridDim = dim3(c);
-          cfg.blockDim = dim3(kThreads);
-          cfg.dynamicSmemBytes = StCfg<BITS>::kSmem;
+          cfg.blockDim = dim3(128);
+          cfg.dynamicSmemBytes = kProbeSmem;
           cudaLaunchAttribute at;
           at.id = cudaLaunchAttributeClusterDimension;
           at.val.clusterDim.x = c;
@@ -453,15 +519,14 @@ struct StInit {
           cfg.attrs = &at;
           cfg.numAttrs = 1;
           int n = 0;
-          if (cudaOccupancyMaxActiveClusters(&n, gemm_stream_kernel<BITS>, &cfg) != cudaSuccess)
-            n = 0;
-          max_clusters[device & 63][c] = n;
+          if (cudaOccupancyMaxActiveClusters(&n, st_room_probe_kernel, &cfg) != cudaSuccess) n = 0;
+          room[device & 63][c] = n;
         }
         cudaGetLastError();  // a refused size above is not an error of this call
         done.fetch_or(bit, std::memory_order_release);
       }
     }
-    for (int c = 0; c <= kMaxSplit; ++c) out[c] = max_clusters[device & 63][c];
+    for (int c = 0; c <= kMaxSplit; ++c) out[c] = room[device & 63][c];
     return cudaSuccess;
   }
 };
@@ -469,37 +534,60 @@ StInit<4> g_st4;
 StInit<8> g_st8;
 
 // The K split: the largest cs <= 8 (and <= the groups) whose CTAs fill at
-// most one slot per SM (the other slot is for the neighbouring launch).
-int st_split(int64_t tiles, int64_t G, int num_sms, int hint) {
+// most one slot per SM (the other slot is for the neighbouring launch) and
+// whose clusters find room in one slot per SM (room[cs], with 10% slack:
+// the neighbour's CTAs do not always sit one per SM).  Clusters that find no
+// room start only when the neighbouring launch ends (a 9728 x 2560 call with
+// 20 clusters of 7 had some CTAs start 6 us late).  room == nullptr (no
+// device to ask): the SM count alone.
+int st_split(int64_t tiles, int64_t G, int num_sms, int hint, const int* room) {
   if (hint > 0) return (hint <= kMaxSplit && hint <= G) ? hint : -1;
   int best = 1;
-  for (int cs = 1; cs <= kMaxSplit && cs <= G; ++cs)
-    if (tiles * cs <= num_sms) best = cs;
+  for (int cs = 1; cs <= kMaxSplit && cs <= G; ++cs) {
+    if (tiles * cs > num_sms) continue;
+    if (room != nullptr && cs > 1 && tiles * 10 > room[cs] * 11) continue;
+    best = cs;
+  }
   return best;
+}
+
+const int* st_caps(int bits, int device) {
+  static thread_local int caps[kMaxSplit + 1];
+  if (device < 0) return nullptr;
+  const cudaError_t e = bits == 4 ? g_st4.ensure(device, caps) : g_st8.ensure(device, caps);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return caps;
 }
 
 }  // namespace
 
-bool gemm_stream_fits(int bits, int64_t K, int64_t N, int split_hint, int num_sms) {
+int gemm_stream_split(int bits, int64_t K, int64_t N, int split_hint, int num_sms, int device) {
   const int64_t G = K / 128, tiles = (N + kCols - 1) / kCols;
-  const int cs = st_split(tiles, G, num_sms, split_hint);
-  if (cs < 1) return false;
-  if ((G + cs - 1) / cs > kMaxGroups) return false;  // the scales of a CTA's range
+  const int cs = st_split(tiles, G, num_sms, split_hint, st_caps(bits, device));
+  if (cs < 1) return -1;
+  if ((G + cs - 1) / cs > kMaxGroups) return -1;  // the scales of a CTA's range
   const int64_t cell_rows = bits == 4 ? 32 : 64;
-  return G * cell_rows < (int64_t(1) << 31) && N / 64 < (int64_t(1) << 31);
+  if (G * cell_rows >= (int64_t(1) << 31) || N / 64 >= (int64_t(1) << 31)) return -1;
+  return cs;
+}
+
+bool gemm_stream_fits(int bits, int64_t K, int64_t N, int split_hint, int num_sms, int device) {
+  return gemm_stream_split(bits, K, N, split_hint, num_sms, device) > 0;
 }
 
 cudaError_t launch_gemm_stream(const GemmArgs& a, cudaStream_t stream) {
   if (a.M > kTok || a.M < 1) return cudaErrorNotSupported;
-  if (!gemm_stream_fits(a.bits, a.K, a.N, a.split_hint, a.num_sms)) return cudaErrorNotSupported;
   TensorMapEncodeFn enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
-  int max_cl[kMaxSplit + 1];
-  cudaError_t e = a.bits == 4 ? g_st4.ensure(a.device, max_cl) : g_st8.ensure(a.device, max_cl);
+  int room[kMaxSplit + 1];
+  cudaError_t e = a.bits == 4 ? g_st4.ensure(a.device, room) : g_st8.ensure(a.device, room);
   if (e != cudaSuccess) return e;
+  const int cs = gemm_stream_split(a.bits, a.K, a.N, a.split_hint, a.num_sms, a.device);
+  if (cs < 1 || room[cs] < 1) return cudaErrorNotSupported;
   const int64_t G = a.K / 128, tiles = (a.N + kCols - 1) / kCols;
-  const int cs = st_split(tiles, G, a.num_sms, a.split_hint);
-  if (cs < 1 || max_cl[cs] < 1) return cudaErrorNotSupported;
   const int ngmax = static_cast<int>((G + cs - 1) / cs);
 
   // X as a 3-D bf16 tensor [K/64 blocks][M rows][64]; one box is a group's

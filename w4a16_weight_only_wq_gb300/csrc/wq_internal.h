@@ -61,8 +61,10 @@ bool gemm_skinny_fits(int bits, int64_t K, int64_t N);
 
 // Tensor-memory GEMM for M <= 16 whose CTAs take half an SM, so that
 // consecutive launches overlap (wq_gemm_stream.cu).
+// device < 0: no device to query, the split follows the SM count alone.
 cudaError_t launch_gemm_stream(const GemmArgs& a, cudaStream_t stream);
-bool gemm_stream_fits(int bits, int64_t K, int64_t N, int split_hint, int num_sms);
+bool gemm_stream_fits(int bits, int64_t K, int64_t N, int split_hint, int num_sms, int device);
+int gemm_stream_split(int bits, int64_t K, int64_t N, int split_hint, int num_sms, int device);
 
 // Tensor-core GEMM for large M, dequantised weights staged in shared
 // memory (wq_gemm_tc.cu).
