@@ -68,6 +68,19 @@ struct SmallParams {
   KernelDiag diag;
 };
 
+// Four adjacent outputs as bf16.  The activation is chosen once here rather
+// than per value inside the store: as a per-value select the compiler
+// evaluated SiLU for every output even when none was asked for.
+__device__ __forceinline__ void store4(__nv_bfloat16* y, float4 v, int act) {
+  if (act != 0) {
+    v.x = apply_act(v.x, 1);
+    v.y = apply_act(v.y, 1);
+    v.z = apply_act(v.z, 1);
+    v.w = apply_act(v.w, 1);
+  }
+  st_global_v2(y, pack_bf16x2_rn(v.x, v.y), pack_bf16x2_rn(v.z, v.w));
+}
+
 // Shared memory: [weight ring | CTA reduction][X rows][part][barriers]
 __host__ __device__ constexpr int wregion_bytes(int wslots, int slot) {
   return wslots * slot > kRedBytes ? wslots * slot : kRedBytes;
@@ -370,9 +383,7 @@ gemm_small_kernel(const SmallParams p) {
       v.w += w.w;
     }
     if (cs == 1) {
-      st_global_v2(p.Y + static_cast<size_t>(r) * p.N + tile * 64 + c,
-                   pack_bf16x2_rn(apply_act(v.x, p.act), apply_act(v.y, p.act)),
-                   pack_bf16x2_rn(apply_act(v.z, p.act), apply_act(v.w, p.act)));
+      store4(p.Y + static_cast<size_t>(r) * p.N + tile * 64 + c, v, p.act);
     } else {
       int owner = (e * cs) / E;  // first rank whose range holds e
       while (owner + 1 < cs && e >= ((owner + 1) * E) / cs) ++owner;
@@ -401,9 +412,7 @@ gemm_small_kernel(const SmallParams p) {
       v.z += w.z;
       v.w += w.w;
     }
-    st_global_v2(p.Y + static_cast<size_t>(e >> 4) * p.N + tile * 64 + (e & 15) * 4,
-                 pack_bf16x2_rn(apply_act(v.x, p.act), apply_act(v.y, p.act)),
-                 pack_bf16x2_rn(apply_act(v.z, p.act), apply_act(v.w, p.act)));
+    store4(p.Y + static_cast<size_t>(e >> 4) * p.N + tile * 64 + (e & 15) * 4, v, p.act);
   }
 }
 

@@ -11,7 +11,7 @@
 // At M = 16 a call is bound by streaming the packed weights, and a lone
 // launch cannot keep HBM busy: it starts, waits for its first bytes, and
 // ends with a reduction while no weight bytes move.  So a CTA here takes
-// under half an SM (384 threads, ~108 KiB of shared memory, 256 TMEM
+// under half an SM (512 threads, ~108 KiB of shared memory, 256 TMEM
 // columns) and the next launch on the stream, started early by programmatic
 // dependent launch, shares the SM with it: while this launch multiplies and
 // reduces, the next one streams its weights into shared memory and
@@ -27,19 +27,26 @@
 //    cells of each group (one TMA per group, both 64-column cells, 128-byte
 //    swizzle) into a ring, and an L2 prefetch of the groups beyond the ring,
 //    all before the programmatic-launch wait.
-//  * Dequant (warps 4-11, two per TMEM lane quadrant, each half a group):
-//    LOP3 extraction, an exact bf16x2 subtraction of the offset and one
-//    bf16x2 multiply by the scale give bf16(s*q), stored with tcgen05.st
-//    into one of three A slots (group u into slot u % 3).
-//  * MMA (warps 1-3, warp-uniform, elect.sync issue): warp 1 + s takes the
-//    groups of A slot s and accumulates them in its own TMEM accumulator,
-//    so three issue chains run side by side (one warp issuing 128x16x16
-//    MMAs and waiting on its barriers cannot keep up with the dequant).
-//    Warp 1 also waits for the preceding kernel, lets the next launch start
-//    and requests X (one TMA per group).
-//  * Epilogue (warps 0-3 once their roles are done): tcgen05.ld of the three
-//    accumulators, added in a fixed order, then Y or the cluster
-//    reduction.
+//  * Three pipelines, one per group residue: pipeline w takes the groups
+//    u = w, w + 3, ... with its own dequant set, MMA warp, two half-group
+//    A slots in tensor memory (64 k x 128 columns, 32 TMEM columns each:
+//    half h of a group goes to slot 2w + h), three X stages and
+//    accumulator.  Every barrier thus has one waiting warp, which waits
+//    its phases in order (a parity wait two phases ahead would pass at
+//    once).  Only the producer's weight ring is shared.
+//  * Dequant (warps 4-15: set w = warps 4 + 4w .. 7 + 4w, one per TMEM lane
+//    quadrant): LOP3 extraction, an exact bf16x2 subtraction of the offset
+//    and one bf16x2 multiply by the scale give bf16(s*q), stored with
+//    tcgen05.st, a group as two halves so that the MMAs of one half run
+//    while the other is dequantised.
+//  * MMA (warps 1-3, warp-uniform, one elected thread issues): four
+//    128x16x16 MMAs per half group.  (Per-CTA traces: a warp needs ~650
+//    cycles around each batch of MMAs, so a single MMA warp paced the whole
+//    pipeline.)  Each warp waits for the preceding kernel before its first
+//    X request (one TMA per group); warp 1 lets the next launch start.
+//  * Epilogue (warps 0-3 once their roles are done, one per lane
+//    quadrant): tcgen05.ld of the three accumulators, added in a fixed
+//    order, then Y or the cluster reduction.
 //  Every wait is bounded; an abort drains copies and MMAs, completes the
 //  cluster exchange and frees TMEM.
 #include <cuda.h>
@@ -59,19 +66,24 @@ namespace {
 
 constexpr int kTok = 16;             // tokens (MMA N)
 constexpr int kCols = 128;           // weight columns per CTA (MMA M, TMEM lanes)
-constexpr int kGA = 3;               // groups of A in tensor memory = MMA warps
+constexpr int kHS = 6;               // half-group A slots in tensor memory
+constexpr int kMmaWarps = 3;         // MMA warps = accumulators = dequant sets
 constexpr uint32_t kTmemCols = 256;  // half of an SM's tensor memory
-constexpr int kACol = 64;            // A slots: TMEM columns 64..255; accumulators 0..47
-constexpr int kXG = 8;               // X ring: groups of 16 tokens x 128 k
+constexpr int kACol = 64;            // accumulators 0..47, A slots 64..255
+static_assert(kHS % kMmaWarps == 0, "a slot must belong to one MMA warp and one set");
+constexpr int kXPer = 3;             // X stages per pipeline (16 tokens x 128 k each)
+constexpr int kXG = 3 * kXPer;       // X stages in all
 constexpr int kXGroupBytes = kTok * 128 * 2;  // 4 KiB: two 64-deep blocks
 constexpr int kXBlockBytes = kTok * 128;      // 2 KiB: 16 rows x 128 bytes
 constexpr int kMaxGroups = 32;       // groups per CTA (the scales buffer)
 constexpr int kMaxSplit = 8;
 constexpr int kPartBytes = 9216;     // >= max over cs of cs * ceil(128/cs) * 64
-constexpr int kProducerWarp = 0, kMmaWarp = 1, kEpiWarps = 4, kFirstDqWarp = 4;
-constexpr int kDqWarps = 8;
+constexpr int kProducerWarp = 0, kMmaWarp = 1, kEpiWarps = 4;
+constexpr int kFirstDqWarp = kMmaWarp + kMmaWarps;  // 4
+constexpr int kDqSets = kMmaWarps;   // sets of four dequant warps (one per quadrant)
+constexpr int kDqWarps = 4 * kDqSets;
 constexpr uint32_t kMmaWaitHintNs = 1000;  // suspend hint of the MMA warps' waits
-constexpr int kThreads = (kFirstDqWarp + kDqWarps) * 32;  // 384
+constexpr int kThreads = (kFirstDqWarp + kDqWarps) * 32;  // 512
 
 template <int BITS>
 struct StCfg {
@@ -84,7 +96,7 @@ struct StCfg {
   static constexpr int kOffS = kOffX + kXG * kXGroupBytes;
   static constexpr int kOffP = kOffS + kMaxGroups * kCols * 2;
   static constexpr int kOffBar = kOffP + kPartBytes;
-  static constexpr int kNumBars = 2 * kRing + 2 * kXG + 2 * kGA + 4;
+  static constexpr int kNumBars = 2 * kRing + 2 * kXG + 2 * kHS + 4;
   // after the barriers: the TMEM address word and the abort flag (16 bytes),
   // then [kXG] the last group requested per X stage
   static constexpr int kOffXLast = kOffBar + kNumBars * 8 + 16;
@@ -111,6 +123,23 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+// Y[m][col] = bf16(act(v[m])) for the first `rows` tokens of one column (row
+// stride N).  The activation is chosen once, outside the stores: inside
+// them the compiler evaluated SiLU for every value even when none was
+// asked for (~2,600 cycles per column of 16).
+__device__ __forceinline__ void store_column(__nv_bfloat16* y, int N, const float (&v)[kTok],
+                                             int rows, int act) {
+  if (act == 0) {
+#pragma unroll
+    for (int m = 0; m < kTok; ++m)
+      if (m < rows) y[static_cast<size_t>(m) * N] = __float2bfloat16_rn(v[m]);
+  } else {
+#pragma unroll
+    for (int m = 0; m < kTok; ++m)
+      if (m < rows) y[static_cast<size_t>(m) * N] = __float2bfloat16_rn(apply_act(v[m], 1));
+  }
+}
+
 template <int BITS>
 __global__ void __launch_bounds__(kThreads, 2)
 gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
@@ -127,9 +156,9 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
   uint64_t* w_empty = w_full + kRing;   // [kRing] dequantised
   uint64_t* x_full = w_empty + kRing;   // [kXG] a group of X landed
   uint64_t* x_empty = x_full + kXG;     // [kXG] MMAs done with it
-  uint64_t* a_full = x_empty + kXG;     // [kGA] group of A written
-  uint64_t* a_empty = a_full + kGA;     // [kGA] MMAs done with it
-  uint64_t* s_full = a_empty + kGA;     // scales landed
+  uint64_t* a_full = x_empty + kXG;     // [kHS] half group of A written
+  uint64_t* a_empty = a_full + kHS;     // [kHS] MMAs done with it
+  uint64_t* s_full = a_empty + kHS;     // scales landed
   uint64_t* d_full = s_full + 1;        // every MMA of this CTA has completed
   uint64_t* part_full = d_full + 1;     // every rank's partials of my columns landed
   uint64_t* never_bar = part_full + 1;  // test hook
@@ -149,25 +178,25 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&w_full[i], 1);
-      mbar_init(&w_empty[i], kDqWarps);
+      mbar_init(&w_empty[i], 4);  // the four quadrant warps of the group's set
     }
     for (int i = 0; i < kXG; ++i) {
       mbar_init(&x_full[i], 1);
-      mbar_init(&x_empty[i], 1);
+      mbar_init(&x_empty[i], 1);  // the group's MMA warp
       x_last[i] = -1;
     }
-    for (int i = 0; i < kGA; ++i) {
-      mbar_init(&a_full[i], kDqWarps);
+    for (int i = 0; i < kHS; ++i) {
+      mbar_init(&a_full[i], 4);  // one dequant warp per lane quadrant
       mbar_init(&a_empty[i], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(d_full, kGA);  // one commit per MMA warp
+    mbar_init(d_full, kMmaWarps);  // one commit per MMA warp
     mbar_init(part_full, 1);
     mbar_init(never_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kProducerWarp) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -175,8 +204,12 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
   __syncthreads();
   tc_fence_after();
   // every CTA of the cluster has initialised its barriers before any remote
-  // store (matched by the wait before the partials are sent)
-  if (cs > 1) cluster_arrive_relaxed();
+  // copy; waited for here, before the weights stream, where it costs
+  // nothing (~800 cycles when waited for just before the exchange)
+  if (cs > 1) {
+    cluster_arrive_relaxed();
+    cluster_wait();
+  }
   const uint32_t tmem_base = *tmem_slot;
   if (p.diag.force_timeout == 1) mbar_wait_bounded(never_bar, 0, p.diag);
 
@@ -221,112 +254,120 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       }
     }
     __syncwarp();
-  } else if (warp < kMmaWarp + kGA) {
+  } else if (warp < kMmaWarp + kMmaWarps) {
     // --------------------------------------------------- MMA issuers ---
-    // Warp kMmaWarp + w takes the groups u = w, w + 3, ... (A slot w) into
-    // its own accumulator (TMEM columns 16 w .. 16 w + 15).
+    // Warp kMmaWarp + w takes the groups u = w, w + 3, ... (A slots 2w,
+    // 2w + 1; X stages w, w + 3, w + 6 in turn) into its own accumulator
+    // (TMEM columns 16 w .. 16 w + 15).
     const int w = warp - kMmaWarp;
-    auto issue_x = [&](int u) {
+    auto issue_x = [&](int u, int xs) {
       if (elect_one()) {
-        const int xs = u & (kXG - 1);
         mbar_arrive_expect_tx(&x_full[xs], kXGroupBytes);
         tma_load_3d(smem + C::kOffX + xs * kXGroupBytes, &tmx, 0, 0, 2 * (g0 + u), &x_full[xs]);
         x_last[xs] = u;
       }
       __syncwarp();
     };
-    if (w == 0) {
-      if (p.prefetch_x && lane < rows) {
-        // X rows of this CTA's K range into L2: harmless before the wait (a
-        // prefetch changes no data) and it hides HBM latency when X is cold
-        prefetch_l2_bulk(p.X + (static_cast<size_t>(lane) * p.G + g0) * 256,
-                         static_cast<uint32_t>(ng) * 256);
-      }
-      if (lane == 0) prefetch_tensor_map(&tmx);
-      pdl_wait_primary();       // X may be the preceding kernel's output
-      pdl_launch_dependents();  // the next launch may start streaming its weights
-      for (int u = 0; u < min(kXG, ng); ++u) issue_x(u);
+    if (w == 0 && p.prefetch_x && lane < rows) {
+      // X rows of this CTA's K range into L2: harmless before the wait (a
+      // prefetch changes no data) and it hides HBM latency when X is cold
+      prefetch_l2_bulk(p.X + (static_cast<size_t>(lane) * p.G + g0) * 256,
+                       static_cast<uint32_t>(ng) * 256);
     }
+    if (lane == 0) prefetch_tensor_map(&tmx);
+    pdl_wait_primary();  // X may be the preceding kernel's output
+    if (w == 0) pdl_launch_dependents();  // the next launch may start streaming its weights
+    for (int k = 0; k < kXPer && w + 3 * k < ng; ++k) issue_x(w + 3 * k, w + 3 * k);
     constexpr uint32_t idesc = idesc_bf16_f32(kCols, kTok);
     const uint64_t xdesc0 = smem_desc_sw128(smem_addr(smem + C::kOffX));
-    const uint32_t a_tmem = tmem_base + kACol + w * 64;
     const uint32_t d_tmem = tmem_base + 16 * w;
-    uint32_t aph = 0;
-    for (int u = w, it = 0; u < ng; u += kGA, ++it) {
-      const int xs = u & (kXG - 1);
-      const bool hook = p.diag.force_timeout == 2 && u == ng / 2;
-      // (the waits suspend the warp instead of spinning: the next launch's
-      // MMA warps wait here for microseconds while this SM's other CTA
-      // dequantises)
-      if (!role_wait(hook ? never_bar : &a_full[w], hook ? 0u : aph, p.diag, abort_flag,
-                     kMmaWaitHintNs) ||
-          !role_wait(&x_full[xs], (u / kXG) & 1, p.diag, abort_flag, kMmaWaitHintNs))
-        break;
-      tc_fence_after();
-      const uint64_t bd = xdesc0 + static_cast<uint64_t>(xs * (kXGroupBytes >> 4));
-      // one elected thread issues the group's eight MMAs and both commits (a
-      // probe: 173 cycles per group this way, 322 with an election per MMA)
-      if (elect_one()) {
+    int xk = 0;  // this group's X stage among the pipeline's kXPer
+    for (int u = w, k = 0; u < ng; u += 3, ++k) {
+      const int xs = w + 3 * xk;
+      const uint32_t xph = static_cast<uint32_t>((k / kXPer) & 1);
+      const bool hook = p.diag.force_timeout == 2 && 2 * u >= ng;
+      bool ok = true;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          umma_bf16_ts(d_tmem, a_tmem + 8 * j,
-                       bd + static_cast<uint64_t>((j >> 2) * (kXBlockBytes >> 4) + 2 * (j & 3)),
-                       idesc, (it | j) != 0);
-        umma_commit(&a_empty[w]);
-        umma_commit(&x_empty[xs]);
-      }
-      __syncwarp();
-      aph ^= 1u;
-      // refill the X stage of this warp's previous group (whose MMAs have
-      // most likely completed) with the group kXG after it
-      const int v = u - kGA;
-      if (v >= 0 && v + kXG < ng) {
-        if (!role_wait(&x_empty[v & (kXG - 1)], (v / kXG) & 1, p.diag, abort_flag,
-                       kMmaWaitHintNs))
+      for (int h = 0; h < 2; ++h) {
+        const int hs = 2 * w + h;
+        // (the waits suspend the warp instead of spinning: the next
+        // launch's MMA warps wait here for microseconds while this SM's
+        // other CTA dequantises)
+        if (!role_wait(hook ? never_bar : &a_full[hs], hook ? 0u : static_cast<uint32_t>(k & 1),
+                       p.diag, abort_flag, kMmaWaitHintNs) ||
+            (h == 0 && !role_wait(&x_full[xs], xph, p.diag, abort_flag, kMmaWaitHintNs))) {
+          ok = false;
           break;
-        issue_x(v + kXG);
+        }
+        tc_fence_after();
+        const uint32_t a_tmem = tmem_base + kACol + hs * 32;
+        // block h of the group's X stage
+        const uint64_t bd =
+            xdesc0 + static_cast<uint64_t>((xs * kXGroupBytes + h * kXBlockBytes) >> 4);
+        // one elected thread issues the half's four MMAs and the commits (a
+        // probe: ~22 cycles per MMA this way, 40 with an election per MMA)
+        if (elect_one()) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            umma_bf16_ts(d_tmem, a_tmem + 8 * j, bd + static_cast<uint64_t>(2 * j), idesc,
+                         (k | h | j) != 0);
+          umma_commit(&a_empty[hs]);
+          if (h == 1) umma_commit(&x_empty[xs]);
+        }
+        __syncwarp();
       }
+      if (!ok) break;
+      // refill the X stage of this pipeline's previous group (whose MMAs
+      // have most likely completed) with the group kXPer after it
+      if (k >= 1) {
+        const int pk = (xk + kXPer - 1) % kXPer, pu = u - 3;
+        if (pu + 3 * kXPer < ng) {
+          if (!role_wait(&x_empty[w + 3 * pk], static_cast<uint32_t>(((k - 1) / kXPer) & 1), p.diag,
+                         abort_flag, kMmaWaitHintNs))
+            break;
+          issue_x(pu + 3 * kXPer, w + 3 * pk);
+        }
+      }
+      if (++xk == kXPer) xk = 0;
     }
     // arrives when every MMA this warp issued has completed
     if (elect_one()) umma_commit(d_full);
     __syncwarp();
-  } else {
+  } else if (warp >= kFirstDqWarp) {
     // ------------------------------------------------- dequant warps ---
-    // Quadrant q = warp % 4 (the TMEM lanes this warp may write); half h
-    // of every group (k in [64h, 64h + 64)).
-    const int q = warp & 3, h = (warp - kFirstDqWarp) >> 2;
+    // Quadrant q = warp % 4 (the TMEM lanes this warp may write); set ds
+    // takes the groups u = ds, ds + 3, ..., half h into A slot 2 ds + h.
+    const int q = warp & 3, ds = (warp - kFirstDqWarp) >> 2;
     const int n = 32 * q + lane;  // weight column within the tile = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t cell_off = (n >> 6) * C::kCellBytes;
+    const LaneOffsets<BITS> lo(n & 63);  // the thread's chunk offsets, once
     if (role_wait(s_full, 0, p.diag, abort_flag, 2000)) {
-      int slot = 0, as = 0;
-      uint32_t wph = 0, aph = 0;
-      for (int u = 0; u < ng; ++u) {
-        if (!role_wait(&w_full[slot], wph, p.diag, abort_flag, 2000) ||
-            (u >= kGA && !role_wait(&a_empty[as], aph ^ 1u, p.diag, abort_flag, 2000)))
-          break;
-        tc_fence_after();
+      bool ok = true;
+      for (int u = ds, k = 0; u < ng && ok; u += 3, ++k) {
+        const int slot = u % kRing;
+        if (!role_wait(&w_full[slot], (u / kRing) & 1, p.diag, abort_flag, 2000)) break;
         const uint32_t s1 = sc[u * kCols + n];
-        dequant_half_to_tmem<BITS>(smem_addr(smem + C::kOffW + slot * C::kWBytes) + cell_off,
-                                   n & 63, h, s1 | (s1 << 16),
-                                   tmem_base + lane_addr + kACol + as * 64 + 32 * h);
-        tmem_st_wait();
-        tc_fence_before();
+        const uint32_t cell = smem_addr(smem + C::kOffW + slot * C::kWBytes) + cell_off;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int hs = 2 * ds + h;
+          if (k > 0 && !role_wait(&a_empty[hs], static_cast<uint32_t>((k - 1) & 1), p.diag,
+                                  abort_flag, 2000)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          dequant_half_to_tmem<BITS>(cell, lo, h, s1 | (s1 << 16),
+                                     tmem_base + lane_addr + kACol + hs * 32);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[hs]);
+        }
         // (the slot was only read here; the barrier hand-off orders those
         // reads before the producer's refill)
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&a_full[as]);
-          mbar_arrive(&w_empty[slot]);
-        }
-        if (++slot == kRing) {
-          slot = 0;
-          wph ^= 1u;
-        }
-        if (++as == kGA) {
-          as = 0;
-          aph ^= 1u;
-        }
+        if (ok && lane == 0) mbar_arrive(&w_empty[slot]);
       }
     }
   }
@@ -334,7 +375,8 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
   // ------------------------------------------------------- epilogue ---
   // Accumulators D_w[column n][token m] (w = 0..2): thread n of warps 0-3
   // (lane quadrant = warp) adds its column's three 16-token partials in
-  // order.
+  // order.  (A warp without a task, when the CTA has a single group, left
+  // its accumulator unwritten.)
   float v[kTok];
 #pragma unroll
   for (int m = 0; m < kTok; ++m) v[m] = 0.f;
@@ -345,18 +387,18 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
     if (role_wait(d_full, 0, p.diag, abort_flag, 200)) {
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * warp) << 16);
-      // (an MMA warp with no group, when the CTA has fewer than three, left
-      // its accumulator unwritten)
-      uint32_t r0[16], r1[16], r2[16];
+      uint32_t r0[16], r1[16];
       tmem_ld_32x32b_x16(taddr, r0);
       if (ng > 1) tmem_ld_32x32b_x16(taddr + 16, r1);
-      if (ng > 2) tmem_ld_32x32b_x16(taddr + 32, r2);
       tmem_ld_wait();
 #pragma unroll
-      for (int m = 0; m < kTok; ++m) {
-        v[m] = __uint_as_float(r0[m]);
-        if (ng > 1) v[m] += __uint_as_float(r1[m]);
-        if (ng > 2) v[m] += __uint_as_float(r2[m]);
+      for (int m = 0; m < kTok; ++m)
+        v[m] = __uint_as_float(r0[m]) + (ng > 1 ? __uint_as_float(r1[m]) : 0.f);
+      if (ng > 2) {  // pipeline 2 starts at the third group
+        tmem_ld_32x32b_x16(taddr + 32, r0);
+        tmem_ld_wait();
+#pragma unroll
+        for (int m = 0; m < kTok; ++m) v[m] += __uint_as_float(r0[m]);
       }
     }
   }
@@ -378,20 +420,17 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       }
     }
     if (warp == kMmaWarp && lane == 0) {
+      // group u sits in stage u % 3 + 3 ((u / 3) % kXPer), phase (u / 3 / kXPer) & 1
       for (int s = 0; s < kXG; ++s)
-        if (x_last[s] >= 0) mbar_wait_bounded(&x_full[s], (x_last[s] / kXG) & 1, drain);
+        if (x_last[s] >= 0)
+          mbar_wait_bounded(&x_full[s], static_cast<uint32_t>((x_last[s] / 3 / kXPer) & 1), drain);
       mbar_wait_bounded(d_full, 0, drain);
     }
     __syncwarp();
     __syncthreads();
   }
   if (cs == 1) {
-    if (epi && n0 + en < p.N) {
-#pragma unroll
-      for (int m = 0; m < kTok; ++m)
-        if (m < rows)
-          p.Y[static_cast<size_t>(m) * p.N + n0 + en] = __float2bfloat16_rn(apply_act(v[m], p.act));
-    }
+    if (epi && n0 + en < p.N) store_column(p.Y + n0 + en, p.N, v, rows, p.act);
   } else {
     // Rank r owns the tile's columns [128 r / cs, 128 (r + 1) / cs).  Each
     // CTA stages its 16 token partials per column in its (now idle) X ring,
@@ -408,7 +447,6 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
     float* stage = reinterpret_cast<float*>(smem + C::kOffX);
     if (threadIdx.x == 0)
       mbar_arrive_expect_tx(part_full, static_cast<uint32_t>(cs * ncol * kTok * 4));
-    cluster_wait();  // every CTA of the cluster is running (the arrive at its start)
     if (epi) {
       const uint32_t dst = smem_addr(stage + en * kTok);
 #pragma unroll
@@ -445,13 +483,7 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
             acc[4 * i + 3] += f.w;
           }
         }
-        if (n0 + cb0 + c < p.N) {
-#pragma unroll
-          for (int m = 0; m < kTok; ++m)
-            if (m < rows)
-              p.Y[static_cast<size_t>(m) * p.N + n0 + cb0 + c] =
-                  __float2bfloat16_rn(apply_act(acc[m], p.act));
-        }
+        if (n0 + cb0 + c < p.N) store_column(p.Y + n0 + cb0 + c, p.N, acc, rows, p.act);
       }
     }
     // No CTA leaves while a peer's copy may still read or write its shared
@@ -466,7 +498,7 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kProducerWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }

@@ -91,14 +91,30 @@ __device__ __forceinline__ uint2 ld_shared_v2_u32(uint32_t addr) {
   return v;
 }
 
-// Half h (k in [64h, 64h + 64)) of one group of this thread's column n:
-// bf16(s * q) into the 32 TMEM columns [taddr, taddr + 32) of its lane
-// (column j holds k = 64h + 2j, 64h + 2j + 1, the low half k even).  Two
-// warps of a lane quadrant split a group this way, so that a group's
-// dequantisation takes half as long as with one warp per quadrant.
+// Byte offsets of this thread's four 16-byte packed chunks within a cell
+// (after the 128-byte swizzle), for half h of the INT8 layout (h = 0 for
+// INT4, whose chunks hold both halves): loop-invariant per thread, so a
+// kernel computes them once instead of per group.
 template <int BITS>
-__device__ __forceinline__ void dequant_half_to_tmem(uint32_t cell, int n, int h, uint32_t s2,
-                                                     uint32_t taddr) {
+struct LaneOffsets {
+  uint32_t o[2][4];
+  __device__ __forceinline__ explicit LaneOffsets(int n) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int t4 = 0; t4 < 4; ++t4) o[h][t4] = wt_lane_offset<BITS>(n, BITS == 4 ? 0 : h, t4);
+  }
+};
+
+// Half h (k in [64h, 64h + 64)) of one group of this thread's column:
+// bf16(s * q) into the 32 TMEM columns [taddr, taddr + 32) of its lane
+// (column j holds k = 64h + 2j, 64h + 2j + 1, the low half k even).  The
+// work of one group is split this way between warps, so that a group's
+// dequantisation is spread over more warps.  `lo` holds the thread's
+// chunk offsets (LaneOffsets).
+template <int BITS>
+__device__ __forceinline__ void dequant_half_to_tmem(uint32_t cell, const LaneOffsets<BITS>& lo,
+                                                     int h, uint32_t s2, uint32_t taddr) {
   constexpr uint32_t kMask = 0x000F000Fu;
   constexpr uint32_t kLo = 0x43004300u;  // bf16 128
   constexpr uint32_t kHi = 0x45004500u;  // bf16 2048
@@ -107,9 +123,10 @@ __device__ __forceinline__ void dequant_half_to_tmem(uint32_t cell, int n, int h
     constexpr uint32_t kB4 = 0x43084308u;  // 136
     // lane 4c + t4 holds words kb = 0..3 (k = 32 kb + 8 t4 + 0..7) in one
     // 16-byte chunk; half h needs kb = 2h, 2h + 1, its bytes 8h .. 8h + 7
+    const uint32_t base = cell + 8 * h;
 #pragma unroll
     for (int t4 = 0; t4 < 4; ++t4) {
-      const uint2 w = ld_shared_v2_u32(cell + wt_lane_offset<4>(n, 0, t4) + 8 * h);
+      const uint2 w = ld_shared_v2_u32(base + lo.o[0][t4]);
 #pragma unroll
       for (int b = 0; b < 2; ++b) {
         const uint32_t word = b == 0 ? w.x : w.y;
@@ -126,7 +143,7 @@ __device__ __forceinline__ void dequant_half_to_tmem(uint32_t cell, int n, int h
     // k = 32 (2h + wi/2) + 8 t4 + 4 (wi & 1) + 0..3
 #pragma unroll
     for (int t4 = 0; t4 < 4; ++t4) {
-      const uint4 w = ld_shared_v4(cell + wt_lane_offset<8>(n, h, t4));
+      const uint4 w = ld_shared_v4(cell + (h ? lo.o[1][t4] : lo.o[0][t4]));
 #pragma unroll
       for (int wi = 0; wi < 4; ++wi) {
         const uint32_t word = wi == 0 ? w.x : wi == 1 ? w.y : wi == 2 ? w.z : w.w;
