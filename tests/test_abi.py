@@ -137,7 +137,9 @@ def test_regime_selection_is_host_logic(wq):
                           (4, 1, 2560, 2560), (4, 128, 2560, 9728),
                           (4, 8192, 2560, 9728)):
         assert wq.wq_gemm_regime(bits, M, N, K) in (0, 1, 3, 4)
-    assert wq.wq_gemm_regime(4, 16, 9728, 2560) == 0
+    assert wq.wq_gemm_regime(4, 16, 9728, 2560) == 4
+    # 33 groups on one column tile: more groups per CTA than kernel 4 holds
+    assert wq.wq_gemm_regime(4, 16, 128, 128 * 33 * 8) == 0
     assert wq.wq_gemm_regime(4, 128, 9728, 2560) == 3
     assert wq.wq_gemm_regime(4, 8192, 9728, 2560) == 3
     # K / 128 = 5 is not a multiple of the INT4 chunk: kernel 1 takes it

@@ -40,9 +40,9 @@ def _run_codes_case(wq, X, q, s, bits, rows=None):
 
 @pytest.fixture(params=[0, 2, 4], ids=["warpmma", "tmem", "stream"])
 def small_kernel(wq, request):
-    """Run the test on each small-M kernel: 0 the warp-MMA kernel (the
-    default for M <= 32), 2 the tensor-memory kernel, 4 the tensor-memory
-    kernel whose launches overlap."""
+    """Run the test on each small-M kernel: 0 the warp-MMA kernel, 2 the
+    tensor-memory kernel, 4 the tensor-memory kernel whose launches overlap
+    (the default for M <= 32)."""
     wq.wq_debug_force_regime(request.param)
     yield request.param
     wq.wq_debug_force_regime(-1)
@@ -102,7 +102,7 @@ def test_tmem_small_m_every_split(wq, skinny_regime, bits):
 
 
 def test_default_kernel_choice(wq):
-    for M, want in [(1, 0), (16, 0), (32, 0), (33, 3), (384, 3), (8192, 3)]:
+    for M, want in [(1, 4), (16, 4), (32, 4), (33, 3), (384, 3), (8192, 3)]:
         assert wq.wq_gemm_regime(4, M, 2560, 2560) == want
 
 
@@ -537,7 +537,7 @@ def test_stream_every_split(wq, stream_regime, bits):
 @pytest.mark.parametrize("G", [9, 30, 32])
 def test_stream_ring_refills(wq, stream_regime, bits, G):
     """One CTA per tile (split 1) walks G groups: more than the weight ring
-    (7 groups INT4, 3 INT8), the X ring (8) and the tensor-memory A slots
+    (6 groups INT4, 3 INT8), the X ring (9) and the tensor-memory A slots
     (3) hold, up to the 32 groups its scales buffer takes."""
     M, K, N = 16, 128 * G, 192
     X, q, s = synth.small_case(M, K, N, bits, seed=G + bits)

@@ -1,7 +1,8 @@
 """The fused MLP pair (wq_mlp_w4a16 / wq_mlp_w8a16) against the oracle's
 pair: H = act(bf16(X . Wu)) and Y = H . Wd, on every kernel family the
-up-projection can take (the activation in the store of the warp-MMA and
-tensor-memory tiled kernels, in a separate pass for the others)."""
+up-projection can take (the activation in the store of the warp-MMA
+small-M kernel, the overlapping-launch small-M kernel and the
+tensor-memory tiled kernel, in a separate pass for the others)."""
 import numpy as np
 import pytest
 import torch
@@ -46,8 +47,8 @@ def test_mlp_pair_workload_shape(wq, act):
 @pytest.mark.parametrize("M,K,N1,N2", [(1, 256, 128, 64), (16, 512, 256, 320),
                                        (40, 512, 256, 320), (130, 1024, 384, 192)])
 def test_mlp_pair_shapes(wq, bits, act, M, K, N1, N2):
-    """M = 1 and 16 (warp-MMA kernel), 40 and 130 (tensor-memory tiled
-    kernel, K split and ragged tiles)."""
+    """M = 1 and 16 (small-M kernel with overlapping launches), 40 and 130
+    (tensor-memory tiled kernel, K split and ragged tiles)."""
     _run_pair(wq, M, K, N1, N2, bits, act, seed=M + K + bits)
 
 

@@ -35,8 +35,10 @@ int pick_regime(int64_t M) {
   const int f = g_force_regime.load();
   if (f >= 0 && f < kNumRegimes) return f;
   // measured at K = 2560, N = 9728: kernel 3 is faster than kernel 1 at
-  // every M from 64 to 8192; kernel 1 takes the shapes kernel 3 cannot
-  return M <= kSmallMaxM ? 0 : 3;
+  // every M from 64 to 8192; kernel 1 takes the shapes kernel 3 cannot.
+  // At M <= 32, kernel 4 (whose launches overlap) beats kernel 0 on the
+  // INT4 decode shapes; kernel 0 takes what kernel 4 cannot.
+  return M <= kSmallMaxM ? 4 : 3;
 }
 thread_local cudaError_t t_last_cuda = cudaSuccess;
 

@@ -33,7 +33,8 @@
 //    half h of a group goes to slot 2w + h), three X stages and
 //    accumulator.  Every barrier thus has one waiting warp, which waits
 //    its phases in order (a parity wait two phases ahead would pass at
-//    once).  Only the producer's weight ring is shared.
+//    once).  The producer's weight ring is shared, but it holds a
+//    multiple of three groups, so each of its slots serves one set.
 //  * Dequant (warps 4-15: set w = warps 4 + 4w .. 7 + 4w, one per TMEM lane
 //    quadrant): LOP3 extraction, an exact bf16x2 subtraction of the offset
 //    and one bf16x2 multiply by the scale give bf16(s*q), stored with
@@ -90,7 +91,14 @@ struct StCfg {
   static constexpr int kCellBytes = BITS == 4 ? 4096 : 8192;
   static constexpr int kCellRows = kCellBytes / 128;
   static constexpr int kWBytes = 2 * kCellBytes;    // one group of both cells
-  static constexpr int kRing = BITS == 4 ? 7 : 3;   // weight groups in the ring
+  // weight groups in the ring: a multiple of the dequant sets, so that slot
+  // s only ever holds groups of set s % 3 and its w_full barrier has one
+  // waiter taking its phases in order.  (With 7 slots, a set could reach
+  // its next group in a slot while another set's earlier group there had
+  // not landed yet: its parity wait passed a phase early, and the ring's
+  // phases fell out of step.)
+  static constexpr int kRing = BITS == 4 ? 6 : 3;
+  static_assert(kRing % kMmaWarps == 0, "one dequant set per ring slot");
   static constexpr int kOffW = 0;
   static constexpr int kOffX = kOffW + kRing * kWBytes;
   static constexpr int kOffS = kOffX + kXG * kXGroupBytes;
