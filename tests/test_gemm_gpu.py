@@ -508,23 +508,28 @@ def stream_regime(wq):
 
 
 @pytest.mark.parametrize("bits", [4, 8])
-@pytest.mark.parametrize("M", [1, 7, 16, 24])
+@pytest.mark.parametrize("M", [1, 7, 16, 24, 33, 64, 100])
 @pytest.mark.parametrize("K,N", [(128, 64), (384, 192), (1280, 576), (3840, 128),
                                  (9728, 2560), (2560, 9728)])
 def test_stream_shapes(wq, stream_regime, bits, M, K, N):
     """Ragged tiles (N = 64, 192, 576 leave a half tile), one to many groups
-    per CTA, the splits the SM count picks, and M > 16 in 16-row slices."""
+    per CTA, the splits the SM count picks; 16-, 32- and 64-token launches
+    (M = 24 and 33 leave rows of the launch past M), and M = 100 as a
+    64-row slice plus a 36-row one."""
     assert wq.wq_gemm_regime(bits, M, N, K) == 4
     X, q, s = synth.small_case(M, K, N, bits, seed=M * 5 + K + N + bits)
     _run_codes_case(wq, X, q, s, bits)
 
 
 @pytest.mark.parametrize("bits", [4, 8])
-def test_stream_every_split(wq, stream_regime, bits):
+@pytest.mark.parametrize("M", [11, 50])
+def test_stream_every_split(wq, stream_regime, bits, M):
     """Each K split 1..8 of the cluster reduction: 16 groups, 3 column tiles
-    (the last one half), 11 rows."""
-    M, K, N = 11, 2048, 320
-    X, q, s = synth.small_case(M, K, N, bits, seed=67 + bits)
+    (the last one half), 11 rows (16-token launches, partials received in a
+    dedicated buffer) or 50 rows (64-token launches, partials received in
+    the weight ring after a cluster rendezvous)."""
+    K, N = 2048, 320
+    X, q, s = synth.small_case(M, K, N, bits, seed=67 + bits + M)
     try:
         for cs in range(1, 9):
             wq.wq_debug_set_split(cs)
@@ -535,12 +540,14 @@ def test_stream_every_split(wq, stream_regime, bits):
 
 @pytest.mark.parametrize("bits", [4, 8])
 @pytest.mark.parametrize("G", [9, 30, 32])
-def test_stream_ring_refills(wq, stream_regime, bits, G):
+@pytest.mark.parametrize("M", [16, 64])
+def test_stream_ring_refills(wq, stream_regime, bits, G, M):
     """One CTA per tile (split 1) walks G groups: more than the weight ring
-    (6 groups INT4, 3 INT8), the X ring (9) and the tensor-memory A slots
-    (3) hold, up to the 32 groups its scales buffer takes."""
-    M, K, N = 16, 128 * G, 192
-    X, q, s = synth.small_case(M, K, N, bits, seed=G + bits)
+    (6 groups INT4, 3 INT8), the X stages (9 at 16 tokens, 3 at 64) and the
+    tensor-memory A slots (3) hold, up to the 32 groups its scales buffer
+    takes."""
+    K, N = 128 * G, 192
+    X, q, s = synth.small_case(M, K, N, bits, seed=G + bits + M)
     try:
         wq.wq_debug_set_split(1)
         assert wq.wq_gemm_regime(bits, M, N, K) == 4
@@ -577,12 +584,14 @@ def _chain_weights(wq, bits, L, K, seed):
 
 
 @pytest.mark.parametrize("bits", [4, 8])
-def test_stream_chain_reads_the_preceding_output(wq, stream_regime, bits):
+@pytest.mark.parametrize("M", [16, 64])
+def test_stream_chain_reads_the_preceding_output(wq, stream_regime, bits, M):
     """Eight GEMMs on one stream with programmatic launch on, each reading
     the previous one's output as X: the launches overlap, so each must still
     see its predecessor's complete result.  Every step is checked against
-    the oracle run on the step's actual input."""
-    M, K, L = 16, 2560, 8
+    the oracle run on the step's actual input (16 rows: 16-token launches;
+    64 rows: 64-token launches)."""
+    K, L = 2560, 8
     ws = _chain_weights(wq, bits, L, K, seed=100 + bits)
     rng = np.random.default_rng(7)
     X0 = oracle.f32_to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
@@ -606,11 +615,12 @@ def test_stream_chain_reads_the_preceding_output(wq, stream_regime, bits):
 
 
 @pytest.mark.parametrize("bits", [4, 8])
-def test_stream_ping_pong_matches_serial_launches(wq, stream_regime, bits):
+@pytest.mark.parametrize("M", [16, 64])
+def test_stream_ping_pong_matches_serial_launches(wq, stream_regime, bits, M):
     """The same chain through two ping-pong buffers, so each launch also
     overwrites the buffer its predecessor read: with programmatic launch the
     bits equal those of launches that do not overlap."""
-    M, K, L = 16, 2560, 8
+    K, L = 2560, 8
     ws = _chain_weights(wq, bits, L, K, seed=200 + bits)
     rng = np.random.default_rng(8)
     X0 = bf16_to_dev(oracle.f32_to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32)))

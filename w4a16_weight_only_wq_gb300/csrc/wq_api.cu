@@ -36,8 +36,10 @@ int pick_regime(int64_t M) {
   if (f >= 0 && f < kNumRegimes) return f;
   // measured at K = 2560, N = 9728: kernel 3 is faster than kernel 1 at
   // every M from 64 to 8192; kernel 1 takes the shapes kernel 3 cannot.
-  // At M <= 32, kernel 4 (whose launches overlap) beats kernel 0 on the
-  // INT4 decode shapes; kernel 0 takes what kernel 4 cannot.
+  // At M <= 32, kernel 4 (whose launches overlap; one launch up to 32 rows)
+  // beats kernel 0 on the INT4 decode shapes; kernel 0 takes what kernel 4
+  // cannot.  At M = 64 kernel 3 matches or beats kernel 4's 64-token launch
+  // (12.5 against 12.2 us at 2560 x 9728, 8.3 against 10.6 at 2560 x 2560).
   return M <= kSmallMaxM ? 4 : 3;
 }
 thread_local cudaError_t t_last_cuda = cudaSuccess;
@@ -189,40 +191,60 @@ wq_status gemm_run(int bits, const void* X, const uint32_t* Wp, const void* scal
     if (e == cudaErrorNotSupported) return WQ_ERR_UNSUPPORTED;
     return cuda_status(e);
   }
-  // The small-M kernels take up to 16 rows per launch; taller inputs are
-  // processed in 16-row slices.
+  // The small-M kernels take a bounded number of rows per launch (the
+  // stream kernel 64, the others 16); taller inputs are processed in slices.
   const size_t xrow = static_cast<size_t>(K) * 2, yrow = static_cast<size_t>(N) * 2;
   // the activation is applied in the store of kernels 0 and 4; kernel 2 has none
   if (regime == 0 || regime == 4) a.act = act;
-  for (int64_t m0 = 0; m0 < M; m0 += 16) {
-    a.X = static_cast<const char*>(X) + m0 * xrow;
-    a.Y = static_cast<char*>(Y) + m0 * yrow;
-    a.M = (M - m0) < 16 ? (M - m0) : 16;
-    const bool last = m0 + 16 >= M;
-    a.l2_prefetch = last && pf != nullptr && regime == 0 ? pf : nullptr;
-    a.l2_prefetch_bytes = a.l2_prefetch != nullptr ? pf_bytes : 0;
-    cudaError_t e = cudaErrorNotSupported;
-    if (regime == 4) e = wq::launch_gemm_stream(a, stream);
-    if (regime == 2) e = wq::launch_gemm_skinny(a, stream);
-    // shapes the tensor-memory kernels cannot index go to the warp-MMA kernel
-    if (regime == 0 || e == cudaErrorNotSupported) e = wq::launch_gemm_small(a, stream);
-    if (e == cudaErrorNotSupported) {
-      // the slice does not fit the small-M kernel: the tiled kernel takes it
-      const int slice_act = a.act;
-      a.act = 0;
-      e = wq::launch_gemm_tc(a, stream);
-      if (e == cudaErrorNotSupported) return WQ_ERR_UNSUPPORTED;
-      if (e != cudaSuccess) return cuda_status(e);
-      if (slice_act != 0) {  // the caller counts on this slice being activated
-        const wq_status st2 = cuda_status(wq::launch_silu_inplace(
-            static_cast<uint16_t*>(a.Y), a.M * N, stream));
-        if (st2 != WQ_OK) return st2;
+  // rows [r0, r0 + h) on the warp-MMA kernel in 16-row slices, each slice
+  // that does not fit it on the tiled kernel
+  auto run_small = [&](int64_t r0, int64_t h, bool last_rows) -> wq_status {
+    for (int64_t m0 = r0; m0 < r0 + h; m0 += 16) {
+      wq::GemmArgs b = a;
+      b.X = static_cast<const char*>(X) + m0 * xrow;
+      b.Y = static_cast<char*>(Y) + m0 * yrow;
+      b.M = (r0 + h - m0) < 16 ? (r0 + h - m0) : 16;
+      const bool last = last_rows && m0 + 16 >= r0 + h;
+      b.l2_prefetch = last && pf != nullptr ? pf : nullptr;
+      b.l2_prefetch_bytes = b.l2_prefetch != nullptr ? pf_bytes : 0;
+      cudaError_t e = wq::launch_gemm_small(b, stream);
+      if (e == cudaErrorNotSupported) {
+        // the slice does not fit the small-M kernel: the tiled kernel takes it
+        b.act = 0;
+        e = wq::launch_gemm_tc(b, stream);
+        if (e == cudaErrorNotSupported) return WQ_ERR_UNSUPPORTED;
+        if (e != cudaSuccess) return cuda_status(e);
+        if (a.act != 0) {  // the caller counts on this slice being activated
+          const wq_status st2 = cuda_status(wq::launch_silu_inplace(
+              static_cast<uint16_t*>(b.Y), b.M * N, stream));
+          if (st2 != WQ_OK) return st2;
+        }
+        continue;
       }
-      a.act = slice_act;
-      continue;
+      if (e != cudaSuccess) return cuda_status(e);
+      if (b.l2_prefetch != nullptr) *prefetched = true;
     }
-    if (e != cudaSuccess) return cuda_status(e);
-    if (a.l2_prefetch != nullptr) *prefetched = true;
+    return WQ_OK;
+  };
+  const int64_t step = regime == 4 ? wq::kMaxStreamRows : 16;
+  for (int64_t m0 = 0; m0 < M; m0 += step) {
+    const int64_t h = (M - m0) < step ? (M - m0) : step;
+    const bool last = m0 + step >= M;
+    cudaError_t e = cudaErrorNotSupported;
+    if (regime == 4 || regime == 2) {
+      a.X = static_cast<const char*>(X) + m0 * xrow;
+      a.Y = static_cast<char*>(Y) + m0 * yrow;
+      a.M = h;
+      a.l2_prefetch = nullptr;
+      a.l2_prefetch_bytes = 0;
+      e = regime == 4 ? wq::launch_gemm_stream(a, stream) : wq::launch_gemm_skinny(a, stream);
+      if (e != cudaSuccess && e != cudaErrorNotSupported) return cuda_status(e);
+    }
+    // shapes the tensor-memory kernels cannot index go to the warp-MMA kernel
+    if (regime == 0 || e == cudaErrorNotSupported) {
+      const wq_status st = run_small(m0, h, last);
+      if (st != WQ_OK) return st;
+    }
   }
   *act_done = act == 0 || regime == 0 || regime == 4;
   return WQ_OK;

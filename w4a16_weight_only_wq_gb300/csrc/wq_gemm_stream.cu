@@ -1,5 +1,6 @@
-// wq_gemm_stream.cu -- tcgen05 W4A16 / W8A16 GEMM for M <= 16 that keeps
-// the weight stream going across consecutive launches.
+// wq_gemm_stream.cu -- tcgen05 W4A16 / W8A16 GEMM for M <= 64 (one launch
+// per 16, 32 or 64 tokens) that keeps the weight stream going across
+// consecutive launches.
 //
 // Y[M,N] = X[M,K] . (s (.) q)[K,N] for the verifier's 16-token block
 // ("Quantize the Target, Quantize the Drafter": the INT4 target checks an
@@ -45,6 +46,12 @@
 //    cycles around each batch of MMAs, so a single MMA warp paced the whole
 //    pipeline.)  Each warp waits for the preceding kernel before its first
 //    X request (one TMA per group); warp 1 lets the next launch start.
+//  * 32 and 64 tokens (M = 17..64 in one launch): the accumulator is TOK
+//    columns wide, so only one MMA pipeline fits beside the six A
+//    half-slots; warp 1 issues every group's MMAs in order, warp 2 requests
+//    X, and the epilogue works in 16-token chunks.  The cluster's partials
+//    are then received in the owners' idle weight rings, after a relaxed
+//    rendezvous.
 //  * Epilogue (warps 0-3 once their roles are done, one per lane
 //    quadrant): tcgen05.ld of the three accumulators, added in a fixed
 //    order, then Y or the cluster reduction.
@@ -65,29 +72,46 @@
 namespace wq {
 namespace {
 
-constexpr int kTok = 16;             // tokens (MMA N)
 constexpr int kCols = 128;           // weight columns per CTA (MMA M, TMEM lanes)
-constexpr int kHS = 6;               // half-group A slots in tensor memory
-constexpr int kMmaWarps = 3;         // MMA warps = accumulators = dequant sets
+constexpr int kDqSets = 3;           // sets of four dequant warps (one per quadrant)
+constexpr int kHS = 2 * kDqSets;     // half-group A slots in tensor memory, two per set
 constexpr uint32_t kTmemCols = 256;  // half of an SM's tensor memory
-constexpr int kACol = 64;            // accumulators 0..47, A slots 64..255
-static_assert(kHS % kMmaWarps == 0, "a slot must belong to one MMA warp and one set");
-constexpr int kXPer = 3;             // X stages per pipeline (16 tokens x 128 k each)
-constexpr int kXG = 3 * kXPer;       // X stages in all
-constexpr int kXGroupBytes = kTok * 128 * 2;  // 4 KiB: two 64-deep blocks
-constexpr int kXBlockBytes = kTok * 128;      // 2 KiB: 16 rows x 128 bytes
+constexpr int kACol = 64;            // accumulators below column 64, A slots 64..255
 constexpr int kMaxGroups = 32;       // groups per CTA (the scales buffer)
 constexpr int kMaxSplit = 8;
-constexpr int kPartBytes = 9216;     // >= max over cs of cs * ceil(128/cs) * 64
 constexpr int kProducerWarp = 0, kMmaWarp = 1, kEpiWarps = 4;
-constexpr int kFirstDqWarp = kMmaWarp + kMmaWarps;  // 4
-constexpr int kDqSets = kMmaWarps;   // sets of four dequant warps (one per quadrant)
+constexpr int kFirstDqWarp = 4;      // warps 1-3 issue MMAs (as many as there are pipelines)
 constexpr int kDqWarps = 4 * kDqSets;
 constexpr uint32_t kMmaWaitHintNs = 1000;  // suspend hint of the MMA warps' waits
 constexpr int kThreads = (kFirstDqWarp + kDqWarps) * 32;  // 512
+constexpr int kChunk = 16;           // tokens per epilogue chunk (16 fp32 registers)
+constexpr int kXRegion = 48 * 1024;  // X stages (and, after the MMAs, staged partials)
 
-template <int BITS>
+// TOK tokens per launch (the MMA's N: 16, 32 or 64).  At 16 there are three
+// MMA pipelines (one per dequant set, each with its own accumulator); at 32
+// and 64 one MMA warp takes every group in order, so that one accumulator of
+// TOK columns plus the six A half-slots fit 256 TMEM columns.  Either way
+// every mbarrier keeps a single waiting warp that takes its phases in order.
+template <int TOK>
+struct TokCfg {
+  static_assert(TOK == 16 || TOK == 32 || TOK == 64, "16, 32 or 64 tokens");
+  static constexpr int kPipes = TOK == 16 ? 3 : 1;
+  static_assert(kPipes * TOK <= kACol, "accumulators below the A slots");
+  static constexpr int kXGroupBytes = TOK * 256;  // a group's two 64-deep blocks
+  static constexpr int kXBlockBytes = TOK * 128;  // one block: TOK rows x 128 bytes
+  // X stages: per pipeline kXPer, in all kXG (36 / 48 / 48 KiB)
+  static constexpr int kXG = TOK == 16 ? 9 : kXRegion / kXGroupBytes;
+  static constexpr int kXPer = kXG / kPipes;
+  static_assert(kXG % kPipes == 0 && kXPer >= 2, "X stages per pipeline");
+  // 16 tokens: a dedicated buffer receives the cluster's partials at any
+  // time; 32 and 64: they are received in the idle weight ring, after a
+  // rendezvous that says every CTA of the cluster is done with its ring
+  static constexpr int kPartBytes = TOK == 16 ? 9216 : 0;  // >= cs * ceil(128/cs) * 64
+};
+
+template <int BITS, int TOK>
 struct StCfg {
+  using T = TokCfg<TOK>;
   static constexpr int kCellBytes = BITS == 4 ? 4096 : 8192;
   static constexpr int kCellRows = kCellBytes / 128;
   static constexpr int kWBytes = 2 * kCellBytes;    // one group of both cells
@@ -98,18 +122,22 @@ struct StCfg {
   // not landed yet: its parity wait passed a phase early, and the ring's
   // phases fell out of step.)
   static constexpr int kRing = BITS == 4 ? 6 : 3;
-  static_assert(kRing % kMmaWarps == 0, "one dequant set per ring slot");
+  static_assert(kRing % kDqSets == 0, "one dequant set per ring slot");
   static constexpr int kOffW = 0;
   static constexpr int kOffX = kOffW + kRing * kWBytes;
-  static constexpr int kOffS = kOffX + kXG * kXGroupBytes;
+  static constexpr int kOffS = kOffX + T::kXG * T::kXGroupBytes;
   static constexpr int kOffP = kOffS + kMaxGroups * kCols * 2;
-  static constexpr int kOffBar = kOffP + kPartBytes;
-  static constexpr int kNumBars = 2 * kRing + 2 * kXG + 2 * kHS + 4;
+  static constexpr int kOffBar = kOffP + T::kPartBytes;
+  static constexpr int kNumBars = 2 * kRing + 2 * T::kXG + 2 * kHS + 4;
   // after the barriers: the TMEM address word and the abort flag (16 bytes),
   // then [kXG] the last group requested per X stage
   static constexpr int kOffXLast = kOffBar + kNumBars * 8 + 16;
-  static constexpr int kSmem = kOffXLast + kXG * 4 + 1024;  // + alignment slack
+  static constexpr int kSmem = kOffXLast + T::kXG * 4 + 1024;  // + alignment slack
   static_assert(kSmem <= 113 * 1024, "two CTAs must fit one SM");
+  // partials: staged in the X region (128 columns x TOK); received (TOK >= 32)
+  // in the weight ring, cs slices of ceil(128 / cs) columns x TOK (<= 34 KiB)
+  static_assert(kCols * TOK * 4 <= T::kXG * T::kXGroupBytes, "staged partials fit the X stages");
+  static_assert(TOK == 16 || 7 * 19 * TOK * 4 <= kRing * kWBytes, "received partials fit the ring");
 };
 
 struct StParams {
@@ -131,29 +159,34 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
-// Y[m][col] = bf16(act(v[m])) for the first `rows` tokens of one column (row
-// stride N).  The activation is chosen once, outside the stores: inside
-// them the compiler evaluated SiLU for every value even when none was
-// asked for (~2,600 cycles per column of 16).
-__device__ __forceinline__ void store_column(__nv_bfloat16* y, int N, const float (&v)[kTok],
+// Y[m][col] = bf16(act(v[m])) for the first `rows` tokens of a 16-token chunk
+// of one column (row stride N).  The activation is chosen once, outside the
+// stores: inside them the compiler evaluated SiLU for every value even when
+// none was asked for (~2,600 cycles per column of 16).
+__device__ __forceinline__ void store_column(__nv_bfloat16* y, int N, const float (&v)[kChunk],
                                              int rows, int act) {
   if (act == 0) {
 #pragma unroll
-    for (int m = 0; m < kTok; ++m)
+    for (int m = 0; m < kChunk; ++m)
       if (m < rows) y[static_cast<size_t>(m) * N] = __float2bfloat16_rn(v[m]);
   } else {
 #pragma unroll
-    for (int m = 0; m < kTok; ++m)
+    for (int m = 0; m < kChunk; ++m)
       if (m < rows) y[static_cast<size_t>(m) * N] = __float2bfloat16_rn(apply_act(v[m], 1));
   }
 }
 
-template <int BITS>
+template <int BITS, int TOK>
 __global__ void __launch_bounds__(kThreads, 2)
 gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                    const __grid_constant__ CUtensorMap tms, const StParams p) {
-  using C = StCfg<BITS>;
+  using C = StCfg<BITS, TOK>;
+  using T = TokCfg<TOK>;
   constexpr int kRing = C::kRing;
+  constexpr int kPipes = T::kPipes, kXG = T::kXG, kXPer = T::kXPer;
+  // with one MMA pipeline, warp 2 requests X so that the MMA warp only waits
+  // and issues (with three, each MMA warp requests its own pipeline's X)
+  constexpr bool kXWarp = kPipes == 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
 
@@ -181,7 +214,7 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
   const int g0 = (p.G * rank) / cs;
   const int ng = (p.G * (rank + 1)) / cs - g0;
   const int n0 = tile * kCols;
-  const int rows = min(kTok, p.M);
+  const int rows = min(TOK, p.M);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRing; ++i) {
@@ -198,7 +231,7 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       mbar_init(&a_empty[i], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(d_full, kMmaWarps);  // one commit per MMA warp
+    mbar_init(d_full, kPipes);  // one commit per MMA warp
     mbar_init(part_full, 1);
     mbar_init(never_bar, 1);
     *abort_flag = 0;
@@ -262,47 +295,66 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       }
     }
     __syncwarp();
-  } else if (warp < kMmaWarp + kMmaWarps) {
+  } else if (warp < kMmaWarp + kPipes + (kXWarp ? 1 : 0)) {
     // --------------------------------------------------- MMA issuers ---
-    // Warp kMmaWarp + w takes the groups u = w, w + 3, ... (A slots 2w,
-    // 2w + 1; X stages w, w + 3, w + 6 in turn) into its own accumulator
-    // (TMEM columns 16 w .. 16 w + 15).
+    // Warp kMmaWarp + w (w < kPipes) takes the groups u = w, w + kPipes, ...
+    // (group u's A slots are its dequant set's, 2 (u % 3) and 2 (u % 3) + 1;
+    // its X stages w, w + kPipes, ... in turn) into its own accumulator (TMEM
+    // columns TOK w .. TOK w + TOK - 1).  With one pipeline, warp
+    // kMmaWarp + 1 requests the X stages instead of the MMA warp.
     const int w = warp - kMmaWarp;
     auto issue_x = [&](int u, int xs) {
       if (elect_one()) {
-        mbar_arrive_expect_tx(&x_full[xs], kXGroupBytes);
-        tma_load_3d(smem + C::kOffX + xs * kXGroupBytes, &tmx, 0, 0, 2 * (g0 + u), &x_full[xs]);
+        mbar_arrive_expect_tx(&x_full[xs], T::kXGroupBytes);
+        tma_load_3d(smem + C::kOffX + xs * T::kXGroupBytes, &tmx, 0, 0, 2 * (g0 + u), &x_full[xs]);
         x_last[xs] = u;
       }
       __syncwarp();
     };
-    if (w == 0 && p.prefetch_x && lane < rows) {
-      // X rows of this CTA's K range into L2: harmless before the wait (a
-      // prefetch changes no data) and it hides HBM latency when X is cold
-      prefetch_l2_bulk(p.X + (static_cast<size_t>(lane) * p.G + g0) * 256,
-                       static_cast<uint32_t>(ng) * 256);
+    const bool x_issuer = kXWarp ? w == kPipes : true;  // requests X for pipeline (kXWarp ? 0 : w)
+    if (x_issuer) {
+      if ((kXWarp || w == 0) && p.prefetch_x) {
+        // X rows of this CTA's K range into L2: harmless before the wait (a
+        // prefetch changes no data) and it hides HBM latency when X is cold
+        for (int r = lane; r < rows; r += 32)
+          prefetch_l2_bulk(p.X + (static_cast<size_t>(r) * p.G + g0) * 256,
+                           static_cast<uint32_t>(ng) * 256);
+      }
+      if (lane == 0) prefetch_tensor_map(&tmx);
+      pdl_wait_primary();  // X may be the preceding kernel's output
+      if (kXWarp || w == 0) pdl_launch_dependents();  // the next launch may stream its weights
+      const int pw = kXWarp ? 0 : w;
+      for (int k = 0; k < kXPer && pw + kPipes * k < ng; ++k)
+        issue_x(pw + kPipes * k, pw + kPipes * k);
     }
-    if (lane == 0) prefetch_tensor_map(&tmx);
-    pdl_wait_primary();  // X may be the preceding kernel's output
-    if (w == 0) pdl_launch_dependents();  // the next launch may start streaming its weights
-    for (int k = 0; k < kXPer && w + 3 * k < ng; ++k) issue_x(w + 3 * k, w + 3 * k);
-    constexpr uint32_t idesc = idesc_bf16_f32(kCols, kTok);
+    if (kXWarp && w == kPipes) {
+      // the X warp: refill stage u % kXPer with group u once group
+      // u - kXPer's MMAs are done with it
+      for (int u = kXPer; u < ng; ++u) {
+        if (!role_wait(&x_empty[u % kXPer], static_cast<uint32_t>((u / kXPer - 1) & 1), p.diag,
+                       abort_flag, kMmaWaitHintNs))
+          break;
+        issue_x(u, u % kXPer);
+      }
+    } else {
+    constexpr uint32_t idesc = idesc_bf16_f32(kCols, TOK);
     const uint64_t xdesc0 = smem_desc_sw128(smem_addr(smem + C::kOffX));
-    const uint32_t d_tmem = tmem_base + 16 * w;
+    const uint32_t d_tmem = tmem_base + TOK * w;
     int xk = 0;  // this group's X stage among the pipeline's kXPer
-    for (int u = w, k = 0; u < ng; u += 3, ++k) {
-      const int xs = w + 3 * xk;
+    for (int u = w, k = 0; u < ng; u += kPipes, ++k) {
+      const int xs = w + kPipes * xk;
       const uint32_t xph = static_cast<uint32_t>((k / kXPer) & 1);
       const bool hook = p.diag.force_timeout == 2 && 2 * u >= ng;
       bool ok = true;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int hs = 2 * w + h;
+        const int hs = 2 * (u % kDqSets) + h;
         // (the waits suspend the warp instead of spinning: the next
         // launch's MMA warps wait here for microseconds while this SM's
         // other CTA dequantises)
-        if (!role_wait(hook ? never_bar : &a_full[hs], hook ? 0u : static_cast<uint32_t>(k & 1),
-                       p.diag, abort_flag, kMmaWaitHintNs) ||
+        if (!role_wait(hook ? never_bar : &a_full[hs],
+                       hook ? 0u : static_cast<uint32_t>((u / kDqSets) & 1), p.diag, abort_flag,
+                       kMmaWaitHintNs) ||
             (h == 0 && !role_wait(&x_full[xs], xph, p.diag, abort_flag, kMmaWaitHintNs))) {
           ok = false;
           break;
@@ -311,7 +363,7 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
         const uint32_t a_tmem = tmem_base + kACol + hs * 32;
         // block h of the group's X stage
         const uint64_t bd =
-            xdesc0 + static_cast<uint64_t>((xs * kXGroupBytes + h * kXBlockBytes) >> 4);
+            xdesc0 + static_cast<uint64_t>((xs * T::kXGroupBytes + h * T::kXBlockBytes) >> 4);
         // one elected thread issues the half's four MMAs and the commits (a
         // probe: ~22 cycles per MMA this way, 40 with an election per MMA)
         if (elect_one()) {
@@ -327,13 +379,13 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       if (!ok) break;
       // refill the X stage of this pipeline's previous group (whose MMAs
       // have most likely completed) with the group kXPer after it
-      if (k >= 1) {
-        const int pk = (xk + kXPer - 1) % kXPer, pu = u - 3;
-        if (pu + 3 * kXPer < ng) {
-          if (!role_wait(&x_empty[w + 3 * pk], static_cast<uint32_t>(((k - 1) / kXPer) & 1), p.diag,
-                         abort_flag, kMmaWaitHintNs))
+      if (!kXWarp && k >= 1) {
+        const int pk = (xk + kXPer - 1) % kXPer, pu = u - kPipes;
+        if (pu + kPipes * kXPer < ng) {
+          if (!role_wait(&x_empty[w + kPipes * pk], static_cast<uint32_t>(((k - 1) / kXPer) & 1),
+                         p.diag, abort_flag, kMmaWaitHintNs))
             break;
-          issue_x(pu + 3 * kXPer, w + 3 * pk);
+          issue_x(pu + kPipes * kXPer, w + kPipes * pk);
         }
       }
       if (++xk == kXPer) xk = 0;
@@ -341,6 +393,7 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
     // arrives when every MMA this warp issued has completed
     if (elect_one()) umma_commit(d_full);
     __syncwarp();
+    }
   } else if (warp >= kFirstDqWarp) {
     // ------------------------------------------------- dequant warps ---
     // Quadrant q = warp % 4 (the TMEM lanes this warp may write); set ds
@@ -381,34 +434,49 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
   }
 
   // ------------------------------------------------------- epilogue ---
-  // Accumulators D_w[column n][token m] (w = 0..2): thread n of warps 0-3
-  // (lane quadrant = warp) adds its column's three 16-token partials in
-  // order.  (A warp without a task, when the CTA has a single group, left
-  // its accumulator unwritten.)
-  float v[kTok];
-#pragma unroll
-  for (int m = 0; m < kTok; ++m) v[m] = 0.f;
+  // Accumulators D_w[column n][token m] (w < kPipes, TMEM columns TOK w ..):
+  // thread n of warps 0-3 (lane quadrant = warp) reads its column in chunks
+  // of 16 tokens and adds the pipelines' partials in order.  (A pipeline
+  // without a group, when the CTA has fewer groups than pipelines, left its
+  // accumulator unwritten.)
   const bool epi = warp < kEpiWarps;
   const int en = 32 * warp + lane;  // the epilogue thread's column
+  bool have = false;
   if (epi) {
     pdl_wait_primary();  // Y may be read or written by the preceding kernel
-    if (role_wait(d_full, 0, p.diag, abort_flag, 200)) {
-      tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * warp) << 16);
-      uint32_t r0[16], r1[16];
+    have = role_wait(d_full, 0, p.diag, abort_flag, 200);
+  }
+  auto load_chunk = [&](int c, float (&v)[kChunk]) {
+#pragma unroll
+    for (int m = 0; m < kChunk; ++m) v[m] = 0.f;
+    if (!have) return;
+    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * warp) << 16) + kChunk * c;
+    if constexpr (kPipes == 3) {
+      uint32_t r0[kChunk], r1[kChunk];
       tmem_ld_32x32b_x16(taddr, r0);
-      if (ng > 1) tmem_ld_32x32b_x16(taddr + 16, r1);
+      if (ng > 1) tmem_ld_32x32b_x16(taddr + TOK, r1);
       tmem_ld_wait();
 #pragma unroll
-      for (int m = 0; m < kTok; ++m)
+      for (int m = 0; m < kChunk; ++m)
         v[m] = __uint_as_float(r0[m]) + (ng > 1 ? __uint_as_float(r1[m]) : 0.f);
       if (ng > 2) {  // pipeline 2 starts at the third group
-        tmem_ld_32x32b_x16(taddr + 32, r0);
+        tmem_ld_32x32b_x16(taddr + 2 * TOK, r0);
         tmem_ld_wait();
 #pragma unroll
-        for (int m = 0; m < kTok; ++m) v[m] += __uint_as_float(r0[m]);
+        for (int m = 0; m < kChunk; ++m) v[m] += __uint_as_float(r0[m]);
       }
+    } else {
+      uint32_t r0[kChunk];
+      tmem_ld_32x32b_x16(taddr, r0);
+      tmem_ld_wait();
+#pragma unroll
+      for (int m = 0; m < kChunk; ++m) v[m] = __uint_as_float(r0[m]);
     }
+  };
+  float v0[kChunk];  // tokens 0..15, read before the block-wide barrier
+  if (epi) {
+    tc_fence_after();
+    load_chunk(0, v0);
   }
   // Roles that ran on one lane rejoin their warp before the block-wide
   // barrier, which a diverged warp must not reach.
@@ -428,46 +496,78 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       }
     }
     if (warp == kMmaWarp && lane == 0) {
-      // group u sits in stage u % 3 + 3 ((u / 3) % kXPer), phase (u / 3 / kXPer) & 1
+      // group u sits in stage u % kPipes + kPipes ((u / kPipes) % kXPer),
+      // phase (u / kPipes / kXPer) & 1; each X stage's MMA warp issued its
+      // copies, and x_last holds the last group requested per stage
       for (int s = 0; s < kXG; ++s)
         if (x_last[s] >= 0)
-          mbar_wait_bounded(&x_full[s], static_cast<uint32_t>((x_last[s] / 3 / kXPer) & 1), drain);
+          mbar_wait_bounded(&x_full[s], static_cast<uint32_t>((x_last[s] / kPipes / kXPer) & 1),
+                            drain);
       mbar_wait_bounded(d_full, 0, drain);
     }
     __syncwarp();
     __syncthreads();
   }
   if (cs == 1) {
-    if (epi && n0 + en < p.N) store_column(p.Y + n0 + en, p.N, v, rows, p.act);
+    if (epi && n0 + en < p.N) {
+      store_column(p.Y + n0 + en, p.N, v0, rows, p.act);
+      for (int c = 1; c < TOK / kChunk && kChunk * c < rows; ++c) {
+        float v[kChunk];
+        tc_fence_after();
+        load_chunk(c, v);
+        store_column(p.Y + static_cast<size_t>(kChunk * c) * p.N + n0 + en, p.N, v, rows - kChunk * c,
+                     p.act);
+      }
+    }
   } else {
     // Rank r owns the tile's columns [128 r / cs, 128 (r + 1) / cs).  Each
-    // CTA stages its 16 token partials per column in its (now idle) X ring,
-    // column-major, so that every owner's columns are one contiguous block,
-    // and sends each owner its block with one bulk copy counted on the
-    // owner's part_full; slice q of the owner's `part` holds rank q's
-    // block.  Measured against the alternatives: byte-counted 16-byte
-    // remote stores serialise on the owner's barrier (1.2 us more), and
-    // plain remote stores need a release/acquire cluster barrier (0.3 us
-    // more).  Every rank sends its blocks even after an abort, so every
-    // owner's count completes.
+    // CTA stages its TOK token partials per column in its (now idle) X
+    // stages, column-major, so that every owner's columns are one contiguous
+    // block, and sends each owner its block with one bulk copy counted on
+    // the owner's part_full; slice q of the owner's receive buffer holds
+    // rank q's block.  With 16 tokens the receive buffer is a dedicated one;
+    // with 32 and 64 it is the owner's weight ring, so the copies wait for
+    // a relaxed cluster rendezvous (every CTA is done with its ring).
+    // Measured against the alternatives (16 tokens): byte-counted 16-byte
+    // remote stores were no faster; plain remote stores need a
+    // release/acquire cluster barrier, which cost 1 us more.  Every rank
+    // sends its blocks even after an abort, so every owner's count completes.
     const int slice = (kCols + cs - 1) / cs;
     const int cb0 = (rank * kCols) / cs, ncol = ((rank + 1) * kCols) / cs - cb0;
     float* stage = reinterpret_cast<float*>(smem + C::kOffX);
+    float* recv = TOK == 16 ? part : reinterpret_cast<float*>(smem + C::kOffW);
     if (threadIdx.x == 0)
-      mbar_arrive_expect_tx(part_full, static_cast<uint32_t>(cs * ncol * kTok * 4));
+      mbar_arrive_expect_tx(part_full, static_cast<uint32_t>(cs * ncol * TOK * 4));
     if (epi) {
-      const uint32_t dst = smem_addr(stage + en * kTok);
+      const uint32_t dst = smem_addr(stage + en * TOK);
 #pragma unroll
-      for (int i = 0; i < kTok / 4; ++i)
-        st_shared_v4(dst + 16 * i, __float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
-                     __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
+      for (int i = 0; i < kChunk / 4; ++i)
+        st_shared_v4(dst + 16 * i, __float_as_uint(v0[4 * i]), __float_as_uint(v0[4 * i + 1]),
+                     __float_as_uint(v0[4 * i + 2]), __float_as_uint(v0[4 * i + 3]));
+      for (int c = 1; c < TOK / kChunk; ++c) {
+        float v[kChunk];
+        tc_fence_after();
+        load_chunk(c, v);
+#pragma unroll
+        for (int i = 0; i < kChunk / 4; ++i)
+          st_shared_v4(dst + 64 * c + 16 * i, __float_as_uint(v[4 * i]),
+                       __float_as_uint(v[4 * i + 1]), __float_as_uint(v[4 * i + 2]),
+                       __float_as_uint(v[4 * i + 3]));
+      }
       fence_proxy_async_smem();  // the bulk copies read what these threads wrote
       named_barrier_sync(1, kEpiWarps * 32);
+    }
+    if (TOK > 16) {
+      __syncwarp();
+      cluster_arrive_relaxed();
+      cluster_wait();  // every CTA of the cluster is done with its weight ring
+    }
+    if (epi) {
       if (en < cs) {
         const int r = en;  // one thread per destination rank
         const int rb0 = (r * kCols) / cs, rn = ((r + 1) * kCols) / cs - rb0;
-        dsmem_bulk_copy(dsmem_map(part + rank * slice * kTok, r), smem_addr(stage + rb0 * kTok),
-                        static_cast<uint32_t>(rn * kTok * 4), dsmem_map(part_full, r));
+        dsmem_bulk_copy(dsmem_map(recv + rank * slice * TOK, r), smem_addr(stage + rb0 * TOK),
+                        static_cast<uint32_t>(rn * TOK * 4), dsmem_map(part_full, r));
       }
       const int c = en;
       if (c < ncol) {
@@ -477,21 +577,26 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
           late.wait_limit_ns = p.diag.wait_limit_ns + 2000000000ull;
           mbar_wait_bounded(part_full, 0, late);
         }
-        float acc[kTok];
+        if (n0 + cb0 + c < p.N) {
+          for (int ch = 0; ch < TOK / kChunk && kChunk * ch < rows; ++ch) {
+            float acc[kChunk];
 #pragma unroll
-        for (int m = 0; m < kTok; ++m) acc[m] = 0.f;
-        for (int qq = 0; qq < cs; ++qq) {
-          const uint32_t src = smem_addr(part + (qq * slice + c) * kTok);
+            for (int m = 0; m < kChunk; ++m) acc[m] = 0.f;
+            for (int qq = 0; qq < cs; ++qq) {
+              const uint32_t src = smem_addr(recv + (qq * slice + c) * TOK + kChunk * ch);
 #pragma unroll
-          for (int i = 0; i < kTok / 4; ++i) {
-            const float4 f = ld_shared_v4_f32(src + 16 * i);
-            acc[4 * i] += f.x;
-            acc[4 * i + 1] += f.y;
-            acc[4 * i + 2] += f.z;
-            acc[4 * i + 3] += f.w;
+              for (int i = 0; i < kChunk / 4; ++i) {
+                const float4 f = ld_shared_v4_f32(src + 16 * i);
+                acc[4 * i] += f.x;
+                acc[4 * i + 1] += f.y;
+                acc[4 * i + 2] += f.z;
+                acc[4 * i + 3] += f.w;
+              }
+            }
+            store_column(p.Y + static_cast<size_t>(kChunk * ch) * p.N + n0 + cb0 + c, p.N, acc,
+                         rows - kChunk * ch, p.act);
           }
         }
-        if (n0 + cb0 + c < p.N) store_column(p.Y + n0 + cb0 + c, p.N, acc, rows, p.act);
       }
     }
     // No CTA leaves while a peer's copy may still read or write its shared
@@ -524,7 +629,7 @@ constexpr int kProbeSmem = 160 * 1024;  // more than half of an SM
 // a launch finds while its neighbour holds the other slot.  (The occupancy
 // calculator counts one CTA of this kernel per SM, while two run side by
 // side, so the count is taken on the probe kernel above.)
-template <int BITS>
+template <int BITS, int TOK>
 struct StInit {
   std::atomic<uint64_t> done{0};
   std::mutex mu;
@@ -534,13 +639,13 @@ struct StInit {
     if (!(done.load(std::memory_order_acquire) & bit)) {
       std::lock_guard<std::mutex> lk(mu);
       if (!(done.load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_stream_kernel<BITS>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_stream_kernel<BITS, TOK>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             StCfg<BITS>::kSmem);
+                                             StCfg<BITS, TOK>::kSmem);
         if (e != cudaSuccess) return e;
         // all of the unified L1/shared memory as shared, so that two CTAs
         // (this launch's and the next one's) fit one SM
-        e = cudaFuncSetAttribute(gemm_stream_kernel<BITS>,
+        e = cudaFuncSetAttribute(gemm_stream_kernel<BITS, TOK>,
                                  cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(st_room_probe_kernel,
@@ -570,8 +675,22 @@ struct StInit {
     return cudaSuccess;
   }
 };
-StInit<4> g_st4;
-StInit<8> g_st8;
+StInit<4, 16> g_st4_16;
+StInit<4, 32> g_st4_32;
+StInit<4, 64> g_st4_64;
+StInit<8, 16> g_st8_16;
+StInit<8, 32> g_st8_32;
+StInit<8, 64> g_st8_64;
+
+// The kernel attributes of (bits, TOK) on `device`, and the cluster room
+// (the same for every TOK: the footprints differ by a few KiB at most).
+cudaError_t st_ensure(int bits, int tok, int device, int (&room)[kMaxSplit + 1]) {
+  if (bits == 4)
+    return tok == 16 ? g_st4_16.ensure(device, room)
+                     : tok == 32 ? g_st4_32.ensure(device, room) : g_st4_64.ensure(device, room);
+  return tok == 16 ? g_st8_16.ensure(device, room)
+                   : tok == 32 ? g_st8_32.ensure(device, room) : g_st8_64.ensure(device, room);
+}
 
 // The K split: the largest cs <= 8 (and <= the groups) whose CTAs fill at
 // most one slot per SM (the other slot is for the neighbouring launch) and
@@ -594,7 +713,7 @@ int st_split(int64_t tiles, int64_t G, int num_sms, int hint, const int* room) {
 const int* st_caps(int bits, int device) {
   static thread_local int caps[kMaxSplit + 1];
   if (device < 0) return nullptr;
-  const cudaError_t e = bits == 4 ? g_st4.ensure(device, caps) : g_st8.ensure(device, caps);
+  const cudaError_t e = st_ensure(bits, 16, device, caps);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return nullptr;
@@ -619,11 +738,13 @@ bool gemm_stream_fits(int bits, int64_t K, int64_t N, int split_hint, int num_sm
 }
 
 cudaError_t launch_gemm_stream(const GemmArgs& a, cudaStream_t stream) {
-  if (a.M > kTok || a.M < 1) return cudaErrorNotSupported;
+  if (a.M > kMaxStreamRows || a.M < 1) return cudaErrorNotSupported;
+  // the MMA's N: the smallest of 16, 32, 64 tokens that holds M
+  const int tok = a.M <= 16 ? 16 : a.M <= 32 ? 32 : 64;
   TensorMapEncodeFn enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
   int room[kMaxSplit + 1];
-  cudaError_t e = a.bits == 4 ? g_st4.ensure(a.device, room) : g_st8.ensure(a.device, room);
+  cudaError_t e = st_ensure(a.bits, tok, a.device, room);
   if (e != cudaSuccess) return e;
   const int cs = gemm_stream_split(a.bits, a.K, a.N, a.split_hint, a.num_sms, a.device);
   if (cs < 1 || room[cs] < 1) return cudaErrorNotSupported;
@@ -631,12 +752,12 @@ cudaError_t launch_gemm_stream(const GemmArgs& a, cudaStream_t stream) {
   const int ngmax = static_cast<int>((G + cs - 1) / cs);
 
   // X as a 3-D bf16 tensor [K/64 blocks][M rows][64]; one box is a group's
-  // two 64-deep blocks for 16 rows (128-byte swizzle); rows past M read as
+  // two 64-deep blocks for `tok` rows (128-byte swizzle); rows past M read as
   // zeros.
   CUtensorMap tmx;
   const cuuint64_t xdim[3] = {64, static_cast<cuuint64_t>(a.M), static_cast<cuuint64_t>(a.K / 64)};
   const cuuint64_t xstride[2] = {static_cast<cuuint64_t>(a.K) * 2, 128};
-  const cuuint32_t xbox[3] = {64, kTok, 2};
+  const cuuint32_t xbox[3] = {64, static_cast<cuuint32_t>(tok), 2};
   const cuuint32_t estride[3] = {1, 1, 1};
   CUresult r = enc(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.X), xdim,
                    xstride, xbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -647,8 +768,8 @@ cudaError_t launch_gemm_stream(const GemmArgs& a, cudaStream_t stream) {
   // 128-byte rows][32 words]; one box is one group's cell of both cell
   // columns of a tile (a column past N reads as zeros).
   CUtensorMap tmw;
-  const int cell_rows = a.bits == 4 ? StCfg<4>::kCellRows : StCfg<8>::kCellRows;
-  const int cell_bytes = a.bits == 4 ? StCfg<4>::kCellBytes : StCfg<8>::kCellBytes;
+  const int cell_rows = a.bits == 4 ? StCfg<4, 16>::kCellRows : StCfg<8, 16>::kCellRows;
+  const int cell_bytes = a.bits == 4 ? StCfg<4, 16>::kCellBytes : StCfg<8, 16>::kCellBytes;
   const cuuint64_t wdim[3] = {32, static_cast<cuuint64_t>(G) * cell_rows,
                               static_cast<cuuint64_t>(a.N / 64)};
   const cuuint64_t wstride[2] = {128, static_cast<cuuint64_t>(G) * cell_bytes};
@@ -686,7 +807,9 @@ cudaError_t launch_gemm_stream(const GemmArgs& a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(tiles * cs));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = a.bits == 4 ? StCfg<4>::kSmem : StCfg<8>::kSmem;
+  cfg.dynamicSmemBytes = static_cast<size_t>(
+      a.bits == 4 ? (tok == 16 ? StCfg<4, 16>::kSmem : tok == 32 ? StCfg<4, 32>::kSmem : StCfg<4, 64>::kSmem)
+                  : (tok == 16 ? StCfg<8, 16>::kSmem : tok == 32 ? StCfg<8, 32>::kSmem : StCfg<8, 64>::kSmem));
   cfg.stream = stream;
   cudaLaunchAttribute attrs[2];
   int na = 0;
@@ -702,8 +825,14 @@ cudaError_t launch_gemm_stream(const GemmArgs& a, cudaStream_t stream) {
   }
   cfg.attrs = attrs;
   cfg.numAttrs = na;
-  if (a.bits == 4) return cudaLaunchKernelEx(&cfg, gemm_stream_kernel<4>, tmx, tmw, tms, p);
-  return cudaLaunchKernelEx(&cfg, gemm_stream_kernel<8>, tmx, tmw, tms, p);
+  if (a.bits == 4) {
+    if (tok == 16) return cudaLaunchKernelEx(&cfg, gemm_stream_kernel<4, 16>, tmx, tmw, tms, p);
+    if (tok == 32) return cudaLaunchKernelEx(&cfg, gemm_stream_kernel<4, 32>, tmx, tmw, tms, p);
+    return cudaLaunchKernelEx(&cfg, gemm_stream_kernel<4, 64>, tmx, tmw, tms, p);
+  }
+  if (tok == 16) return cudaLaunchKernelEx(&cfg, gemm_stream_kernel<8, 16>, tmx, tmw, tms, p);
+  if (tok == 32) return cudaLaunchKernelEx(&cfg, gemm_stream_kernel<8, 32>, tmx, tmw, tms, p);
+  return cudaLaunchKernelEx(&cfg, gemm_stream_kernel<8, 64>, tmx, tmw, tms, p);
 }
 
 }  // namespace wq

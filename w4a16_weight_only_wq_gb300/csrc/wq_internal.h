@@ -59,9 +59,12 @@ bool gemm_small_fits(int bits, int64_t K, int64_t N, int split_hint, int num_sms
 cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t stream);
 bool gemm_skinny_fits(int bits, int64_t K, int64_t N);
 
-// Tensor-memory GEMM for M <= 16 whose CTAs take half an SM, so that
-// consecutive launches overlap (wq_gemm_stream.cu).
+// Tensor-memory GEMM for M <= 64 (16, 32 or 64 tokens per launch) whose
+// CTAs take half an SM, so that consecutive launches overlap
+// (wq_gemm_stream.cu).
 // device < 0: no device to query, the split follows the SM count alone.
+// Rows one launch of it takes (the MMA's N is 16, 32 or 64 tokens).
+constexpr int kMaxStreamRows = 64;
 cudaError_t launch_gemm_stream(const GemmArgs& a, cudaStream_t stream);
 bool gemm_stream_fits(int bits, int64_t K, int64_t N, int split_hint, int num_sms, int device);
 int gemm_stream_split(int bits, int64_t K, int64_t N, int split_hint, int num_sms, int device);
