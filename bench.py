@@ -12,8 +12,8 @@ is offline (once per weight) and is timed separately ("pack" in the line).
           inputs resident in HBM; CUDA graph replay of the K steps, the
           buffers rotated over enough copies that every call misses L2.
   e2e     the same metric through the public API with host buffers: each
-          step copies X from pinned host memory, runs both GEMMs and reads
-          both outputs back, then synchronises.
+          step copies both GEMMs' X from pinned host memory (one copy), runs
+          both GEMMs, reads both outputs back (one copy), then synchronises.
   roofline  the small-M GEMM kernel: algorithmic bytes per launch over its
           average launch duration, against the measured HBM copy bandwidth.
   cpu_baseline  the CPU oracle (plain C, fp64) timed on a bounded sample.
@@ -433,23 +433,26 @@ def run_wq(args):
             configs[case.name] = {k_: r[k_] for k_ in ("us", "GB/s", "TFLOP/s", "bound", "frac",
                                                        "regime", "bytes")}
 
-    # End to end through the API with host buffers.
-    hx_up = torch.empty((M, K_UP), dtype=torch.bfloat16).pin_memory()
-    hx_dn = torch.empty((M, K_DN), dtype=torch.bfloat16).pin_memory()
-    hx_up.copy_(x_up.cpu())
-    hx_dn.copy_(x_dn.cpu())
-    hy_up = torch.empty((M, N_UP), dtype=torch.bfloat16).pin_memory()
-    hy_dn = torch.empty((M, N_DN), dtype=torch.bfloat16).pin_memory()
+    # End to end through the API with host buffers.  Both GEMMs' inputs sit
+    # in one pinned buffer (and one device buffer), and so do both results,
+    # so that a step makes one copy each way.
+    nx_up, nx_dn, ny_up, ny_dn = M * K_UP, M * K_DN, M * N_UP, M * N_DN
+    hx = torch.empty(nx_up + nx_dn, dtype=torch.bfloat16).pin_memory()
+    hx[:nx_up].copy_(x_up.cpu().reshape(-1))
+    hx[nx_up:].copy_(x_dn.cpu().reshape(-1))
+    hy = torch.empty(ny_up + ny_dn, dtype=torch.bfloat16).pin_memory()
+    dx = torch.empty(nx_up + nx_dn, dtype=torch.bfloat16, device=dev)
+    dy = torch.empty(ny_up + ny_dn, dtype=torch.bfloat16, device=dev)
+    ex_up, ex_dn = dx[:nx_up].view(M, K_UP), dx[nx_up:].view(M, K_DN)
+    ey_up, ey_dn = dy[:ny_up].view(M, N_UP), dy[ny_up:].view(M, N_DN)
     b0 = sets[0]
 
     def e2e_step():
         with torch.cuda.stream(stream):
-            b0["xu"].copy_(hx_up, non_blocking=True)
-            b0["xd"].copy_(hx_dn, non_blocking=True)
-            wq.gemm_w4a16(b0["xu"], b0["wu"], b0["su"], Y=b0["yu"], stream=stream)
-            wq.gemm_w4a16(b0["xd"], b0["wd"], b0["sd"], Y=b0["yd"], stream=stream)
-            hy_up.copy_(b0["yu"], non_blocking=True)
-            hy_dn.copy_(b0["yd"], non_blocking=True)
+            dx.copy_(hx, non_blocking=True)
+            wq.gemm_w4a16(ex_up, b0["wu"], b0["su"], Y=ey_up, stream=stream)
+            wq.gemm_w4a16(ex_dn, b0["wd"], b0["sd"], Y=ey_dn, stream=stream)
+            hy.copy_(dy, non_blocking=True)
         stream.synchronize()
 
     for _ in range(20):
@@ -462,8 +465,8 @@ def run_wq(args):
     barrier()
     t_e2e = time.perf_counter() - t0
     e2e_val = BYTES_STEP * n_e2e * world / t_e2e / 1e9
-    h2d = hx_up.numel() * 2 + hx_dn.numel() * 2
-    d2h = hy_up.numel() * 2 + hy_dn.numel() * 2
+    h2d = hx.numel() * 2
+    d2h = hy.numel() * 2
 
     # Offline pack, timed on its own.
     wf = torch.randn(K_UP, N_UP, device=dev) * 0.02

@@ -346,14 +346,17 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       const uint32_t xph = static_cast<uint32_t>((k / kXPer) & 1);
       const bool hook = p.diag.force_timeout == 2 && 2 * u >= ng;
       bool ok = true;
+      // group u's dequant set and the phase of its A slots (with one
+      // pipeline per set these are the warp's own and k)
+      const int set = kPipes == kDqSets ? w : u % kDqSets;
+      const uint32_t aph = static_cast<uint32_t>((kPipes == kDqSets ? k : u / kDqSets) & 1);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int hs = 2 * (u % kDqSets) + h;
+        const int hs = 2 * set + h;
         // (the waits suspend the warp instead of spinning: the next
         // launch's MMA warps wait here for microseconds while this SM's
         // other CTA dequantises)
-        if (!role_wait(hook ? never_bar : &a_full[hs],
-                       hook ? 0u : static_cast<uint32_t>((u / kDqSets) & 1), p.diag, abort_flag,
+        if (!role_wait(hook ? never_bar : &a_full[hs], hook ? 0u : aph, p.diag, abort_flag,
                        kMmaWaitHintNs) ||
             (h == 0 && !role_wait(&x_full[xs], xph, p.diag, abort_flag, kMmaWaitHintNs))) {
           ok = false;
@@ -434,179 +437,308 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
   }
 
   // ------------------------------------------------------- epilogue ---
-  // Accumulators D_w[column n][token m] (w < kPipes, TMEM columns TOK w ..):
-  // thread n of warps 0-3 (lane quadrant = warp) reads its column in chunks
-  // of 16 tokens and adds the pipelines' partials in order.  (A pipeline
-  // without a group, when the CTA has fewer groups than pipelines, left its
-  // accumulator unwritten.)
-  const bool epi = warp < kEpiWarps;
-  const int en = 32 * warp + lane;  // the epilogue thread's column
-  bool have = false;
-  if (epi) {
-    pdl_wait_primary();  // Y may be read or written by the preceding kernel
-    have = role_wait(d_full, 0, p.diag, abort_flag, 200);
-  }
-  auto load_chunk = [&](int c, float (&v)[kChunk]) {
+  // Two forms of the same steps: at 16 tokens the thread's 16 partials are
+  // read once into registers (this form needs no register spill); at 32 and
+  // 64 tokens the epilogue works in 16-token chunks, which also changes
+  // where the cluster's partials are received.
+  if constexpr (TOK == 16) {
+    // Accumulators D_w[column n][token m] (w = 0..2): thread n of warps 0-3
+    // (lane quadrant = warp) adds its column's three 16-token partials in
+    // order.  (A warp without a task, when the CTA has a single group, left
+    // its accumulator unwritten.)
+    float v[TOK];
 #pragma unroll
-    for (int m = 0; m < kChunk; ++m) v[m] = 0.f;
-    if (!have) return;
-    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * warp) << 16) + kChunk * c;
-    if constexpr (kPipes == 3) {
-      uint32_t r0[kChunk], r1[kChunk];
-      tmem_ld_32x32b_x16(taddr, r0);
-      if (ng > 1) tmem_ld_32x32b_x16(taddr + TOK, r1);
-      tmem_ld_wait();
-#pragma unroll
-      for (int m = 0; m < kChunk; ++m)
-        v[m] = __uint_as_float(r0[m]) + (ng > 1 ? __uint_as_float(r1[m]) : 0.f);
-      if (ng > 2) {  // pipeline 2 starts at the third group
-        tmem_ld_32x32b_x16(taddr + 2 * TOK, r0);
+    for (int m = 0; m < TOK; ++m) v[m] = 0.f;
+    const bool epi = warp < kEpiWarps;
+    const int en = 32 * warp + lane;  // the epilogue thread's column
+    if (epi) {
+      pdl_wait_primary();  // Y may be read or written by the preceding kernel
+      if (role_wait(d_full, 0, p.diag, abort_flag, 200)) {
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * warp) << 16);
+        uint32_t r0[16], r1[16];
+        tmem_ld_32x32b_x16(taddr, r0);
+        if (ng > 1) tmem_ld_32x32b_x16(taddr + 16, r1);
         tmem_ld_wait();
 #pragma unroll
-        for (int m = 0; m < kChunk; ++m) v[m] += __uint_as_float(r0[m]);
-      }
-    } else {
-      uint32_t r0[kChunk];
-      tmem_ld_32x32b_x16(taddr, r0);
-      tmem_ld_wait();
+        for (int m = 0; m < TOK; ++m)
+          v[m] = __uint_as_float(r0[m]) + (ng > 1 ? __uint_as_float(r1[m]) : 0.f);
+        if (ng > 2) {  // pipeline 2 starts at the third group
+          tmem_ld_32x32b_x16(taddr + 32, r0);
+          tmem_ld_wait();
 #pragma unroll
-      for (int m = 0; m < kChunk; ++m) v[m] = __uint_as_float(r0[m]);
-    }
-  };
-  float v0[kChunk];  // tokens 0..15, read before the block-wide barrier
-  if (epi) {
-    tc_fence_after();
-    load_chunk(0, v0);
-  }
-  // Roles that ran on one lane rejoin their warp before the block-wide
-  // barrier, which a diverged warp must not reach.
-  __syncwarp();
-  tc_fence_before();
-  __syncthreads();
-  if (*abort_flag) {
-    // Let every issued copy land and every issued MMA finish (bounded, at
-    // least 1 s) before shared and tensor memory are released.
-    KernelDiag drain = p.diag;
-    if (drain.wait_limit_ns < 1000000000ull) drain.wait_limit_ns = 1000000000ull;
-    if (warp == kProducerWarp && lane == 0) {
-      mbar_wait_bounded(s_full, 0, drain);
-      for (int s = 0; s < kRing && s < issued_w; ++s) {
-        const int last = s + ((issued_w - 1 - s) / kRing) * kRing;
-        mbar_wait_bounded(&w_full[s], (last / kRing) & 1, drain);
+          for (int m = 0; m < TOK; ++m) v[m] += __uint_as_float(r0[m]);
+        }
       }
     }
-    if (warp == kMmaWarp && lane == 0) {
-      // group u sits in stage u % kPipes + kPipes ((u / kPipes) % kXPer),
-      // phase (u / kPipes / kXPer) & 1; each X stage's MMA warp issued its
-      // copies, and x_last holds the last group requested per stage
-      for (int s = 0; s < kXG; ++s)
-        if (x_last[s] >= 0)
-          mbar_wait_bounded(&x_full[s], static_cast<uint32_t>((x_last[s] / kPipes / kXPer) & 1),
-                            drain);
-      mbar_wait_bounded(d_full, 0, drain);
-    }
+    // Roles that ran on one lane rejoin their warp before the block-wide
+    // barrier, which a diverged warp must not reach.
     __syncwarp();
+    tc_fence_before();
     __syncthreads();
-  }
-  if (cs == 1) {
-    if (epi && n0 + en < p.N) {
-      store_column(p.Y + n0 + en, p.N, v0, rows, p.act);
-      for (int c = 1; c < TOK / kChunk && kChunk * c < rows; ++c) {
-        float v[kChunk];
-        tc_fence_after();
-        load_chunk(c, v);
-        store_column(p.Y + static_cast<size_t>(kChunk * c) * p.N + n0 + en, p.N, v, rows - kChunk * c,
-                     p.act);
+    if (*abort_flag) {
+      // Let every issued copy land and every issued MMA finish (bounded, at
+      // least 1 s) before shared and tensor memory are released.
+      KernelDiag drain = p.diag;
+      if (drain.wait_limit_ns < 1000000000ull) drain.wait_limit_ns = 1000000000ull;
+      if (warp == kProducerWarp && lane == 0) {
+        mbar_wait_bounded(s_full, 0, drain);
+        for (int s = 0; s < kRing && s < issued_w; ++s) {
+          const int last = s + ((issued_w - 1 - s) / kRing) * kRing;
+          mbar_wait_bounded(&w_full[s], (last / kRing) & 1, drain);
+        }
       }
-    }
-  } else {
-    // Rank r owns the tile's columns [128 r / cs, 128 (r + 1) / cs).  Each
-    // CTA stages its TOK token partials per column in its (now idle) X
-    // stages, column-major, so that every owner's columns are one contiguous
-    // block, and sends each owner its block with one bulk copy counted on
-    // the owner's part_full; slice q of the owner's receive buffer holds
-    // rank q's block.  With 16 tokens the receive buffer is a dedicated one;
-    // with 32 and 64 it is the owner's weight ring, so the copies wait for
-    // a relaxed cluster rendezvous (every CTA is done with its ring).
-    // Measured against the alternatives (16 tokens): byte-counted 16-byte
-    // remote stores were no faster; plain remote stores need a
-    // release/acquire cluster barrier, which cost 1 us more.  Every rank
-    // sends its blocks even after an abort, so every owner's count completes.
-    const int slice = (kCols + cs - 1) / cs;
-    const int cb0 = (rank * kCols) / cs, ncol = ((rank + 1) * kCols) / cs - cb0;
-    float* stage = reinterpret_cast<float*>(smem + C::kOffX);
-    float* recv = TOK == 16 ? part : reinterpret_cast<float*>(smem + C::kOffW);
-    if (threadIdx.x == 0)
-      mbar_arrive_expect_tx(part_full, static_cast<uint32_t>(cs * ncol * TOK * 4));
-    if (epi) {
-      const uint32_t dst = smem_addr(stage + en * TOK);
-#pragma unroll
-      for (int i = 0; i < kChunk / 4; ++i)
-        st_shared_v4(dst + 16 * i, __float_as_uint(v0[4 * i]), __float_as_uint(v0[4 * i + 1]),
-                     __float_as_uint(v0[4 * i + 2]), __float_as_uint(v0[4 * i + 3]));
-      for (int c = 1; c < TOK / kChunk; ++c) {
-        float v[kChunk];
-        tc_fence_after();
-        load_chunk(c, v);
-#pragma unroll
-        for (int i = 0; i < kChunk / 4; ++i)
-          st_shared_v4(dst + 64 * c + 16 * i, __float_as_uint(v[4 * i]),
-                       __float_as_uint(v[4 * i + 1]), __float_as_uint(v[4 * i + 2]),
-                       __float_as_uint(v[4 * i + 3]));
+      if (warp == kMmaWarp && lane == 0) {
+        // group u sits in stage u % kPipes + kPipes ((u / kPipes) % kXPer), phase (u / kPipes / kXPer) & 1
+        for (int s = 0; s < kXG; ++s)
+          if (x_last[s] >= 0)
+            mbar_wait_bounded(&x_full[s], static_cast<uint32_t>((x_last[s] / kPipes / kXPer) & 1), drain);
+        mbar_wait_bounded(d_full, 0, drain);
       }
-      fence_proxy_async_smem();  // the bulk copies read what these threads wrote
-      named_barrier_sync(1, kEpiWarps * 32);
+      __syncwarp();
+      __syncthreads();
     }
-    if (TOK > 16) {
+    if (cs == 1) {
+      if (epi && n0 + en < p.N) store_column(p.Y + n0 + en, p.N, v, rows, p.act);
+    } else {
+      // Rank r owns the tile's columns [128 r / cs, 128 (r + 1) / cs).  Each
+      // CTA stages its 16 token partials per column in its (now idle) X ring,
+      // column-major, so that every owner's columns are one contiguous block,
+      // and sends each owner its block with one bulk copy counted on the
+      // owner's part_full; slice q of the owner's `part` holds rank q's
+      // block.  Measured against the alternatives: byte-counted 16-byte
+      // remote stores serialise on the owner's barrier (1.2 us more), and
+      // plain remote stores need a release/acquire cluster barrier (0.3 us
+      // more).  Every rank sends its blocks even after an abort, so every
+      // owner's count completes.
+      const int slice = (kCols + cs - 1) / cs;
+      const int cb0 = (rank * kCols) / cs, ncol = ((rank + 1) * kCols) / cs - cb0;
+      float* stage = reinterpret_cast<float*>(smem + C::kOffX);
+      if (threadIdx.x == 0)
+        mbar_arrive_expect_tx(part_full, static_cast<uint32_t>(cs * ncol * TOK * 4));
+      if (epi) {
+        const uint32_t dst = smem_addr(stage + en * TOK);
+#pragma unroll
+        for (int i = 0; i < TOK / 4; ++i)
+          st_shared_v4(dst + 16 * i, __float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+                       __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
+        fence_proxy_async_smem();  // the bulk copies read what these threads wrote
+        named_barrier_sync(1, kEpiWarps * 32);
+        if (en < cs) {
+          const int r = en;  // one thread per destination rank
+          const int rb0 = (r * kCols) / cs, rn = ((r + 1) * kCols) / cs - rb0;
+          dsmem_bulk_copy(dsmem_map(part + rank * slice * TOK, r), smem_addr(stage + rb0 * TOK),
+                          static_cast<uint32_t>(rn * TOK * 4), dsmem_map(part_full, r));
+        }
+        const int c = en;
+        if (c < ncol) {
+          if (!mbar_wait_bounded(part_full, 0, p.diag)) {
+            // a peer can be late by its own timed-out wait plus its drain
+            KernelDiag late = p.diag;
+            late.wait_limit_ns = p.diag.wait_limit_ns + 2000000000ull;
+            mbar_wait_bounded(part_full, 0, late);
+          }
+          float acc[TOK];
+#pragma unroll
+          for (int m = 0; m < TOK; ++m) acc[m] = 0.f;
+          for (int qq = 0; qq < cs; ++qq) {
+            const uint32_t src = smem_addr(part + (qq * slice + c) * TOK);
+#pragma unroll
+            for (int i = 0; i < TOK / 4; ++i) {
+              const float4 f = ld_shared_v4_f32(src + 16 * i);
+              acc[4 * i] += f.x;
+              acc[4 * i + 1] += f.y;
+              acc[4 * i + 2] += f.z;
+              acc[4 * i + 3] += f.w;
+            }
+          }
+          if (n0 + cb0 + c < p.N) store_column(p.Y + n0 + cb0 + c, p.N, acc, rows, p.act);
+        }
+      }
+      // No CTA leaves while a peer's copy may still read or write its shared
+      // memory.  The owners have waited for all of their bytes before
+      // arriving, so every copy has completed once all have arrived; the
+      // barrier orders nothing else (relaxed: it does not wait for this CTA's
+      // Y stores to become visible).
       __syncwarp();
       cluster_arrive_relaxed();
-      cluster_wait();  // every CTA of the cluster is done with its weight ring
+      cluster_wait();
     }
+  } else {
+    // Accumulators D_w[column n][token m] (w < kPipes, TMEM columns TOK w ..):
+    // thread n of warps 0-3 (lane quadrant = warp) reads its column in chunks
+    // of 16 tokens and adds the pipelines' partials in order.  (A pipeline
+    // without a group, when the CTA has fewer groups than pipelines, left its
+    // accumulator unwritten.)
+    const bool epi = warp < kEpiWarps;
+    const int en = 32 * warp + lane;  // the epilogue thread's column
+    bool have = false;
     if (epi) {
-      if (en < cs) {
-        const int r = en;  // one thread per destination rank
-        const int rb0 = (r * kCols) / cs, rn = ((r + 1) * kCols) / cs - rb0;
-        dsmem_bulk_copy(dsmem_map(recv + rank * slice * TOK, r), smem_addr(stage + rb0 * TOK),
-                        static_cast<uint32_t>(rn * TOK * 4), dsmem_map(part_full, r));
-      }
-      const int c = en;
-      if (c < ncol) {
-        if (!mbar_wait_bounded(part_full, 0, p.diag)) {
-          // a peer can be late by its own timed-out wait plus its drain
-          KernelDiag late = p.diag;
-          late.wait_limit_ns = p.diag.wait_limit_ns + 2000000000ull;
-          mbar_wait_bounded(part_full, 0, late);
+      pdl_wait_primary();  // Y may be read or written by the preceding kernel
+      have = role_wait(d_full, 0, p.diag, abort_flag, 200);
+    }
+    auto load_chunk = [&](int c, float (&v)[kChunk]) {
+#pragma unroll
+      for (int m = 0; m < kChunk; ++m) v[m] = 0.f;
+      if (!have) return;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * warp) << 16) + kChunk * c;
+      if constexpr (kPipes == 3) {
+        uint32_t r0[kChunk], r1[kChunk];
+        tmem_ld_32x32b_x16(taddr, r0);
+        if (ng > 1) tmem_ld_32x32b_x16(taddr + TOK, r1);
+        tmem_ld_wait();
+#pragma unroll
+        for (int m = 0; m < kChunk; ++m)
+          v[m] = __uint_as_float(r0[m]) + (ng > 1 ? __uint_as_float(r1[m]) : 0.f);
+        if (ng > 2) {  // pipeline 2 starts at the third group
+          tmem_ld_32x32b_x16(taddr + 2 * TOK, r0);
+          tmem_ld_wait();
+#pragma unroll
+          for (int m = 0; m < kChunk; ++m) v[m] += __uint_as_float(r0[m]);
         }
-        if (n0 + cb0 + c < p.N) {
-          for (int ch = 0; ch < TOK / kChunk && kChunk * ch < rows; ++ch) {
-            float acc[kChunk];
+      } else {
+        uint32_t r0[kChunk];
+        tmem_ld_32x32b_x16(taddr, r0);
+        tmem_ld_wait();
 #pragma unroll
-            for (int m = 0; m < kChunk; ++m) acc[m] = 0.f;
-            for (int qq = 0; qq < cs; ++qq) {
-              const uint32_t src = smem_addr(recv + (qq * slice + c) * TOK + kChunk * ch);
+        for (int m = 0; m < kChunk; ++m) v[m] = __uint_as_float(r0[m]);
+      }
+    };
+    float v0[kChunk];  // tokens 0..15, read before the block-wide barrier
+    if (epi) {
+      tc_fence_after();
+      load_chunk(0, v0);
+    }
+    // Roles that ran on one lane rejoin their warp before the block-wide
+    // barrier, which a diverged warp must not reach.
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag) {
+      // Let every issued copy land and every issued MMA finish (bounded, at
+      // least 1 s) before shared and tensor memory are released.
+      KernelDiag drain = p.diag;
+      if (drain.wait_limit_ns < 1000000000ull) drain.wait_limit_ns = 1000000000ull;
+      if (warp == kProducerWarp && lane == 0) {
+        mbar_wait_bounded(s_full, 0, drain);
+        for (int s = 0; s < kRing && s < issued_w; ++s) {
+          const int last = s + ((issued_w - 1 - s) / kRing) * kRing;
+          mbar_wait_bounded(&w_full[s], (last / kRing) & 1, drain);
+        }
+      }
+      if (warp == kMmaWarp && lane == 0) {
+        // group u sits in stage u % kPipes + kPipes ((u / kPipes) % kXPer),
+        // phase (u / kPipes / kXPer) & 1; each X stage's MMA warp issued its
+        // copies, and x_last holds the last group requested per stage
+        for (int s = 0; s < kXG; ++s)
+          if (x_last[s] >= 0)
+            mbar_wait_bounded(&x_full[s], static_cast<uint32_t>((x_last[s] / kPipes / kXPer) & 1),
+                              drain);
+        mbar_wait_bounded(d_full, 0, drain);
+      }
+      __syncwarp();
+      __syncthreads();
+    }
+    if (cs == 1) {
+      if (epi && n0 + en < p.N) {
+        store_column(p.Y + n0 + en, p.N, v0, rows, p.act);
+        for (int c = 1; c < TOK / kChunk && kChunk * c < rows; ++c) {
+          float v[kChunk];
+          tc_fence_after();
+          load_chunk(c, v);
+          store_column(p.Y + static_cast<size_t>(kChunk * c) * p.N + n0 + en, p.N, v, rows - kChunk * c,
+                       p.act);
+        }
+      }
+    } else {
+      // Rank r owns the tile's columns [128 r / cs, 128 (r + 1) / cs).  Each
+      // CTA stages its TOK token partials per column in its (now idle) X
+      // stages, column-major, so that every owner's columns are one contiguous
+      // block, and sends each owner its block with one bulk copy counted on
+      // the owner's part_full; slice q of the owner's receive buffer holds
+      // rank q's block.  With 16 tokens the receive buffer is a dedicated one;
+      // with 32 and 64 it is the owner's weight ring, so the copies wait for
+      // a relaxed cluster rendezvous (every CTA is done with its ring).
+      // Measured against the alternatives (16 tokens): byte-counted 16-byte
+      // remote stores were no faster; plain remote stores need a
+      // release/acquire cluster barrier, which cost 1 us more.  Every rank
+      // sends its blocks even after an abort, so every owner's count completes.
+      const int slice = (kCols + cs - 1) / cs;
+      const int cb0 = (rank * kCols) / cs, ncol = ((rank + 1) * kCols) / cs - cb0;
+      float* stage = reinterpret_cast<float*>(smem + C::kOffX);
+      float* recv = TOK == 16 ? part : reinterpret_cast<float*>(smem + C::kOffW);
+      if (threadIdx.x == 0)
+        mbar_arrive_expect_tx(part_full, static_cast<uint32_t>(cs * ncol * TOK * 4));
+      if (epi) {
+        const uint32_t dst = smem_addr(stage + en * TOK);
 #pragma unroll
-              for (int i = 0; i < kChunk / 4; ++i) {
-                const float4 f = ld_shared_v4_f32(src + 16 * i);
-                acc[4 * i] += f.x;
-                acc[4 * i + 1] += f.y;
-                acc[4 * i + 2] += f.z;
-                acc[4 * i + 3] += f.w;
+        for (int i = 0; i < kChunk / 4; ++i)
+          st_shared_v4(dst + 16 * i, __float_as_uint(v0[4 * i]), __float_as_uint(v0[4 * i + 1]),
+                       __float_as_uint(v0[4 * i + 2]), __float_as_uint(v0[4 * i + 3]));
+        for (int c = 1; c < TOK / kChunk; ++c) {
+          float v[kChunk];
+          tc_fence_after();
+          load_chunk(c, v);
+#pragma unroll
+          for (int i = 0; i < kChunk / 4; ++i)
+            st_shared_v4(dst + 64 * c + 16 * i, __float_as_uint(v[4 * i]),
+                         __float_as_uint(v[4 * i + 1]), __float_as_uint(v[4 * i + 2]),
+                         __float_as_uint(v[4 * i + 3]));
+        }
+        fence_proxy_async_smem();  // the bulk copies read what these threads wrote
+        named_barrier_sync(1, kEpiWarps * 32);
+      }
+      if (TOK > 16) {
+        __syncwarp();
+        cluster_arrive_relaxed();
+        cluster_wait();  // every CTA of the cluster is done with its weight ring
+      }
+      if (epi) {
+        if (en < cs) {
+          const int r = en;  // one thread per destination rank
+          const int rb0 = (r * kCols) / cs, rn = ((r + 1) * kCols) / cs - rb0;
+          dsmem_bulk_copy(dsmem_map(recv + rank * slice * TOK, r), smem_addr(stage + rb0 * TOK),
+                          static_cast<uint32_t>(rn * TOK * 4), dsmem_map(part_full, r));
+        }
+        const int c = en;
+        if (c < ncol) {
+          if (!mbar_wait_bounded(part_full, 0, p.diag)) {
+            // a peer can be late by its own timed-out wait plus its drain
+            KernelDiag late = p.diag;
+            late.wait_limit_ns = p.diag.wait_limit_ns + 2000000000ull;
+            mbar_wait_bounded(part_full, 0, late);
+          }
+          if (n0 + cb0 + c < p.N) {
+            for (int ch = 0; ch < TOK / kChunk && kChunk * ch < rows; ++ch) {
+              float acc[kChunk];
+#pragma unroll
+              for (int m = 0; m < kChunk; ++m) acc[m] = 0.f;
+              for (int qq = 0; qq < cs; ++qq) {
+                const uint32_t src = smem_addr(recv + (qq * slice + c) * TOK + kChunk * ch);
+#pragma unroll
+                for (int i = 0; i < kChunk / 4; ++i) {
+                  const float4 f = ld_shared_v4_f32(src + 16 * i);
+                  acc[4 * i] += f.x;
+                  acc[4 * i + 1] += f.y;
+                  acc[4 * i + 2] += f.z;
+                  acc[4 * i + 3] += f.w;
+                }
               }
+              store_column(p.Y + static_cast<size_t>(kChunk * ch) * p.N + n0 + cb0 + c, p.N, acc,
+                           rows - kChunk * ch, p.act);
             }
-            store_column(p.Y + static_cast<size_t>(kChunk * ch) * p.N + n0 + cb0 + c, p.N, acc,
-                         rows - kChunk * ch, p.act);
           }
         }
       }
+      // No CTA leaves while a peer's copy may still read or write its shared
+      // memory.  The owners have waited for all of their bytes before
+      // arriving, so every copy has completed once all have arrived; the
+      // barrier orders nothing else (relaxed: it does not wait for this CTA's
+      // Y stores to become visible).
+      __syncwarp();
+      cluster_arrive_relaxed();
+      cluster_wait();
     }
-    // No CTA leaves while a peer's copy may still read or write its shared
-    // memory.  The owners have waited for all of their bytes before
-    // arriving, so every copy has completed once all have arrived; the
-    // barrier orders nothing else (relaxed: it does not wait for this CTA's
-    // Y stores to become visible).
-    __syncwarp();
-    cluster_arrive_relaxed();
-    cluster_wait();
   }
   __syncwarp();
   tc_fence_before();
