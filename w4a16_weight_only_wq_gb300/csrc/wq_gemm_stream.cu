@@ -86,6 +86,7 @@ constexpr uint32_t kMmaWaitHintNs = 1000;  // suspend hint of the MMA warps' wai
 constexpr int kThreads = (kFirstDqWarp + kDqWarps) * 32;  // 512
 constexpr int kChunk = 16;           // tokens per epilogue chunk (16 fp32 registers)
 constexpr int kXRegion = 48 * 1024;  // X stages (and, after the MMAs, staged partials)
+constexpr int kLeadGroups = 1;       // split 2: rank 0's groups beyond half (see the epilogue)
 
 // TOK tokens per launch (the MMA's N: 16, 32 or 64).  At 16 there are three
 // MMA pipelines (one per dequant set, each with its own accumulator); at 32
@@ -143,6 +144,8 @@ struct StCfg {
 struct StParams {
   __nv_bfloat16* Y;
   int M, N, G, cs;
+  int lead;           // > 0 (16 tokens, cs = 2): rank 0 takes G / 2 + lead groups and all
+                      // 128 columns, rank 1 sends it the partials of the rest
   int ngmax;          // groups of the longest CTA range (scales box rows)
   int act;            // 0 none, 1 SiLU applied to the stored bf16 result
   int prefetch_x;     // pull the CTA's X rows into L2 before the wait
@@ -211,8 +214,12 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
   const int cs = p.cs;
   const int tile = blockIdx.x / cs;
   const int rank = blockIdx.x % cs;  // == %cluster_ctarank for cluster (cs,1,1)
-  const int g0 = (p.G * rank) / cs;
-  const int ng = (p.G * (rank + 1)) / cs - g0;
+  // the CTA's groups [g0, g0 + ng): an even split, or with a lead, rank 0
+  // ahead by 2 lead groups so that rank 1's partials travel while it works
+  const bool lead = TOK == 16 && cs == 2 && p.lead > 0;
+  const int g_lead = p.G / 2 + p.lead;
+  const int g0 = lead ? (rank == 0 ? 0 : g_lead) : (p.G * rank) / cs;
+  const int ng = lead ? (rank == 0 ? g_lead : p.G - g_lead) : (p.G * (rank + 1)) / cs - g0;
   const int n0 = tile * kCols;
   const int rows = min(TOK, p.M);
 
@@ -514,9 +521,47 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       const int slice = (kCols + cs - 1) / cs;
       const int cb0 = (rank * kCols) / cs, ncol = ((rank + 1) * kCols) / cs - cb0;
       float* stage = reinterpret_cast<float*>(smem + C::kOffX);
-      if (threadIdx.x == 0)
+      if (lead) {
+        // Rank 0 owns all 128 columns and ran G / 2 + lead groups; rank 1,
+        // with fewer, finished earlier and sends all of its partials (8 KiB)
+        // while rank 0 still works, so their transfer is off the critical
+        // path.  Rank 0 adds its own partial and rank 1's, in rank order.
+        if (rank == 0 && threadIdx.x == 0)
+          mbar_arrive_expect_tx(part_full, static_cast<uint32_t>(kCols * TOK * 4));
+        if (epi && rank == 1) {
+          const uint32_t dst = smem_addr(stage + en * TOK);
+#pragma unroll
+          for (int i = 0; i < TOK / 4; ++i)
+            st_shared_v4(dst + 16 * i, __float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+                         __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
+          fence_proxy_async_smem();  // the bulk copy reads what these threads wrote
+          named_barrier_sync(1, kEpiWarps * 32);
+          if (en == 0)
+            dsmem_bulk_copy(dsmem_map(part, 0), smem_addr(stage),
+                            static_cast<uint32_t>(kCols * TOK * 4), dsmem_map(part_full, 0));
+        }
+        if (epi && rank == 0) {
+          if (!mbar_wait_bounded(part_full, 0, p.diag)) {
+            // a peer can be late by its own timed-out wait plus its drain
+            KernelDiag late = p.diag;
+            late.wait_limit_ns = p.diag.wait_limit_ns + 2000000000ull;
+            mbar_wait_bounded(part_full, 0, late);
+          }
+          const uint32_t src = smem_addr(part + en * TOK);
+#pragma unroll
+          for (int i = 0; i < TOK / 4; ++i) {
+            const float4 f = ld_shared_v4_f32(src + 16 * i);
+            v[4 * i] += f.x;
+            v[4 * i + 1] += f.y;
+            v[4 * i + 2] += f.z;
+            v[4 * i + 3] += f.w;
+          }
+          if (n0 + en < p.N) store_column(p.Y + n0 + en, p.N, v, rows, p.act);
+        }
+      } else if (threadIdx.x == 0) {
         mbar_arrive_expect_tx(part_full, static_cast<uint32_t>(cs * ncol * TOK * 4));
-      if (epi) {
+      }
+      if (!lead && epi) {
         const uint32_t dst = smem_addr(stage + en * TOK);
 #pragma unroll
         for (int i = 0; i < TOK / 4; ++i)
@@ -881,7 +926,14 @@ cudaError_t launch_gemm_stream(const GemmArgs& a, cudaStream_t stream) {
   const int cs = gemm_stream_split(a.bits, a.K, a.N, a.split_hint, a.num_sms, a.device);
   if (cs < 1 || room[cs] < 1) return cudaErrorNotSupported;
   const int64_t G = a.K / 128, tiles = (a.N + kCols - 1) / kCols;
-  const int ngmax = static_cast<int>((G + cs - 1) / cs);
+  // split 2 at 16 tokens: rank 0 takes kLeadGroups more than half (both
+  // ranks keep at least one group, and rank 0 at most the scales buffer)
+  int lead = 0;
+  if (tok == 16 && cs == 2) {
+    lead = kLeadGroups;
+    while (lead > 0 && (G / 2 + lead > G - 1 || G / 2 + lead > kMaxGroups)) --lead;
+  }
+  const int ngmax = lead > 0 ? static_cast<int>(G / 2 + lead) : static_cast<int>((G + cs - 1) / cs);
 
   // X as a 3-D bf16 tensor [K/64 blocks][M rows][64]; one box is a group's
   // two 64-deep blocks for `tok` rows (128-byte swizzle); rows past M read as
@@ -928,6 +980,7 @@ cudaError_t launch_gemm_stream(const GemmArgs& a, cudaStream_t stream) {
   p.G = static_cast<int>(G);
   p.cs = cs;
   p.ngmax = ngmax;
+  p.lead = lead;
   p.act = a.act;
   p.prefetch_x = 1;
   p.Wp = reinterpret_cast<const uint8_t*>(a.Wp);
