@@ -556,6 +556,23 @@ def test_stream_ring_refills(wq, stream_regime, bits, G, M):
         wq.wq_debug_set_split(0)
 
 
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("G", [5, 63, 64])
+def test_stream_lead_split_limits(wq, stream_regime, bits, G):
+    """A split of 2 gives rank 0 one group past half and sends rank 1's
+    partials to it (the lead split): G = 5 (3 + 2 groups) and G = 63 (32 +
+    31, rank 0 at the scales buffer's limit); at G = 64 the lead would take
+    rank 0 past it, so the even split and the per-owner reduction run."""
+    M, K, N = 16, 128 * G, 192
+    X, q, s = synth.small_case(M, K, N, bits, seed=300 + G + bits)
+    try:
+        wq.wq_debug_set_split(2)
+        assert wq.wq_gemm_regime(bits, M, N, K) == 4
+        _run_codes_case(wq, X, q, s, bits)
+    finally:
+        wq.wq_debug_set_split(0)
+
+
 def test_stream_too_many_groups_per_cta_falls_back(wq, stream_regime):
     """33 groups in one CTA exceed the scales buffer: the warp-MMA kernel
     takes the shape."""
