@@ -160,7 +160,11 @@ swa_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_const
     mbar_arrive_expect_tx(recv_bar, S * owned * kRowPart * 4);
   }
   __syncthreads();
-  cluster_arrive_relaxed();  // every CTA's barrier is initialised before any remote store
+  // every CTA's barrier is initialised before any remote store; waited for
+  // here, where it overlaps the launch wait and the first chunks, rather
+  // than just before the merges
+  cluster_arrive_relaxed();
+  cluster_wait();
   // Q, K and V may come from the preceding kernel (programmatic launch):
   // nothing global is read before it completes; the next kernel may start
   // launching now.
@@ -416,7 +420,6 @@ swa_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_const
     st_shared_v2_f32(mine + ((g + 8) * kORow + col) * 4, o[db][2] * f[1], o[db][3] * f[1]);
   }
   __syncthreads();
-  cluster_wait();  // every CTA of the cluster has initialised its barriers
   const int max_owned = (kRows + S - 1) / S;
   const uint32_t recv_local = smem_addr(smem + kOffRecv);
   for (int q = threadIdx.x; q < kRows * kD / 4; q += kThreads) {
