@@ -85,6 +85,44 @@ def test_abandoned_data_wait_drains_and_recovers(wq, small, bits):
     assert_close_to_oracle(Y, Yref, "after an abandoned wait")
 
 
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M,K,N", [(16, 2560, 9728), (32, 2560, 9728), (64, 2560, 2560)],
+                         ids=["lead_split", "tok32", "tok64_cluster6"])
+def test_stream_abandoned_wait_paths(wq, bits, M, K, N):
+    """The stream kernel's other reductions under an abandoned wait: the
+    lead split (a split of 2: rank 1 sends its whole partial to rank 0), and
+    the 32- and 64-token launches (partials received in the owners' weight
+    rings after a rendezvous).  Every rank still sends and every thread
+    reaches the cluster barriers; the error is reported and a normal call
+    afterwards is correct."""
+    X, q, s = synth.small_case(M, K, N, bits, seed=13 + M)
+    Wp = wq.pack_codes(i8_to_dev(q), bits)
+    Xt, st = bf16_to_dev(X), bf16_to_dev(s)
+    fn = wq.gemm_w4a16 if bits == 4 else wq.gemm_w8a16
+    torch.cuda.synchronize()
+    assert wq.wq_clear_device_error() == wq.WQ_OK
+    try:
+        wq.wq_debug_force_regime(4)
+        assert wq.wq_gemm_regime(bits, M, N, K) == 4
+        wq.wq_debug_set_wait_limit_ns(1_000_000)  # 1 ms
+        wq.wq_debug_force_timeout(2)
+        fn(Xt, Wp, st)
+        torch.cuda.synchronize()
+        assert wq.wq_last_device_error() == wq.WQ_ERR_DEVICE_TIMEOUT
+        assert wq.wq_clear_device_error() == wq.WQ_OK
+        wq.wq_debug_force_timeout(0)
+        wq.wq_debug_set_wait_limit_ns(0)
+        Y = fn(Xt, Wp, st)
+        torch.cuda.synchronize()
+    finally:
+        wq.wq_debug_force_timeout(0)
+        wq.wq_debug_set_wait_limit_ns(0)
+        wq.wq_debug_force_regime(-1)
+    assert wq.wq_last_device_error() == wq.WQ_OK
+    Yref = oracle.gemm(X, oracle.pack(q, bits), s, K, N, bits)
+    assert_close_to_oracle(Y, Yref, "after an abandoned wait")
+
+
 def test_attention_abandoned_wait_reports_and_recovers(wq):
     """The wait for the last key/value chunk and the merge wait of the
     sliding-window attention look at a barrier that never completes: the
