@@ -22,8 +22,11 @@
 //  * Work unit: 128 weight columns x a contiguous range of 128-deep groups;
 //    a cluster of `cs` CTAs splits one column tile's K range and each CTA
 //    accumulates its range in one TMEM accumulator [128 x 16].  Partial sums
-//    go to the owning CTA's shared memory (distributed shared memory, byte-
-//    counted asynchronous stores) and are added there in rank order.
+//    go to the owning CTA's shared memory as staged bulk copies counted on
+//    the owner's mbarrier, and are added there in rank order.  At a split of
+//    2 rank 0 owns the whole tile and takes one group more than half: rank
+//    1 finishes earlier and its partial travels while rank 0 still works
+//    (the lead split).
 //  * Producer (warp 0): the scales of the CTA's range (one TMA), the packed
 //    cells of each group (one TMA per group, both 64-column cells, 128-byte
 //    swizzle) into a ring, and an L2 prefetch of the groups beyond the ring,
