@@ -165,6 +165,12 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
 // Y[m][col] = bf16(act(v[m])) for the first `rows` tokens of a 16-token chunk
 // of one column (row stride N).  The activation is chosen once, outside the
 // stores: inside them the compiler evaluated SiLU for every value even when
@@ -700,82 +706,84 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       }
     } else {
       // Rank r owns the tile's columns [128 r / cs, 128 (r + 1) / cs).  Each
-      // CTA stages its TOK token partials per column in its (now idle) X
-      // stages, column-major, so that every owner's columns are one contiguous
-      // block, and sends each owner its block with one bulk copy counted on
-      // the owner's part_full; slice q of the owner's receive buffer holds
-      // rank q's block.  With 16 tokens the receive buffer is a dedicated one;
-      // with 32 and 64 it is the owner's weight ring, so the copies wait for
-      // a relaxed cluster rendezvous (every CTA is done with its ring).
-      // Measured against the alternatives (16 tokens): byte-counted 16-byte
-      // remote stores were no faster; plain remote stores need a
-      // release/acquire cluster barrier, which cost 1 us more.  Every rank
+      // CTA stages its partials in its (now idle) X stages as one block per
+      // owner, token-major ([token][owner's columns]; a warp's stores of one
+      // token are contiguous), and sends each owner its block with one bulk
+      // copy counted on the owner's part_full, into the owner's weight ring,
+      // after a relaxed cluster rendezvous (every CTA is done with its ring).
+      // Slice q of the receive buffer is rank q's block [token][owned
+      // column]: all 512 threads then add the slices in rank order, one
+      // (token, column) each, consecutive threads on consecutive columns, so
+      // the loads are conflict-free and the Y stores of a row coalesce.
+      // (With one thread per owned column, only ~21 of 128 at a split of 6,
+      // each summing all tokens, the owners' phase was the tail.)  Every rank
       // sends its blocks even after an abort, so every owner's count completes.
-      const int slice = (kCols + cs - 1) / cs;
       const int cb0 = (rank * kCols) / cs, ncol = ((rank + 1) * kCols) / cs - cb0;
-      float* stage = reinterpret_cast<float*>(smem + C::kOffX);
-      float* recv = TOK == 16 ? part : reinterpret_cast<float*>(smem + C::kOffW);
+      const uint32_t stage = smem_addr(smem + C::kOffX);
+      const uint32_t recv = smem_addr(smem + C::kOffW);
       if (threadIdx.x == 0)
         mbar_arrive_expect_tx(part_full, static_cast<uint32_t>(cs * ncol * TOK * 4));
       if (epi) {
-        const uint32_t dst = smem_addr(stage + en * TOK);
+        int owner = 0;
+        while (((owner + 1) * kCols) / cs <= en) ++owner;
+        const int ob0 = (owner * kCols) / cs, oncol = ((owner + 1) * kCols) / cs - ob0;
+        // the blocks of the owners before this one hold TOK x ob0 floats
+        const uint32_t blk = stage + static_cast<uint32_t>((ob0 * TOK + (en - ob0)) * 4);
 #pragma unroll
-        for (int i = 0; i < kChunk / 4; ++i)
-          st_shared_v4(dst + 16 * i, __float_as_uint(v0[4 * i]), __float_as_uint(v0[4 * i + 1]),
-                       __float_as_uint(v0[4 * i + 2]), __float_as_uint(v0[4 * i + 3]));
+        for (int m = 0; m < kChunk; ++m)
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(blk + static_cast<uint32_t>(m * oncol * 4)),
+                       "f"(v0[m])
+                       : "memory");
         for (int c = 1; c < TOK / kChunk; ++c) {
           float v[kChunk];
           tc_fence_after();
           load_chunk(c, v);
 #pragma unroll
-          for (int i = 0; i < kChunk / 4; ++i)
-            st_shared_v4(dst + 64 * c + 16 * i, __float_as_uint(v[4 * i]),
-                         __float_as_uint(v[4 * i + 1]), __float_as_uint(v[4 * i + 2]),
-                         __float_as_uint(v[4 * i + 3]));
+          for (int m = 0; m < kChunk; ++m)
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(blk + static_cast<uint32_t>(
+                                                           (kChunk * c + m) * oncol * 4)),
+                         "f"(v[m])
+                         : "memory");
         }
         fence_proxy_async_smem();  // the bulk copies read what these threads wrote
         named_barrier_sync(1, kEpiWarps * 32);
       }
-      if (TOK > 16) {
-        __syncwarp();
-        cluster_arrive_relaxed();
-        cluster_wait();  // every CTA of the cluster is done with its weight ring
+      __syncwarp();
+      cluster_arrive_relaxed();
+      cluster_wait();  // every CTA of the cluster is done with its weight ring
+      if (epi && en < cs) {
+        const int r = en;  // one thread per destination rank
+        const int rb0 = (r * kCols) / cs, rn = ((r + 1) * kCols) / cs - rb0;
+        dsmem_bulk_copy(dsmem_map_addr(recv + static_cast<uint32_t>(rank * TOK * rn * 4), r),
+                        stage + static_cast<uint32_t>(rb0 * TOK * 4),
+                        static_cast<uint32_t>(rn * TOK * 4), dsmem_map(part_full, r));
       }
-      if (epi) {
-        if (en < cs) {
-          const int r = en;  // one thread per destination rank
-          const int rb0 = (r * kCols) / cs, rn = ((r + 1) * kCols) / cs - rb0;
-          dsmem_bulk_copy(dsmem_map(recv + rank * slice * TOK, r), smem_addr(stage + rb0 * TOK),
-                          static_cast<uint32_t>(rn * TOK * 4), dsmem_map(part_full, r));
+      if (!mbar_wait_bounded(part_full, 0, p.diag)) {
+        // a peer can be late by its own timed-out wait plus its drain
+        KernelDiag late = p.diag;
+        late.wait_limit_ns = p.diag.wait_limit_ns + 2000000000ull;
+        mbar_wait_bounded(part_full, 0, late);
+      }
+      auto owner_sum = [&](int it) {
+        const int m = it / ncol, c = it - m * ncol;
+        float acc = 0.f;
+        for (int q = 0; q < cs; ++q)
+          acc += ld_shared_f32(recv + static_cast<uint32_t>(((q * TOK + m) * ncol + c) * 4));
+        return acc;
+      };
+      const int items = rows * ncol;
+      if (p.act == 0) {
+        for (int it = threadIdx.x; it < items; it += kThreads) {
+          const int m = it / ncol, c = it - m * ncol;
+          if (n0 + cb0 + c < p.N)
+            p.Y[static_cast<size_t>(m) * p.N + n0 + cb0 + c] = __float2bfloat16_rn(owner_sum(it));
         }
-        const int c = en;
-        if (c < ncol) {
-          if (!mbar_wait_bounded(part_full, 0, p.diag)) {
-            // a peer can be late by its own timed-out wait plus its drain
-            KernelDiag late = p.diag;
-            late.wait_limit_ns = p.diag.wait_limit_ns + 2000000000ull;
-            mbar_wait_bounded(part_full, 0, late);
-          }
-          if (n0 + cb0 + c < p.N) {
-            for (int ch = 0; ch < TOK / kChunk && kChunk * ch < rows; ++ch) {
-              float acc[kChunk];
-#pragma unroll
-              for (int m = 0; m < kChunk; ++m) acc[m] = 0.f;
-              for (int qq = 0; qq < cs; ++qq) {
-                const uint32_t src = smem_addr(recv + (qq * slice + c) * TOK + kChunk * ch);
-#pragma unroll
-                for (int i = 0; i < kChunk / 4; ++i) {
-                  const float4 f = ld_shared_v4_f32(src + 16 * i);
-                  acc[4 * i] += f.x;
-                  acc[4 * i + 1] += f.y;
-                  acc[4 * i + 2] += f.z;
-                  acc[4 * i + 3] += f.w;
-                }
-              }
-              store_column(p.Y + static_cast<size_t>(kChunk * ch) * p.N + n0 + cb0 + c, p.N, acc,
-                           rows - kChunk * ch, p.act);
-            }
-          }
+      } else {
+        for (int it = threadIdx.x; it < items; it += kThreads) {
+          const int m = it / ncol, c = it - m * ncol;
+          if (n0 + cb0 + c < p.N)
+            p.Y[static_cast<size_t>(m) * p.N + n0 + cb0 + c] =
+                __float2bfloat16_rn(apply_act(owner_sum(it), 1));
         }
       }
       // No CTA leaves while a peer's copy may still read or write its shared
