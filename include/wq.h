@@ -293,9 +293,10 @@ WQ_API void wq_set_programmatic_launch(int on);
    (weights streamed by TMA, a K split reduced across a thread-block
    cluster; up to 64 rows per launch, taller inputs in 64-row slices),
    which needs at most 32 groups per CTA and otherwise falls back to 0;
-   any other value restores the automatic choice: M <= 32 kernel 4 (one
-   launch), or kernel 0 in 16-row slices where kernel 4 does not apply,
-   larger M kernel 3, or kernel 1 where kernel 3 does not apply). */
+   any other value restores the automatic choice: M <= 64 kernel 4 (one
+   launch), or where kernel 4 does not apply kernel 0 in 16-row slices
+   (M <= 32) or kernel 3 (M from 33 to 64); larger M kernel 3, or kernel 1
+   where kernel 3 does not apply). */
 WQ_API void wq_debug_force_regime(int regime);
 
 /* Which kernel family a GEMM of this shape runs (numbering as in

@@ -140,6 +140,12 @@ def test_regime_selection_is_host_logic(wq):
     assert wq.wq_gemm_regime(4, 16, 9728, 2560) == 4
     # 33 groups on one column tile: more groups per CTA than kernel 4 holds
     assert wq.wq_gemm_regime(4, 16, 128, 128 * 33 * 8) == 0
+    # kernel 4 takes up to 64 rows in one launch; a taller M runs tiled, and
+    # so does a 33- to 64-row shape kernel 4 cannot take
+    assert wq.wq_gemm_regime(4, 64, 9728, 2560) == 4
+    assert wq.wq_gemm_regime(8, 33, 2560, 9728) == 4
+    assert wq.wq_gemm_regime(4, 65, 9728, 2560) == 3
+    assert wq.wq_gemm_regime(4, 48, 128, 128 * 33 * 8) == 3
     assert wq.wq_gemm_regime(4, 128, 9728, 2560) == 3
     assert wq.wq_gemm_regime(4, 8192, 9728, 2560) == 3
     # K / 128 = 5 is not a multiple of the INT4 chunk: kernel 1 takes it

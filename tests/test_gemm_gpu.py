@@ -102,7 +102,7 @@ def test_tmem_small_m_every_split(wq, skinny_regime, bits):
 
 
 def test_default_kernel_choice(wq):
-    for M, want in [(1, 4), (16, 4), (32, 4), (33, 3), (384, 3), (8192, 3)]:
+    for M, want in [(1, 4), (16, 4), (32, 4), (33, 4), (64, 4), (65, 3), (384, 3), (8192, 3)]:
         assert wq.wq_gemm_regime(4, M, 2560, 2560) == want
 
 

@@ -21,8 +21,11 @@ std::atomic<int> g_pdl{0};
 std::atomic<int> g_split_hint{0};
 std::atomic<int> g_force_regime{-1};
 
-// Rows up to which the small-M kernel (16 rows per launch) is used; larger
-// M runs on the tensor-core kernel.
+// Rows up to which the stream kernel (one launch takes up to 64 rows) is
+// used; larger M runs on the tiled tensor-memory kernel.  Of the shapes the
+// stream kernel cannot take, those up to kSmallMaxM rows go to the warp-MMA
+// kernel (16 rows per launch), taller ones to the tiled kernel.
+constexpr int64_t kStreamMaxM = wq::kMaxStreamRows;
 constexpr int64_t kSmallMaxM = 32;
 
 // 0: warp-MMA small-M kernel (16 rows per launch), 1: tensor-core tiled
@@ -36,12 +39,16 @@ int pick_regime(int64_t M) {
   if (f >= 0 && f < kNumRegimes) return f;
   // measured at K = 2560, N = 9728: kernel 3 is faster than kernel 1 at
   // every M from 64 to 8192; kernel 1 takes the shapes kernel 3 cannot.
-  // At M <= 32, kernel 4 (whose launches overlap; one launch up to 32 rows)
-  // beats kernel 0 on the INT4 decode shapes; kernel 0 takes what kernel 4
-  // cannot.  At M = 64 kernel 3 matches or beats kernel 4's 64-token launch
-  // (12.5 against 12.2 us at 2560 x 9728, 8.3 against 10.6 at 2560 x 2560).
-  return M <= kSmallMaxM ? 4 : 3;
+  // At M <= 32, kernel 4 (whose launches overlap) beats kernel 0 on the
+  // INT4 decode shapes.  From 33 to 64 rows kernel 4's single launch beats
+  // kernel 3 on K x N = 2560 x 9728, 2560 x 2560 and 9728 x 2560, INT4 and
+  // INT8 (M = 64, INT4: 11.2 against 12.1 us, 7.5 against 7.9, 11.9
+  // against 14.6); above 64 rows it needs a second launch and kernel 3 wins.
+  return M <= kStreamMaxM ? 4 : 3;
 }
+
+// The family that takes a shape kernel 4 cannot index.
+int stream_fallback(int64_t M) { return M <= kSmallMaxM ? 0 : 3; }
 thread_local cudaError_t t_last_cuda = cudaSuccess;
 
 wq_status cuda_status(cudaError_t e) {
@@ -176,7 +183,8 @@ wq_status gemm_run(int bits, const void* X, const uint32_t* Wp, const void* scal
   a.weights_in_l2 = weights_in_l2 ? 1 : 0;
   a.diag = diag_for(d);
   int regime = pick_regime(M);
-  if (regime == 4 && !wq::gemm_stream_fits(bits, K, N, a.split_hint, d.num_sms, dev)) regime = 0;
+  if (regime == 4 && !wq::gemm_stream_fits(bits, K, N, a.split_hint, d.num_sms, dev))
+    regime = stream_fallback(M);
   if (regime == 0 && !wq::gemm_small_fits(bits, K, N, a.split_hint, d.num_sms)) regime = 1;
   if (regime == 3 && !wq::gemm_wt_fits(bits, M, K, N)) regime = 1;
   if (regime == 3) {
@@ -490,7 +498,7 @@ int wq_gemm_regime(int bits, int64_t M, int64_t N, int64_t K) {
   int r = pick_regime(M);
   const int sms = sm_count_or_default();
   if (r == 4 && !wq::gemm_stream_fits(bits, K, N, g_split_hint.load(), sms, current_sm103()))
-    r = 0;
+    r = stream_fallback(M);
   if (r == 2 && !wq::gemm_skinny_fits(bits, K, N)) r = 0;
   // shapes whose X slice does not fit the small-M kernel run on the tiled one
   if (r == 0 && !wq::gemm_small_fits(bits, K, N, g_split_hint.load(), sms)) r = 1;

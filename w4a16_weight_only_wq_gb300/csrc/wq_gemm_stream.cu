@@ -53,8 +53,8 @@
 //    columns wide, so only one MMA pipeline fits beside the six A
 //    half-slots; warp 1 issues every group's MMAs in order, warp 2 requests
 //    X, and the epilogue works in 16-token chunks.  The cluster's partials
-//    are then received in the owners' idle weight rings, after a relaxed
-//    rendezvous.
+//    go token-major, one bulk copy per owner after a relaxed rendezvous,
+//    into the owners' idle weight rings, where all 512 threads add them.
 //  * Epilogue (warps 0-3 once their roles are done, one per lane
 //    quadrant): tcgen05.ld of the three accumulators, added in a fixed
 //    order, then Y or the cluster reduction.
