@@ -51,10 +51,12 @@
 //    X request (one TMA per group); warp 1 lets the next launch start.
 //  * 32 and 64 tokens (M = 17..64 in one launch): the accumulator is TOK
 //    columns wide, so only one MMA pipeline fits beside the six A
-//    half-slots; warp 1 issues every group's MMAs in order, warp 2 requests
-//    X, and the epilogue works in 16-token chunks.  The cluster's partials
-//    go token-major, one bulk copy per owner after a relaxed rendezvous,
-//    into the owners' idle weight rings, where all 512 threads add them.
+//    half-slots; warp 1 waits once per group and issues both halves' MMAs,
+//    warp 2 requests X, and the epilogue reads the accumulator in 16-token
+//    chunks, one per group of four warps.  The cluster's partials go column
+//    by column (padded rows, 16-byte accesses), one bulk copy per owner after
+//    a relaxed rendezvous, into the owners' idle weight rings, where all 512
+//    threads add them.
 //  * Epilogue (warps 0-3 once their roles are done, one per lane
 //    quadrant): tcgen05.ld of the three accumulators, added in a fixed
 //    order, then Y or the cluster reduction.
@@ -138,10 +140,12 @@ struct StCfg {
   static constexpr int kOffXLast = kOffBar + kNumBars * 8 + 16;
   static constexpr int kSmem = kOffXLast + T::kXG * 4 + 1024;  // + alignment slack
   static_assert(kSmem <= 113 * 1024, "two CTAs must fit one SM");
-  // partials: staged in the X region (128 columns x TOK); received (TOK >= 32)
-  // in the weight ring, cs slices of ceil(128 / cs) columns x TOK (<= 34 KiB)
-  static_assert(kCols * TOK * 4 <= T::kXG * T::kXGroupBytes, "staged partials fit the X stages");
-  static_assert(TOK == 16 || 7 * 19 * TOK * 4 <= kRing * kWBytes, "received partials fit the ring");
+  // partials: staged in the X region (128 columns x at most TOK + 4 floats);
+  // received (TOK >= 32) in the weight ring, cs slices of ceil(128 / cs)
+  // columns x (TOK + 4) floats (<= 36 KiB)
+  static_assert(kCols * (TOK + 4) * 4 <= T::kXG * T::kXGroupBytes, "staged partials fit the X stages");
+  static_assert(TOK == 16 || 7 * 19 * (TOK + 4) * 4 <= kRing * kWBytes,
+                "received partials fit the ring");
 };
 
 struct StParams {
@@ -163,12 +167,6 @@ __device__ __forceinline__ bool elect_one() {
       "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(pred));
   return pred != 0;
-}
-
-__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-  return v;
 }
 
 // Y[m][col] = bf16(act(v[m])) for the first `rows` tokens of a 16-token chunk
@@ -366,6 +364,38 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       // pipeline per set these are the warp's own and k)
       const int set = kPipes == kDqSets ? w : u % kDqSets;
       const uint32_t aph = static_cast<uint32_t>((kPipes == kDqSets ? k : u / kDqSets) & 1);
+      if constexpr (kPipes == 1) {
+        // One warp issues every group, so its per-group steps are the MMA
+        // phase's pace: one wait for A, one for X, then both halves' MMAs
+        // from one elected thread.  Each warp of the set arrives on half 1's
+        // barrier after its half-0 stores and arrival, so half 1 complete
+        // means the whole group's A is in tensor memory.  (Waiting and
+        // issuing per half, with the SM shared by the dequant warps, took
+        // ~1,000 cycles per group.)
+        if (!role_wait(hook ? never_bar : &a_full[2 * set + 1], hook ? 0u : aph, p.diag, abort_flag,
+                       kMmaWaitHintNs) ||
+            !role_wait(&x_full[xs], xph, p.diag, abort_flag, kMmaWaitHintNs)) {
+          ok = false;
+        } else {
+          tc_fence_after();
+          const uint64_t bd = xdesc0 + static_cast<uint64_t>((xs * T::kXGroupBytes) >> 4);
+          if (elect_one()) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t a_tmem = tmem_base + kACol + (2 * set + h) * 32;
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                umma_bf16_ts(d_tmem, a_tmem + 8 * j,
+                             bd + static_cast<uint64_t>((h * T::kXBlockBytes) >> 4) +
+                                 static_cast<uint64_t>(2 * j),
+                             idesc, (k | h | j) != 0);
+              umma_commit(&a_empty[2 * set + h]);
+            }
+            umma_commit(&x_empty[xs]);
+          }
+          __syncwarp();
+        }
+      } else {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int hs = 2 * set + h;
@@ -394,6 +424,7 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
           if (h == 1) umma_commit(&x_empty[xs]);
         }
         __syncwarp();
+      }
       }
       if (!ok) break;
       // refill the X stage of this pipeline's previous group (whose MMAs
@@ -619,13 +650,18 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       cluster_wait();
     }
   } else {
-    // Accumulators D_w[column n][token m] (w < kPipes, TMEM columns TOK w ..):
-    // thread n of warps 0-3 (lane quadrant = warp) reads its column in chunks
-    // of 16 tokens and adds the pipelines' partials in order.  (A pipeline
-    // without a group, when the CTA has fewer groups than pipelines, left its
-    // accumulator unwritten.)
+    // Accumulators D_w[column n][token m] (w < kPipes, TMEM columns TOK w ..)
+    // are read in chunks of 16 tokens, the pipelines' partials added in
+    // order: warp w reads chunk w / 4 of the columns of its lane quadrant
+    // w % 4 (thread n = 32 (w % 4) + lane, column n), so the TOK / 16 chunks
+    // are read by as many groups of four warps at once.  Warps 0-3 read
+    // chunk 0 as soon as the MMAs complete, the others after the block-wide
+    // barrier that passes that on.  (A pipeline without a group, when the
+    // CTA has fewer groups than pipelines, left its accumulator unwritten.)
     const bool epi = warp < kEpiWarps;
-    const int en = 32 * warp + lane;  // the epilogue thread's column
+    const int en = 32 * (warp & 3) + lane;  // the thread's column
+    const int cw = warp >> 2;               // the warp's chunk of tokens
+    const bool has_chunk = cw < TOK / kChunk && kChunk * cw < rows;
     bool have = false;
     if (epi) {
       pdl_wait_primary();  // Y may be read or written by the preceding kernel
@@ -635,7 +671,7 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
 #pragma unroll
       for (int m = 0; m < kChunk; ++m) v[m] = 0.f;
       if (!have) return;
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * warp) << 16) + kChunk * c;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + kChunk * c;
       if constexpr (kPipes == 3) {
         uint32_t r0[kChunk], r1[kChunk];
         tmem_ld_32x32b_x16(taddr, r0);
@@ -693,70 +729,57 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       __syncwarp();
       __syncthreads();
     }
+    if (!epi && has_chunk) {
+      // the MMAs completed before the barrier (warps 0-3 saw d_full); after
+      // an abort the chunk stays zero (the result is reported as failed)
+      have = *abort_flag == 0;
+      tc_fence_after();
+      load_chunk(cw, v0);
+    }
     if (cs == 1) {
-      if (epi && n0 + en < p.N) {
-        store_column(p.Y + n0 + en, p.N, v0, rows, p.act);
-        for (int c = 1; c < TOK / kChunk && kChunk * c < rows; ++c) {
-          float v[kChunk];
-          tc_fence_after();
-          load_chunk(c, v);
-          store_column(p.Y + static_cast<size_t>(kChunk * c) * p.N + n0 + en, p.N, v, rows - kChunk * c,
-                       p.act);
-        }
-      }
+      if (has_chunk && n0 + en < p.N)
+        store_column(p.Y + static_cast<size_t>(kChunk * cw) * p.N + n0 + en, p.N, v0,
+                     rows - kChunk * cw, p.act);
     } else {
       // Rank r owns the tile's columns [128 r / cs, 128 (r + 1) / cs).  Each
-      // CTA stages its partials in its (now idle) X stages as one block per
-      // owner, token-major ([token][owner's columns]; a warp's stores of one
-      // token are contiguous), and sends each owner its block with one bulk
-      // copy counted on the owner's part_full, into the owner's weight ring,
-      // after a relaxed cluster rendezvous (every CTA is done with its ring).
-      // Slice q of the receive buffer is rank q's block [token][owned
-      // column]: all 512 threads then add the slices in rank order, one
-      // (token, column) each, consecutive threads on consecutive columns, so
-      // the loads are conflict-free and the Y stores of a row coalesce.
-      // (With one thread per owned column, only ~21 of 128 at a split of 6,
-      // each summing all tokens, the owners' phase was the tail.)  Every rank
-      // sends its blocks even after an abort, so every owner's count completes.
+      // CTA stages its partials in its (now idle) X stages column by column,
+      // TOK + 4 floats per column (a thread's 16 tokens are four 16-byte
+      // stores; with the 16-byte pad a warp's consecutive columns fall on
+      // distinct banks), so that every owner's columns are one contiguous
+      // block, and sends each owner its block with one bulk copy counted on
+      // the owner's part_full, into the owner's weight ring, after a relaxed
+      // cluster rendezvous (every CTA is done with its ring).  Slice q of the
+      // receive buffer is rank q's block: all 512 threads then add the slices
+      // in rank order, four tokens of one column at a time, consecutive
+      // threads on consecutive columns, so the Y stores of a row coalesce.
+      // (Token-major blocks added one float at a time took ~500 cycles per
+      // item at a split of 2: a chain of dependent accesses per thread, with
+      // only 16 warps to hide it.)  Every rank sends its blocks even after an
+      // abort, so every owner's count completes.
+      constexpr int kRow = TOK + 4;  // floats per staged column
       const int cb0 = (rank * kCols) / cs, ncol = ((rank + 1) * kCols) / cs - cb0;
-      const uint32_t stage = smem_addr(smem + C::kOffX);
-      const uint32_t recv = smem_addr(smem + C::kOffW);
+      float* stage = reinterpret_cast<float*>(smem + C::kOffX);
+      const float4* recv = reinterpret_cast<const float4*>(smem + C::kOffW);
       if (threadIdx.x == 0)
-        mbar_arrive_expect_tx(part_full, static_cast<uint32_t>(cs * ncol * TOK * 4));
-      if (epi) {
-        int owner = 0;
-        while (((owner + 1) * kCols) / cs <= en) ++owner;
-        const int ob0 = (owner * kCols) / cs, oncol = ((owner + 1) * kCols) / cs - ob0;
-        // the blocks of the owners before this one hold TOK x ob0 floats
-        const uint32_t blk = stage + static_cast<uint32_t>((ob0 * TOK + (en - ob0)) * 4);
+        mbar_arrive_expect_tx(part_full, static_cast<uint32_t>(cs * ncol * kRow * 4));
+      // (chunks of tokens past M are not staged: the owners never read them)
+      if (has_chunk) {
+        float4* dst = reinterpret_cast<float4*>(stage + en * kRow + kChunk * cw);
 #pragma unroll
-        for (int m = 0; m < kChunk; ++m)
-          asm volatile("st.shared.f32 [%0], %1;" ::"r"(blk + static_cast<uint32_t>(m * oncol * 4)),
-                       "f"(v0[m])
-                       : "memory");
-        for (int c = 1; c < TOK / kChunk; ++c) {
-          float v[kChunk];
-          tc_fence_after();
-          load_chunk(c, v);
-#pragma unroll
-          for (int m = 0; m < kChunk; ++m)
-            asm volatile("st.shared.f32 [%0], %1;" ::"r"(blk + static_cast<uint32_t>(
-                                                           (kChunk * c + m) * oncol * 4)),
-                         "f"(v[m])
-                         : "memory");
-        }
+        for (int i = 0; i < kChunk / 4; ++i)
+          dst[i] = make_float4(v0[4 * i], v0[4 * i + 1], v0[4 * i + 2], v0[4 * i + 3]);
         fence_proxy_async_smem();  // the bulk copies read what these threads wrote
-        named_barrier_sync(1, kEpiWarps * 32);
       }
-      __syncwarp();
+      __syncthreads();
       cluster_arrive_relaxed();
       cluster_wait();  // every CTA of the cluster is done with its weight ring
-      if (epi && en < cs) {
-        const int r = en;  // one thread per destination rank
+      if (threadIdx.x < cs) {
+        const int r = threadIdx.x;  // one thread per destination rank
         const int rb0 = (r * kCols) / cs, rn = ((r + 1) * kCols) / cs - rb0;
-        dsmem_bulk_copy(dsmem_map_addr(recv + static_cast<uint32_t>(rank * TOK * rn * 4), r),
-                        stage + static_cast<uint32_t>(rb0 * TOK * 4),
-                        static_cast<uint32_t>(rn * TOK * 4), dsmem_map(part_full, r));
+        dsmem_bulk_copy(
+            dsmem_map_addr(smem_addr(smem + C::kOffW) + static_cast<uint32_t>(rank * rn * kRow * 4), r),
+            smem_addr(stage) + static_cast<uint32_t>(rb0 * kRow * 4),
+            static_cast<uint32_t>(rn * kRow * 4), dsmem_map(part_full, r));
       }
       if (!mbar_wait_bounded(part_full, 0, p.diag)) {
         // a peer can be late by its own timed-out wait plus its drain
@@ -764,26 +787,58 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
         late.wait_limit_ns = p.diag.wait_limit_ns + 2000000000ull;
         mbar_wait_bounded(part_full, 0, late);
       }
-      auto owner_sum = [&](int it) {
-        const int m = it / ncol, c = it - m * ncol;
-        float acc = 0.f;
-        for (int q = 0; q < cs; ++q)
-          acc += ld_shared_f32(recv + static_cast<uint32_t>(((q * TOK + m) * ncol + c) * 4));
+      // item (column c, token quad t4), c the faster index; a thread's next
+      // item is kThreads further, so (t4, c) advance by a fixed step
+      constexpr int kRow4 = kRow / 4;
+      const int nq = (rows + 3) / 4;  // quads holding a token below M
+      const int dq = kThreads / ncol, dc = kThreads - dq * ncol;
+      auto owner_sum = [&](int t4, int c) {
+        float4 acc = recv[c * kRow4 + t4];
+        for (int q = 1; q < cs; ++q) {
+          const float4 v = recv[(q * ncol + c) * kRow4 + t4];
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
         return acc;
       };
-      const int items = rows * ncol;
+      const int q0 = threadIdx.x / ncol, c0 = threadIdx.x - q0 * ncol;
       if (p.act == 0) {
-        for (int it = threadIdx.x; it < items; it += kThreads) {
-          const int m = it / ncol, c = it - m * ncol;
-          if (n0 + cb0 + c < p.N)
-            p.Y[static_cast<size_t>(m) * p.N + n0 + cb0 + c] = __float2bfloat16_rn(owner_sum(it));
+        for (int t4 = q0, c = c0; t4 < nq;) {
+          if (n0 + cb0 + c < p.N) {
+            const float4 a = owner_sum(t4, c);
+            __nv_bfloat16* y = p.Y + static_cast<size_t>(4 * t4) * p.N + n0 + cb0 + c;
+            const int left = rows - 4 * t4;
+            y[0] = __float2bfloat16_rn(a.x);
+            if (left > 1) y[p.N] = __float2bfloat16_rn(a.y);
+            if (left > 2) y[2 * static_cast<size_t>(p.N)] = __float2bfloat16_rn(a.z);
+            if (left > 3) y[3 * static_cast<size_t>(p.N)] = __float2bfloat16_rn(a.w);
+          }
+          t4 += dq;
+          c += dc;
+          if (c >= ncol) {
+            c -= ncol;
+            ++t4;
+          }
         }
       } else {
-        for (int it = threadIdx.x; it < items; it += kThreads) {
-          const int m = it / ncol, c = it - m * ncol;
-          if (n0 + cb0 + c < p.N)
-            p.Y[static_cast<size_t>(m) * p.N + n0 + cb0 + c] =
-                __float2bfloat16_rn(apply_act(owner_sum(it), 1));
+        for (int t4 = q0, c = c0; t4 < nq;) {
+          if (n0 + cb0 + c < p.N) {
+            const float4 a = owner_sum(t4, c);
+            __nv_bfloat16* y = p.Y + static_cast<size_t>(4 * t4) * p.N + n0 + cb0 + c;
+            const int left = rows - 4 * t4;
+            y[0] = __float2bfloat16_rn(apply_act(a.x, 1));
+            if (left > 1) y[p.N] = __float2bfloat16_rn(apply_act(a.y, 1));
+            if (left > 2) y[2 * static_cast<size_t>(p.N)] = __float2bfloat16_rn(apply_act(a.z, 1));
+            if (left > 3) y[3 * static_cast<size_t>(p.N)] = __float2bfloat16_rn(apply_act(a.w, 1));
+          }
+          t4 += dq;
+          c += dc;
+          if (c >= ncol) {
+            c -= ncol;
+            ++t4;
+          }
         }
       }
       // No CTA leaves while a peer's copy may still read or write its shared
