@@ -112,7 +112,7 @@ struct TokCfg {
   // 16 tokens: a dedicated buffer receives the cluster's partials at any
   // time; 32 and 64: they are received in the idle weight ring, after a
   // rendezvous that says every CTA of the cluster is done with its ring
-  static constexpr int kPartBytes = TOK == 16 ? 9216 : 0;  // >= cs * ceil(128/cs) * 64
+  static constexpr int kPartBytes = TOK == 16 ? 10752 : 0;  // >= cs * ceil(128/cs) * (16 + 4) * 4
 };
 
 template <int BITS, int TOK>
@@ -183,6 +183,23 @@ __device__ __forceinline__ void store_column(__nv_bfloat16* y, int N, const floa
 #pragma unroll
     for (int m = 0; m < kChunk; ++m)
       if (m < rows) y[static_cast<size_t>(m) * N] = __float2bfloat16_rn(apply_act(v[m], 1));
+  }
+}
+
+// Y[m][col] = bf16(act(a.m)) for tokens m = 0..3 (those below `left`) of
+// one column (row stride N), the activation chosen outside the stores.
+__device__ __forceinline__ void store_quad(__nv_bfloat16* y, int N, float4 a, int left, int act) {
+  const size_t n = static_cast<size_t>(N);
+  if (act == 0) {
+    y[0] = __float2bfloat16_rn(a.x);
+    if (left > 1) y[n] = __float2bfloat16_rn(a.y);
+    if (left > 2) y[2 * n] = __float2bfloat16_rn(a.z);
+    if (left > 3) y[3 * n] = __float2bfloat16_rn(a.w);
+  } else {
+    y[0] = __float2bfloat16_rn(apply_act(a.x, 1));
+    if (left > 1) y[n] = __float2bfloat16_rn(apply_act(a.y, 1));
+    if (left > 2) y[2 * n] = __float2bfloat16_rn(apply_act(a.z, 1));
+    if (left > 3) y[3 * n] = __float2bfloat16_rn(apply_act(a.w, 1));
   }
 }
 
@@ -550,14 +567,18 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
     } else {
       // Rank r owns the tile's columns [128 r / cs, 128 (r + 1) / cs).  Each
       // CTA stages its 16 token partials per column in its (now idle) X ring,
-      // column-major, so that every owner's columns are one contiguous block,
-      // and sends each owner its block with one bulk copy counted on the
-      // owner's part_full; slice q of the owner's `part` holds rank q's
-      // block.  Measured against the alternatives: byte-counted 16-byte
+      // column-major in rows of 16 + 4 floats (with the pad a warp's 16-byte
+      // accesses of consecutive columns fall on distinct banks), so that
+      // every owner's columns are one contiguous block, and sends each owner
+      // its block with one bulk copy counted on the owner's part_full; slice
+      // q of the owner's `part` holds rank q's block.  Every thread of the
+      // owner then adds the slices, in rank order, for one (column, 4
+      // tokens).  Measured against the alternatives: byte-counted 16-byte
       // remote stores serialise on the owner's barrier (1.2 us more), and
       // plain remote stores need a release/acquire cluster barrier (0.3 us
       // more).  Every rank sends its blocks even after an abort, so every
       // owner's count completes.
+      constexpr int kRow = TOK + 4;  // floats per staged column
       const int slice = (kCols + cs - 1) / cs;
       const int cb0 = (rank * kCols) / cs, ncol = ((rank + 1) * kCols) / cs - cb0;
       float* stage = reinterpret_cast<float*>(smem + C::kOffX);
@@ -567,9 +588,9 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
         // while rank 0 still works, so their transfer is off the critical
         // path.  Rank 0 adds its own partial and rank 1's, in rank order.
         if (rank == 0 && threadIdx.x == 0)
-          mbar_arrive_expect_tx(part_full, static_cast<uint32_t>(kCols * TOK * 4));
+          mbar_arrive_expect_tx(part_full, static_cast<uint32_t>(kCols * kRow * 4));
         if (epi && rank == 1) {
-          const uint32_t dst = smem_addr(stage + en * TOK);
+          const uint32_t dst = smem_addr(stage + en * kRow);
 #pragma unroll
           for (int i = 0; i < TOK / 4; ++i)
             st_shared_v4(dst + 16 * i, __float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
@@ -578,7 +599,7 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
           named_barrier_sync(1, kEpiWarps * 32);
           if (en == 0)
             dsmem_bulk_copy(dsmem_map(part, 0), smem_addr(stage),
-                            static_cast<uint32_t>(kCols * TOK * 4), dsmem_map(part_full, 0));
+                            static_cast<uint32_t>(kCols * kRow * 4), dsmem_map(part_full, 0));
         }
         if (epi && rank == 0) {
           if (!mbar_wait_bounded(part_full, 0, p.diag)) {
@@ -587,7 +608,7 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
             late.wait_limit_ns = p.diag.wait_limit_ns + 2000000000ull;
             mbar_wait_bounded(part_full, 0, late);
           }
-          const uint32_t src = smem_addr(part + en * TOK);
+          const uint32_t src = smem_addr(part + en * kRow);
 #pragma unroll
           for (int i = 0; i < TOK / 4; ++i) {
             const float4 f = ld_shared_v4_f32(src + 16 * i);
@@ -599,10 +620,10 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
           if (n0 + en < p.N) store_column(p.Y + n0 + en, p.N, v, rows, p.act);
         }
       } else if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(part_full, static_cast<uint32_t>(cs * ncol * TOK * 4));
+        mbar_arrive_expect_tx(part_full, static_cast<uint32_t>(cs * ncol * kRow * 4));
       }
       if (!lead && epi) {
-        const uint32_t dst = smem_addr(stage + en * TOK);
+        const uint32_t dst = smem_addr(stage + en * kRow);
 #pragma unroll
         for (int i = 0; i < TOK / 4; ++i)
           st_shared_v4(dst + 16 * i, __float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
@@ -612,33 +633,32 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
         if (en < cs) {
           const int r = en;  // one thread per destination rank
           const int rb0 = (r * kCols) / cs, rn = ((r + 1) * kCols) / cs - rb0;
-          dsmem_bulk_copy(dsmem_map(part + rank * slice * TOK, r), smem_addr(stage + rb0 * TOK),
-                          static_cast<uint32_t>(rn * TOK * 4), dsmem_map(part_full, r));
+          dsmem_bulk_copy(dsmem_map(part + rank * slice * kRow, r), smem_addr(stage + rb0 * kRow),
+                          static_cast<uint32_t>(rn * kRow * 4), dsmem_map(part_full, r));
         }
-        const int c = en;
-        if (c < ncol) {
-          if (!mbar_wait_bounded(part_full, 0, p.diag)) {
-            // a peer can be late by its own timed-out wait plus its drain
-            KernelDiag late = p.diag;
-            late.wait_limit_ns = p.diag.wait_limit_ns + 2000000000ull;
-            mbar_wait_bounded(part_full, 0, late);
-          }
-          float acc[TOK];
-#pragma unroll
-          for (int m = 0; m < TOK; ++m) acc[m] = 0.f;
-          for (int qq = 0; qq < cs; ++qq) {
-            const uint32_t src = smem_addr(part + (qq * slice + c) * TOK);
-#pragma unroll
-            for (int i = 0; i < TOK / 4; ++i) {
-              const float4 f = ld_shared_v4_f32(src + 16 * i);
-              acc[4 * i] += f.x;
-              acc[4 * i + 1] += f.y;
-              acc[4 * i + 2] += f.z;
-              acc[4 * i + 3] += f.w;
-            }
-          }
-          if (n0 + cb0 + c < p.N) store_column(p.Y + n0 + cb0 + c, p.N, acc, rows, p.act);
+      }
+      // one (column c, 4 tokens t4) per thread, c the faster index: at most
+      // 128 columns x 4 quads = kThreads items
+      const int nq = (rows + 3) / 4;
+      if (!lead && static_cast<int>(threadIdx.x) < ncol * nq) {
+        const int t4 = threadIdx.x / ncol, c = threadIdx.x - t4 * ncol;
+        if (!mbar_wait_bounded(part_full, 0, p.diag)) {
+          // a peer can be late by its own timed-out wait plus its drain
+          KernelDiag late = p.diag;
+          late.wait_limit_ns = p.diag.wait_limit_ns + 2000000000ull;
+          mbar_wait_bounded(part_full, 0, late);
         }
+        float4 a = ld_shared_v4_f32(smem_addr(part + c * kRow) + 16 * t4);
+        for (int qq = 1; qq < cs; ++qq) {
+          const float4 f = ld_shared_v4_f32(smem_addr(part + (qq * slice + c) * kRow) + 16 * t4);
+          a.x += f.x;
+          a.y += f.y;
+          a.z += f.z;
+          a.w += f.w;
+        }
+        if (n0 + cb0 + c < p.N)
+          store_quad(p.Y + static_cast<size_t>(4 * t4) * p.N + n0 + cb0 + c, p.N, a, rows - 4 * t4,
+                     p.act);
       }
       // No CTA leaves while a peer's copy may still read or write its shared
       // memory.  The owners have waited for all of their bytes before
