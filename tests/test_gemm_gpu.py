@@ -522,12 +522,13 @@ def test_stream_shapes(wq, stream_regime, bits, M, K, N):
 
 
 @pytest.mark.parametrize("bits", [4, 8])
-@pytest.mark.parametrize("M", [11, 50])
+@pytest.mark.parametrize("M", [11, 30, 50])
 def test_stream_every_split(wq, stream_regime, bits, M):
     """Each K split 1..8 of the cluster reduction: 16 groups, 3 column tiles
     (the last one half), 11 rows (16-token launches, partials received in a
-    dedicated buffer) or 50 rows (64-token launches, partials received in
-    the weight ring after a cluster rendezvous)."""
+    dedicated buffer), 30 or 50 rows (32- and 64-token launches, partials
+    received in the weight ring after a cluster rendezvous; the last 4-token
+    quad and 16-token chunk part past M)."""
     K, N = 2048, 320
     X, q, s = synth.small_case(M, K, N, bits, seed=67 + bits + M)
     try:

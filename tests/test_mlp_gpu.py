@@ -47,17 +47,19 @@ def test_mlp_pair_workload_shape(wq, act):
 @pytest.mark.parametrize("M,K,N1,N2", [(1, 256, 128, 64), (16, 512, 256, 320),
                                        (40, 512, 256, 320), (130, 1024, 384, 192)])
 def test_mlp_pair_shapes(wq, bits, act, M, K, N1, N2):
-    """M = 1 and 16 (small-M kernel with overlapping launches), 40 and 130
-    (tensor-memory tiled kernel, K split and ragged tiles)."""
+    """M = 1 and 16 (16-token launches of the small-M kernel with
+    overlapping launches), 40 (one 64-token launch of it, K split over a
+    cluster), 130 (tensor-memory tiled kernel, K split and ragged tiles)."""
     _run_pair(wq, M, K, N1, N2, bits, act, seed=M + K + bits)
 
 
-@pytest.mark.parametrize("regime,M", [(1, 40), (2, 16), (0, 33), (4, 33)])
+@pytest.mark.parametrize("regime,M", [(1, 40), (2, 16), (0, 33), (4, 33), (3, 40)])
 def test_mlp_pair_every_family(wq, regime, M):
     """Forced kernel families: the tiled shared-memory kernel and the
     tensor-memory small-M kernel take the activation as a separate pass; the
-    warp-MMA kernel and the overlapping-launch kernel at M = 33 run in two
-    16-row slices plus one row."""
+    warp-MMA kernel runs M = 33 in two 16-row slices plus one row, the
+    overlapping-launch kernel in one 64-token launch; the tensor-memory tiled
+    kernel applies it in its store."""
     try:
         wq.wq_debug_force_regime(regime)
         _run_pair(wq, M, 512, 256, 192, 4, "silu", seed=7 + regime)
