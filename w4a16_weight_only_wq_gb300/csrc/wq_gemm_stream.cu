@@ -766,12 +766,15 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       // TOK + 4 floats per column (a thread's 16 tokens are four 16-byte
       // stores; with the 16-byte pad a warp's consecutive columns fall on
       // distinct banks), so that every owner's columns are one contiguous
-      // block, and sends each owner its block with one bulk copy counted on
-      // the owner's part_full, into the owner's weight ring, after a relaxed
-      // cluster rendezvous (every CTA is done with its ring).  Slice q of the
-      // receive buffer is rank q's block: all 512 threads then add the slices
-      // in rank order, four tokens of one column at a time, consecutive
-      // threads on consecutive columns, so the Y stores of a row coalesce.
+      // block, and sends every other owner its block with one bulk copy
+      // counted on the owner's part_full, into the owner's weight ring, after
+      // a relaxed cluster rendezvous (every CTA is done with its ring).  Slice
+      // q of the receive buffer is rank q's block, and the owner's own block
+      // is read in place from its stage (copying it to itself through the
+      // cluster cost 0.9 us at M = 64, 2560 x 9728): all 512 threads then add
+      // the slices in rank order, four tokens of one column at a time,
+      // consecutive threads on consecutive columns, so the Y stores of a row
+      // coalesce.
       // (Token-major blocks added one float at a time took ~500 cycles per
       // item at a split of 2: a chain of dependent accesses per thread, with
       // only 16 warps to hide it.)  Every rank sends its blocks even after an
@@ -781,7 +784,7 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       float* stage = reinterpret_cast<float*>(smem + C::kOffX);
       const float4* recv = reinterpret_cast<const float4*>(smem + C::kOffW);
       if (threadIdx.x == 0)
-        mbar_arrive_expect_tx(part_full, static_cast<uint32_t>(cs * ncol * kRow * 4));
+        mbar_arrive_expect_tx(part_full, static_cast<uint32_t>((cs - 1) * ncol * kRow * 4));
       // (chunks of tokens past M are not staged: the owners never read them)
       if (has_chunk) {
         float4* dst = reinterpret_cast<float4*>(stage + en * kRow + kChunk * cw);
@@ -793,8 +796,8 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       __syncthreads();
       cluster_arrive_relaxed();
       cluster_wait();  // every CTA of the cluster is done with its weight ring
-      if (threadIdx.x < cs) {
-        const int r = threadIdx.x;  // one thread per destination rank
+      if (threadIdx.x < cs && threadIdx.x != rank) {
+        const int r = threadIdx.x;  // one thread per other rank (its own block is read in place)
         const int rb0 = (r * kCols) / cs, rn = ((r + 1) * kCols) / cs - rb0;
         dsmem_bulk_copy(
             dsmem_map_addr(smem_addr(smem + C::kOffW) + static_cast<uint32_t>(rank * rn * kRow * 4), r),
@@ -812,10 +815,11 @@ gemm_stream_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
       constexpr int kRow4 = kRow / 4;
       const int nq = (rows + 3) / 4;  // quads holding a token below M
       const int dq = kThreads / ncol, dc = kThreads - dq * ncol;
+      const float4* own = reinterpret_cast<const float4*>(stage + cb0 * kRow);
       auto owner_sum = [&](int t4, int c) {
-        float4 acc = recv[c * kRow4 + t4];
+        float4 acc = rank == 0 ? own[c * kRow4 + t4] : recv[c * kRow4 + t4];
         for (int q = 1; q < cs; ++q) {
-          const float4 v = recv[(q * ncol + c) * kRow4 + t4];
+          const float4 v = q == rank ? own[c * kRow4 + t4] : recv[(q * ncol + c) * kRow4 + t4];
           acc.x += v.x;
           acc.y += v.y;
           acc.z += v.z;
