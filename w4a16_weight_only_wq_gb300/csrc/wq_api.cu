@@ -42,8 +42,8 @@ int pick_regime(int64_t M) {
   // At M <= 32, kernel 4 (whose launches overlap) beats kernel 0 on the
   // INT4 decode shapes.  From 33 to 64 rows kernel 4's single launch beats
   // kernel 3 on K x N = 2560 x 9728, 2560 x 2560 and 9728 x 2560, INT4 and
-  // INT8 (M = 64, INT4: 11.2 against 12.1 us, 7.5 against 7.9, 11.9
-  // against 14.6); above 64 rows it needs a second launch and kernel 3 wins.
+  // INT8 (M = 64, INT4: 8.1 against 12.1 us, 5.8 against 7.9, 9.6 against
+  // 14.6); above 64 rows it needs a second launch and kernel 3 wins.
   return M <= kStreamMaxM ? 4 : 3;
 }
 
